@@ -1,0 +1,194 @@
+"""Float64 CPU oracle of the paged q_len=1 decode step (ctypes over oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline leg are the only callers.  Nothing here imports or links the
+CUDA library, and the CUDA library never calls into this package.
+
+All functions take CPU torch tensors: bf16 tensors are read as their bit
+patterns, float64 tensors are used as is.  See oracle.c for what each step
+computes and which passage it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (-O2, OpenMP, strict IEEE) into liboracle.so."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall",
+                        "-fno-fast-math", _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.oracle_bf16_from_double.argtypes = [D]
+            lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = D
+            lib.oracle_num_threads.restype = I
+            lib.oracle_set_num_threads.argtypes = [I]
+            lib.oracle_rope_kv_append.argtypes = [P, P, P, P, P, P, I64, I64, P, I, I, P, P, P,
+                                                  I, I, I, I, I, D]
+            lib.oracle_rope_kv_append.restype = I
+            lib.oracle_decode_attn.argtypes = [P, P, P, I64, I64, P, I, P, P, P, P, D, P, I,
+                                               I, I, I, I, I]
+            lib.oracle_decode_attn.restype = None
+            lib.oracle_decode_attn_split.argtypes = [P, P, P, I64, I64, P, I, P, P, P, D, I,
+                                                     I, I, I, I, I]
+            lib.oracle_decode_attn_split.restype = None
+            lib.oracle_lse_combine.argtypes = [P, P, I, I, P]
+            lib.oracle_lse_combine.restype = D
+            _lib = lib
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    assert t.device.type == "cpu" and t.is_contiguous()
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _i32(t: torch.Tensor) -> torch.Tensor:
+    return t.detach().to("cpu", torch.int32).contiguous()
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(n)
+
+
+def bf16_from_double(x: float) -> int:
+    """bf16 bit pattern nearest to x (ties to even), one rounding step."""
+    return int(_load().oracle_bf16_from_double(float(x)))
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().oracle_bf16_to_double(bits & 0xFFFF))
+
+
+def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, theta,
+                   positions=None, num_pages=None):
+    """RoPE + append on a copy of `pool` ([NP, 2, P, Hkv, D] bf16).
+
+    Returns (q_rot float64 [B, Hq, D], pool_after bf16, n_bad).  Rows with
+    active == 0 keep q_rot = 0 and write nothing.
+    """
+    lib = _load()
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    pool_after = pool.detach().to("cpu").contiguous().clone()
+    NP = pool_after.shape[0]
+    bits = pool_after.view(torch.int16)
+    q_rot = torch.zeros((B, Hq, D), dtype=torch.float64)
+    qb = q.detach().to("cpu").contiguous().view(torch.int16)
+    kb = k_new.detach().to("cpu").contiguous().view(torch.int16)
+    vb = v_new.detach().to("cpu").contiguous().view(torch.int16)
+    pt = _i32(page_table)
+    sl = _i32(seq_lens)
+    ac = _i32(active)
+    pos = _i32(positions) if positions is not None else None
+    page_stride = 2 * P * Hkv * D
+    token_stride = Hkv * D
+    k_ptr = bits.data_ptr()
+    v_ptr = bits.data_ptr() + P * Hkv * D * 2
+    bad = lib.oracle_rope_kv_append(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pos),
+                                    ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                    page_stride, token_stride, _ptr(pt), pt.shape[1],
+                                    NP if num_pages is None else num_pages,
+                                    _ptr(sl), _ptr(ac), _ptr(q_rot), B, Hq, Hkv, D, P, float(theta))
+    return q_rot, pool_after, int(bad)
+
+
+def decode_attn(q_rot, pool, page_table, seq_lens, active, *, P, sm_scale=0.0, rows=None,
+                return_lse=False):
+    """Softmax attention of every (or the listed) row over its paged keys.
+
+    q_rot: float64 [B, Hq, D]; pool: bf16 [NP, 2, P, Hkv, D].
+    Returns float64 out [B, Hq, D] (rows not listed stay zero), and the
+    natural-log lse [B, Hq] if return_lse.
+    """
+    lib = _load()
+    B, Hq, D = q_rot.shape
+    Hkv = pool.shape[3]
+    qr = q_rot.detach().to("cpu", torch.float64).contiguous()
+    bits = pool.detach().to("cpu").contiguous().view(torch.int16)
+    pt = _i32(page_table)
+    sl = _i32(seq_lens)
+    ac = _i32(active)
+    out = torch.zeros((B, Hq, D), dtype=torch.float64)
+    lse = torch.full((B, Hq), float("-inf"), dtype=torch.float64)
+    rw = _i32(torch.as_tensor(rows)) if rows is not None else None
+    lib.oracle_decode_attn(_ptr(qr), ctypes.c_void_p(bits.data_ptr()),
+                           ctypes.c_void_p(bits.data_ptr() + P * Hkv * D * 2),
+                           2 * P * Hkv * D, Hkv * D, _ptr(pt), pt.shape[1], _ptr(sl), _ptr(ac),
+                           _ptr(out), _ptr(lse), float(sm_scale), _ptr(rw),
+                           0 if rw is None else rw.numel(), B, Hq, Hkv, D, P)
+    return (out, lse) if return_lse else out
+
+
+def decode_attn_split(q_rot, pool, page_table, seq_lens, active, *, P, n_splits, sm_scale=0.0):
+    """The same attention as decode_attn, as n_splits segments merged by LSE."""
+    lib = _load()
+    B, Hq, D = q_rot.shape
+    Hkv = pool.shape[3]
+    qr = q_rot.detach().to("cpu", torch.float64).contiguous()
+    bits = pool.detach().to("cpu").contiguous().view(torch.int16)
+    pt = _i32(page_table)
+    sl = _i32(seq_lens)
+    ac = _i32(active)
+    out = torch.zeros((B, Hq, D), dtype=torch.float64)
+    lib.oracle_decode_attn_split(_ptr(qr), ctypes.c_void_p(bits.data_ptr()),
+                                 ctypes.c_void_p(bits.data_ptr() + P * Hkv * D * 2),
+                                 2 * P * Hkv * D, Hkv * D, _ptr(pt), pt.shape[1], _ptr(sl),
+                                 _ptr(ac), _ptr(out), float(sm_scale), int(n_splits),
+                                 B, Hq, Hkv, D, P)
+    return out
+
+
+def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor):
+    """Merge S partials of one head: o_parts float64 [S, D], lse_parts [S]."""
+    lib = _load()
+    op = o_parts.detach().to("cpu", torch.float64).contiguous()
+    lp = lse_parts.detach().to("cpu", torch.float64).contiguous()
+    S, D = op.shape
+    o = torch.zeros(D, dtype=torch.float64)
+    lse = lib.oracle_lse_combine(_ptr(op), _ptr(lp), S, D, _ptr(o))
+    return o, float(lse)
+
+
+def reference_step(inp, positions=None, rows=None, sm_scale=0.0):
+    """Whole step on one layer's inputs (any object with the DecodeInputs fields).
+
+    Returns dict(q_rot, pool_after, out, n_bad): RoPE + append, then attention
+    over the appended cache.
+    """
+    q_rot, pool_after, bad = rope_kv_append(inp.q, inp.k_new, inp.v_new, inp.pool, inp.page_table,
+                                            inp.seq_lens, inp.active, P=inp.P, theta=inp.theta,
+                                            positions=positions, num_pages=inp.num_pages)
+    out = decode_attn(q_rot, pool_after, inp.page_table, inp.seq_lens, inp.active, P=inp.P,
+                      rows=rows, sm_scale=sm_scale)
+    return {"q_rot": q_rot, "pool_after": pool_after, "out": out, "n_bad": bad}
