@@ -1,0 +1,179 @@
+/*
+ * vh.h -- C interface of the GB300 paged q_len=1 decode-attention library.
+ *
+ * One decode step of a Talker/LM layer for a batch of requests, in three
+ * calls on the caller's CUDA stream:
+ *
+ *   vh_rope_kv_append     RoPE on the new q and k, then append of k and v
+ *                         into each request's current KV page;
+ *   vh_paged_decode_attn  single-token GQA attention of every request over
+ *                         its pages, split across CTAs where a request is
+ *                         long, writing finished rows and partial results;
+ *   vh_decode_combine     log-sum-exp merge of the partial results.
+ *
+ * Sources of the operation (pages this library was written from):
+ *   - "Engineering TTS inference in vLLM-Omni" (vLLM blog), Fish Speech S2 Pro,
+ *     "model-specific attention kernel": decode-only attention with q_len = 1,
+ *     bf16, head_dim 128, block size 16, GQA where one kv head serves its
+ *     group of q heads; long sequences are split into segments whose partial
+ *     max / sum / accumulator are merged by the online-softmax recurrence;
+ *     the short/long choice is made without a device-to-host sync.
+ *   - same page, Qwen3-TTS section 4 "numerical precision": RoPE cos/sin and
+ *     attention are kept in fp32.
+ *   - "Adding a Model" (vox-serve docs), "How a program runs": one row per
+ *     request, static shapes, no host sync, inputs in device buffers; padding
+ *     entries (active == 0) point at the dummy KV page 0, compute garbage
+ *     that is ignored and must never write another request's state.
+ *   - same page, section "1. The model code": keys and values are written
+ *     into the paged cache, then attention runs over it; cache layout
+ *     [num_layers, num_pages, 2, page_size, num_kv_heads, head_dim].
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing, frees nothing and keeps no state between calls
+ *     other than per-device launch settings it caches on first use.
+ *   - bf16 values are passed as uint16_t bit patterns (vh_bf16).
+ *   - Strides are in ELEMENTS.  One layer's cache is reached through
+ *     k_cache / v_cache plus page_stride (elements between pages) and
+ *     token_stride (elements between token slots of a page); within a slot
+ *     the heads are contiguous, head h at offset h*D.  For the layout
+ *     [NP, 2, P, Hkv, D]: v_cache = k_cache + P*Hkv*D, page_stride =
+ *     2*P*Hkv*D, token_stride = Hkv*D.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Every call checks its scalar arguments and pointer alignment on the
+ *     host, launches asynchronously and never synchronises or reads device
+ *     memory on the host, so a sequence of calls can be captured in a CUDA
+ *     graph.  Make the first call of each function on a device before any
+ *     capture: it sets per-kernel launch attributes once.
+ *   - Return value: VH_OK (0) or a negative VH_E* status; a negative status
+ *     means nothing was launched, except VH_ECUDA, which reports the CUDA
+ *     error raised by the launch itself.
+ *   - Data errors found on the device never trap: the offending row is
+ *     skipped (or clamped, see below) and a VH_ERR_* bit is ORed into
+ *     *err_flag when err_flag is not NULL.  The caller reads it later.
+ *
+ * Shapes: B rows, Hq q heads, Hkv kv heads (Hq % Hkv == 0, G = Hq / Hkv
+ * in {1, 2, 4, 8}), head dim D in {64, 128}, page size P a multiple of 16
+ * (16 <= P <= 1024), 1 <= B <= 65535.  seq_len counts the token being
+ * appended: row b attends over logical slots 0 .. seq_lens[b]-1, and the new
+ * token is slot seq_lens[b]-1, i.e. page page_table[b][(L-1)/P], offset
+ * (L-1) % P.  page_table is int32 [B][max_pages_per_seq], row-major.
+ */
+#ifndef VH_H
+#define VH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t vh_bf16;
+
+/* return codes */
+#define VH_OK 0
+#define VH_EINVAL (-1)      /* bad shape, NULL pointer or out-of-range scalar */
+#define VH_EALIGN (-2)      /* a pointer or stride is not 16-byte aligned */
+#define VH_EWORKSPACE (-3)  /* workspace NULL or smaller than required */
+#define VH_ECUDA (-4)       /* CUDA reported an error at launch */
+#define VH_ENODEV (-5)      /* no usable sm_103 device is current */
+
+/* device-side data-error bits, ORed into *err_flag */
+#define VH_ERR_SEQLEN 1     /* active row with seq_len outside [1, max_pages_per_seq*P]: row skipped */
+#define VH_ERR_PAGE 2       /* page id outside [0, num_pages): the append or the page read is skipped */
+#define VH_ERR_POS 4        /* position outside [0, max_pos): the row is skipped by the append */
+#define VH_ERR_TIMEOUT 8    /* an internal pipeline wait ran out of time: the CTA gave up */
+
+/* Fill the RoPE table used by vh_rope_kv_append.
+ * cos_sin: float [max_pos][D]; row p holds cos(p * f_i) in columns 0..D/2-1
+ * and sin(p * f_i) in columns D/2..D-1, f_i = theta^(-2i/D).  Angles and
+ * cos/sin are evaluated in double and stored as float (the pages keep RoPE
+ * cos/sin in fp32 for alignment with the reference model).  Init-time call.
+ * Errors: VH_EINVAL if cos_sin is NULL, max_pos < 1, D not in {64, 128} or
+ * theta <= 0; VH_EALIGN if cos_sin is not 16-byte aligned. */
+int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void* stream);
+
+/* RoPE + KV append, one CTA per row.
+ * q      bf16 [B][Hq][D]   new queries (contiguous)
+ * k_new  bf16 [B][Hkv][D]  new keys, rotated here before they are stored
+ * v_new  bf16 [B][Hkv][D]  new values, stored bit for bit
+ * cos_sin float [max_pos][D] from vh_rope_table
+ * positions int32 [B] or NULL; NULL means position = seq_lens[b] - 1
+ * k_cache, v_cache, page_stride, token_stride: the layer's paged cache
+ * num_pages: pages in the pool, used only to bounds-check page ids (> 0)
+ * page_table int32 [B][max_pages_per_seq]; seq_lens, active int32 [B]
+ * q_rot  float [B][Hq][D] out: rotated q in fp32 (rows with active == 0
+ *        are not written)
+ * err_flag int32* or NULL
+ * For every active row: q_rot = rope(q); the cache slot of token
+ * seq_len-1 receives bf16_rne(rope(k_new)) and v_new.  Rotation is computed
+ * in fp32 ("rotate half": element i pairs with i + D/2).  Rows with
+ * active == 0 write nothing.  Precondition (not checked): live rows own
+ * disjoint append slots.
+ * Errors: VH_EINVAL (NULL pointer other than positions/err_flag, bad shape,
+ * max_pos < 1, num_pages < 1, max_pages_per_seq < 1), VH_EALIGN (a pointer
+ * or a stride not 16-byte aligned), VH_ECUDA. */
+int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+                      const float* cos_sin, int max_pos, const int32_t* positions,
+                      vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride,
+                      int64_t token_stride, int num_pages,
+                      const int32_t* page_table, int max_pages_per_seq,
+                      const int32_t* seq_lens, const int32_t* active,
+                      float* q_rot, int32_t* err_flag,
+                      int B, int Hq, int Hkv, int D, int page_size, void* stream);
+
+/* Number of CTAs per kv-head group that vh_paged_decode_attn launches on the
+ * current device when num_ctas == 0 (a multiple of the SM count).  Returns a
+ * negative VH_E* status on bad shapes or when no device is usable. */
+int vh_decode_num_ctas(int B, int Hq, int Hkv, int D, int page_size);
+
+/* Bytes of workspace vh_paged_decode_attn / vh_decode_combine need for this
+ * shape and CTA count (num_ctas == 0: the automatic count on the current
+ * device).  Returns 0 on bad arguments. */
+size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int num_ctas);
+
+/* Paged GQA decode attention.
+ * q_rot float [B][Hq][D] (from vh_rope_kv_append); cache as above.
+ * out bf16 [B][Hq][D]: rows whose keys one CTA covered entirely are written
+ *     here directly; rows with active == 0 (or flagged VH_ERR_SEQLEN) are
+ *     written as zeros; rows split across CTAs are finished by
+ *     vh_decode_combine.
+ * sm_scale: softmax scale; <= 0 means 1/sqrt(D).
+ * num_ctas: CTAs per kv-head group, 0 = automatic.  The work is the list of
+ *     16-token tiles of all active rows in row order; on the device each CTA
+ *     takes an equal contiguous share of that list (no host sync), so a row
+ *     is split exactly where its tiles straddle two CTAs.
+ * workspace / workspace_bytes: caller-owned device scratch of at least
+ *     vh_decode_workspace_bytes(...) bytes, 256-byte aligned; it holds the
+ *     per-row split plan and the fp32 partial results.  No initialisation
+ *     is needed.  Calls that overlap on the device must use distinct
+ *     workspaces.
+ * Softmax in fp32 with a running max, exp2 with log2(e) folded into the
+ * scale; keys beyond seq_len (tail of the last page) are never used.
+ * Errors: VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
+int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
+                         int64_t page_stride, int64_t token_stride, int num_pages,
+                         const int32_t* page_table, int max_pages_per_seq,
+                         const int32_t* seq_lens, const int32_t* active,
+                         vh_bf16* out, float sm_scale, int num_ctas,
+                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                         int B, int Hq, int Hkv, int D, int page_size, void* stream);
+
+/* Merge the partial results of split rows into out (bf16 [B][Hq][D]):
+ * M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s (lse in
+ * base 2).  Rows that were not split are left as vh_paged_decode_attn wrote
+ * them.  Must run after vh_paged_decode_attn on the same stream with the same
+ * workspace and the same shape / num_ctas arguments.
+ * Errors: VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
+int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
+                      int B, int Hq, int Hkv, int D, int page_size, void* stream);
+
+/* Static text for a return code. */
+const char* vh_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VH_H */

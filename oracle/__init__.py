@@ -47,7 +47,7 @@ def _load():
             lib.oracle_bf16_to_double.restype = D
             lib.oracle_num_threads.restype = I
             lib.oracle_set_num_threads.argtypes = [I]
-            lib.oracle_rope_kv_append.argtypes = [P, P, P, P, P, P, I64, I64, P, I, I, P, P, P,
+            lib.oracle_rope_kv_append.argtypes = [P, P, P, P, P, P, I64, I64, P, I, I, P, P, P, P,
                                                   I, I, I, I, I, D]
             lib.oracle_rope_kv_append.restype = I
             lib.oracle_decode_attn.argtypes = [P, P, P, I64, I64, P, I, P, P, P, P, D, P, I,
@@ -91,19 +91,26 @@ def bf16_to_double(bits: int) -> float:
 
 
 def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, theta,
-                   positions=None, num_pages=None):
-    """RoPE + append on a copy of `pool` ([NP, 2, P, Hkv, D] bf16).
+                   positions=None, num_pages=None, return_k_rot=False, in_place=False):
+    """RoPE + append on a copy of `pool` ([NP, 2, P, Hkv, D] bf16), or on `pool`
+    itself when in_place (a contiguous CPU tensor).
 
-    Returns (q_rot float64 [B, Hq, D], pool_after bf16, n_bad).  Rows with
+    Returns (q_rot float64 [B, Hq, D], pool_after bf16, n_bad), plus the
+    unrounded rotated keys float64 [B, Hkv, D] if return_k_rot.  Rows with
     active == 0 keep q_rot = 0 and write nothing.
     """
     lib = _load()
     B, Hq, D = q.shape
     Hkv = k_new.shape[1]
-    pool_after = pool.detach().to("cpu").contiguous().clone()
+    if in_place:
+        assert pool.device.type == "cpu" and pool.is_contiguous()
+        pool_after = pool
+    else:
+        pool_after = pool.detach().to("cpu").contiguous().clone()
     NP = pool_after.shape[0]
     bits = pool_after.view(torch.int16)
     q_rot = torch.zeros((B, Hq, D), dtype=torch.float64)
+    k_rot = torch.zeros((B, Hkv, D), dtype=torch.float64)
     qb = q.detach().to("cpu").contiguous().view(torch.int16)
     kb = k_new.detach().to("cpu").contiguous().view(torch.int16)
     vb = v_new.detach().to("cpu").contiguous().view(torch.int16)
@@ -119,7 +126,10 @@ def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, th
                                     ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                                     page_stride, token_stride, _ptr(pt), pt.shape[1],
                                     NP if num_pages is None else num_pages,
-                                    _ptr(sl), _ptr(ac), _ptr(q_rot), B, Hq, Hkv, D, P, float(theta))
+                                    _ptr(sl), _ptr(ac), _ptr(q_rot), _ptr(k_rot),
+                                    B, Hq, Hkv, D, P, float(theta))
+    if return_k_rot:
+        return q_rot, pool_after, int(bad), k_rot
     return q_rot, pool_after, int(bad)
 
 
@@ -183,12 +193,14 @@ def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor):
 def reference_step(inp, positions=None, rows=None, sm_scale=0.0):
     """Whole step on one layer's inputs (any object with the DecodeInputs fields).
 
-    Returns dict(q_rot, pool_after, out, n_bad): RoPE + append, then attention
-    over the appended cache.
+    Returns dict(q_rot, k_rot, pool_after, out, n_bad): RoPE + append, then
+    attention over the appended cache.  k_rot is the rotated key before its
+    bf16 rounding.
     """
-    q_rot, pool_after, bad = rope_kv_append(inp.q, inp.k_new, inp.v_new, inp.pool, inp.page_table,
-                                            inp.seq_lens, inp.active, P=inp.P, theta=inp.theta,
-                                            positions=positions, num_pages=inp.num_pages)
+    q_rot, pool_after, bad, k_rot = rope_kv_append(inp.q, inp.k_new, inp.v_new, inp.pool,
+                                                   inp.page_table, inp.seq_lens, inp.active,
+                                                   P=inp.P, theta=inp.theta, positions=positions,
+                                                   num_pages=inp.num_pages, return_k_rot=True)
     out = decode_attn(q_rot, pool_after, inp.page_table, inp.seq_lens, inp.active, P=inp.P,
                       rows=rows, sm_scale=sm_scale)
-    return {"q_rot": q_rot, "pool_after": pool_after, "out": out, "n_bad": bad}
+    return {"q_rot": q_rot, "k_rot": k_rot, "pool_after": pool_after, "out": out, "n_bad": bad}

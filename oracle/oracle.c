@@ -122,6 +122,8 @@ static void rope_rotate(double* x, int D, double pos, double theta) {
  * q, k_new, v_new: bf16 [B][Hq][D], [B][Hkv][D], [B][Hkv][D].
  * positions: NULL means seq_len - 1.
  * q_rot: float64 [B][Hq][D] out; rows with active == 0 are left untouched.
+ * k_rot: float64 [B][Hkv][D] out or NULL: the rotated key before its bf16
+ *        rounding (rows that are skipped are left untouched).
  * Returns the number of active rows whose slot could not be placed
  * (seq_len outside [1, MPS*P] or a page id outside [0, num_pages)); those
  * rows write nothing.
@@ -132,7 +134,7 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
                           int64_t page_stride, int64_t token_stride,
                           const int32_t* page_table, int max_pages_per_seq, int num_pages,
                           const int32_t* seq_lens, const int32_t* active,
-                          double* q_rot,
+                          double* q_rot, double* k_rot,
                           int B, int Hq, int Hkv, int D, int P, double theta) {
     int bad = 0;
     double* tmp = (double*)malloc(sizeof(double) * (size_t)D);
@@ -156,6 +158,7 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
             const uint16_t* vs = v_new + ((size_t)b * Hkv + h) * D;
             for (int d = 0; d < D; ++d) tmp[d] = bf16_to_double(ks[d]);
             rope_rotate(tmp, D, pos, theta);
+            if (k_rot) memcpy(k_rot + ((size_t)b * Hkv + h) * D, tmp, sizeof(double) * (size_t)D);
             uint16_t* kd = k_cache + (int64_t)page * page_stride + (int64_t)off * token_stride + (int64_t)h * D;
             uint16_t* vd = v_cache + (int64_t)page * page_stride + (int64_t)off * token_stride + (int64_t)h * D;
             for (int d = 0; d < D; ++d) {

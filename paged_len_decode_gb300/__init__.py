@@ -1,0 +1,193 @@
+"""Thin Python binding of libvh.so (the C interface in include/vh.h).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of libvh.so.  Tensors are torch CUDA tensors; the binding checks
+dtypes, contiguity and devices, reads shapes and strides, and passes raw
+pointers plus the current torch stream.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+
+Functions mirror the C entry points by name:
+    vh_rope_table, vh_rope_kv_append, vh_decode_num_ctas,
+    vh_decode_workspace_bytes, vh_paged_decode_attn, vh_decode_combine,
+    vh_status_string
+plus `decode_step`, which issues the three calls of one decode step.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvh.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
+
+VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3, -4, -5
+VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
+
+
+class VHError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({vh_status_string(status)})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first (paged_len_decode_gb300.build.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, F, D, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                           ctypes.c_double, ctypes.c_size_t)
+    lib.vh_status_string.argtypes = [I]
+    lib.vh_status_string.restype = ctypes.c_char_p
+    lib.vh_rope_table.argtypes = [P, I, I, D, P]
+    lib.vh_rope_table.restype = I
+    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, I64, I64, I, P, I, P, P, P, P,
+                                      I, I, I, I, I, P]
+    lib.vh_rope_kv_append.restype = I
+    lib.vh_decode_num_ctas.argtypes = [I, I, I, I, I]
+    lib.vh_decode_num_ctas.restype = I
+    lib.vh_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.vh_decode_workspace_bytes.restype = SZ
+    lib.vh_paged_decode_attn.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P,
+                                         I, I, I, I, I, P]
+    lib.vh_paged_decode_attn.restype = I
+    lib.vh_decode_combine.argtypes = [P, SZ, P, I, I, I, I, I, I, P]
+    lib.vh_decode_combine.restype = I
+    return lib
+
+
+lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/vh.h declares."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(vh_\w+)\s*\(", text, flags=re.M)))
+
+
+def vh_status_string(status: int) -> str:
+    return lib.vh_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != VH_OK:
+        raise VHError(status, where)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> ctypes.c_void_p | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _contig(t: torch.Tensor, dtype, name: str) -> ctypes.c_void_p:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return _ptr(t, dtype, name)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _cache_view(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    """Pointers and element strides of a [NP, P, Hkv, D] paged cache view."""
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache / v_cache must be [NP, P, Hkv, D] views with equal strides")
+    if k_cache.stride(3) != 1 or k_cache.stride(2) != k_cache.shape[3]:
+        raise ValueError("the heads of one token slot must be contiguous ([.., Hkv, D] dense)")
+    NP, P, Hkv, D = k_cache.shape
+    return (_ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+            k_cache.stride(0), k_cache.stride(1), NP, P, Hkv, D)
+
+
+def vh_rope_table(cos_sin: torch.Tensor, theta: float = 10000.0, stream=None) -> torch.Tensor:
+    """Fill cos_sin (float32 [max_pos, D]) with the RoPE table."""
+    max_pos, D = cos_sin.shape
+    _check(lib.vh_rope_table(_contig(cos_sin, torch.float32, "cos_sin"), max_pos, D, float(theta),
+                             _stream(stream)), "vh_rope_table")
+    return cos_sin
+
+
+def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
+                      q_rot, positions=None, err_flag=None, stream=None) -> None:
+    B, Hq, D = q.shape
+    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or q_rot.shape != (B, Hq, D):
+        raise ValueError("shape mismatch between q, k_new, v_new, q_rot and the cache")
+    _check(lib.vh_rope_kv_append(
+        _contig(q, torch.bfloat16, "q"), _contig(k_new, torch.bfloat16, "k_new"),
+        _contig(v_new, torch.bfloat16, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
+        cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
+        kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
+        _contig(q_rot, torch.float32, "q_rot"),
+        None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
+        B, Hq, Hkv, D, P, _stream(stream)), "vh_rope_kv_append")
+
+
+def vh_decode_num_ctas(B: int, Hq: int, Hkv: int, D: int, page_size: int) -> int:
+    n = lib.vh_decode_num_ctas(B, Hq, Hkv, D, page_size)
+    if n < 0:
+        raise VHError(n, "vh_decode_num_ctas")
+    return n
+
+
+def vh_decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas: int = 0) -> int:
+    n = lib.vh_decode_workspace_bytes(B, Hq, Hkv, D, page_size, num_ctas)
+    if n == 0:
+        raise VHError(VH_EINVAL, "vh_decode_workspace_bytes")
+    return n
+
+
+def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
+                         sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None, stream=None) -> None:
+    B, Hq, D = q_rot.shape
+    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    if Dc != D or out.shape != (B, Hq, D):
+        raise ValueError("shape mismatch between q_rot, out and the cache")
+    _check(lib.vh_paged_decode_attn(
+        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, NP,
+        _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
+        _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
+        _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
+        B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn")
+
+
+def vh_decode_combine(workspace, out, Hkv: int, page_size: int, num_ctas: int = 0, stream=None) -> None:
+    B, Hq, D = out.shape
+    _check(lib.vh_decode_combine(
+        _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _contig(out, torch.bfloat16, "out"), int(num_ctas), B, Hq, Hkv, D, page_size,
+        _stream(stream)), "vh_decode_combine")
+
+
+def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas: int = 0,
+                    device=None) -> torch.Tensor:
+    """Device scratch for vh_paged_decode_attn / vh_decode_combine (torch allocation)."""
+    n = vh_decode_workspace_bytes(B, Hq, Hkv, D, page_size, num_ctas)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_step(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, q_rot,
+                out, workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0,
+                err_flag=None, stream=None) -> torch.Tensor:
+    """One decode step of one layer: RoPE + append, attention, combine."""
+    vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
+                      q_rot, positions=positions, err_flag=err_flag, stream=stream)
+    vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
+                         sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, stream=stream)
+    vh_decode_combine(workspace, out, k_cache.shape[2], k_cache.shape[1], num_ctas=num_ctas,
+                      stream=stream)
+    return out

@@ -1,0 +1,124 @@
+// rope_append.cu -- RoPE table and the fused RoPE + KV-append kernel.
+//
+// Operation ("Adding a Model", vox-serve docs, section "1. The model code":
+// keys and values are written into the paged cache before attention; RoPE is
+// applied to q/k first; "Engineering TTS inference in vLLM-Omni", Qwen3-TTS
+// section 4: RoPE cos/sin in fp32): for each active row b at position
+// pos = seq_len - 1 (or positions[b]),
+//   q_rot[b]            = rope(q[b], pos)                 (fp32 out)
+//   cache slot (L - 1)  = bf16_rne(rope(k_new[b], pos)), v_new[b]
+// Rotation pairs element i with i + D/2, angle pos * theta^(-2i/D).
+//
+// The work is tiny (a few hundred KB per call) and latency-bound: one CTA per
+// row, 16-byte vector loads and stores, cos/sin read from a table built once
+// in double precision so no per-call transcendental is evaluated.
+#include "vh_common.cuh"
+#include "vh_kernels.h"
+
+namespace vh {
+
+__global__ void rope_table_kernel(float* __restrict__ cos_sin, int max_pos, int D, double theta) {
+  const int half = D / 2;
+  const long long n = static_cast<long long>(max_pos) * half;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(idx / half);
+    const int i = static_cast<int>(idx % half);
+    const double f = pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(D));
+    const double a = static_cast<double>(p) * f;
+    double s, c;
+    sincos(a, &s, &c);
+    cos_sin[static_cast<long long>(p) * D + i] = static_cast<float>(c);
+    cos_sin[static_cast<long long>(p) * D + half + i] = static_cast<float>(s);
+  }
+}
+
+// One CTA per row.  Work units: each thread rotates 4 consecutive pairs
+// (elements i..i+3 and i+D/2..i+D/2+3) of one head; heads 0..Hq-1 are q heads
+// (written to q_rot), heads Hq..Hq+Hkv-1 are the new k (written to the cache).
+// V is copied 16 bytes per thread.
+__global__ void __launch_bounds__(128) rope_kv_append_kernel(RopeAppendParams p) {
+  const int b = blockIdx.x;
+  if (!p.active[b]) return;
+  const int L = p.seq_lens[b];
+  const int max_len = p.max_pages_per_seq * p.P;
+  if (L < 1 || L > max_len) {
+    if (threadIdx.x == 0) flag_error(p.err_flag, VH_ERR_SEQLEN);
+    return;
+  }
+  const int pos = p.positions ? p.positions[b] : L - 1;
+  if (pos < 0 || pos >= p.max_pos) {
+    if (threadIdx.x == 0) flag_error(p.err_flag, VH_ERR_POS);
+    return;
+  }
+  const int slot = L - 1;
+  const int page = p.page_table[static_cast<long long>(b) * p.max_pages_per_seq + slot / p.P];
+  const bool page_ok = page >= 0 && page < p.num_pages;
+  if (!page_ok && threadIdx.x == 0) flag_error(p.err_flag, VH_ERR_PAGE);
+  const long long slot_off = static_cast<long long>(page) * p.page_stride +
+                             static_cast<long long>(slot % p.P) * p.token_stride;
+
+  const int D = p.D, half = D / 2;
+  const int quads = half / 4;                  // 4-pair units per head
+  const int heads = p.Hq + (page_ok ? p.Hkv : 0);
+  const float* cs = p.cos_sin + static_cast<long long>(pos) * D;
+
+  for (int u = threadIdx.x; u < heads * quads; u += blockDim.x) {
+    const int h = u / quads;
+    const int i = (u % quads) * 4;
+    const float4 c = *reinterpret_cast<const float4*>(cs + i);
+    const float4 s = *reinterpret_cast<const float4*>(cs + half + i);
+    const uint16_t* src;
+    if (h < p.Hq)
+      src = p.q + (static_cast<long long>(b) * p.Hq + h) * D;
+    else
+      src = p.k_new + (static_cast<long long>(b) * p.Hkv + (h - p.Hq)) * D;
+    const uint2 lo = *reinterpret_cast<const uint2*>(src + i);
+    const uint2 hi = *reinterpret_cast<const uint2*>(src + half + i);
+    const float2 x01 = bf16x2_to_float2(lo.x), x23 = bf16x2_to_float2(lo.y);
+    const float2 y01 = bf16x2_to_float2(hi.x), y23 = bf16x2_to_float2(hi.y);
+    const float x[4] = {x01.x, x01.y, x23.x, x23.y};
+    const float y[4] = {y01.x, y01.y, y23.x, y23.y};
+    const float cc[4] = {c.x, c.y, c.z, c.w};
+    const float ss[4] = {s.x, s.y, s.z, s.w};
+    float rx[4], ry[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      rx[k] = x[k] * cc[k] - y[k] * ss[k];
+      ry[k] = y[k] * cc[k] + x[k] * ss[k];
+    }
+    if (h < p.Hq) {
+      float* dst = p.q_rot + (static_cast<long long>(b) * p.Hq + h) * D;
+      *reinterpret_cast<float4*>(dst + i) = make_float4(rx[0], rx[1], rx[2], rx[3]);
+      *reinterpret_cast<float4*>(dst + half + i) = make_float4(ry[0], ry[1], ry[2], ry[3]);
+    } else {
+      uint16_t* dst = p.k_cache + slot_off + static_cast<long long>(h - p.Hq) * D;
+      *reinterpret_cast<uint2*>(dst + i) = make_uint2(pack_bf16x2(rx[0], rx[1]), pack_bf16x2(rx[2], rx[3]));
+      *reinterpret_cast<uint2*>(dst + half + i) =
+          make_uint2(pack_bf16x2(ry[0], ry[1]), pack_bf16x2(ry[2], ry[3]));
+    }
+  }
+  if (!page_ok) return;
+  // V: Hkv*D bf16 contiguous in v_new and in the slot; 8 elements per thread.
+  const int nvec = p.Hkv * D / 8;
+  const uint4* vsrc = reinterpret_cast<const uint4*>(p.v_new + static_cast<long long>(b) * p.Hkv * D);
+  for (int u = threadIdx.x; u < nvec; u += blockDim.x) {
+    const int h = (u * 8) / D, d = (u * 8) % D;
+    *reinterpret_cast<uint4*>(p.v_cache + slot_off + static_cast<long long>(h) * D + d) = vsrc[u];
+  }
+}
+
+cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, cudaStream_t stream) {
+  const long long n = static_cast<long long>(max_pos) * (D / 2);
+  int blocks = static_cast<int>((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  rope_table_kernel<<<blocks, 256, 0, stream>>>(cos_sin, max_pos, D, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream) {
+  rope_kv_append_kernel<<<p.B, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace vh

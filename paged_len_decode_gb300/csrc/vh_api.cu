@@ -1,0 +1,334 @@
+// vh_api.cu -- host side of the C interface declared in include/vh.h.
+//
+// Every entry point validates host scalars and pointer alignment, derives the
+// launch plan from the shape and the current device, and launches on the
+// caller's stream.  Nothing here synchronises, allocates or reads device
+// memory, so the calls can be captured into a CUDA graph (after the first
+// call on a device, which sets kernel attributes).
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/vh.h"
+#include "vh_kernels.h"
+
+namespace {
+
+using vh::AttnParams;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxStages = 8;
+constexpr int kMinTilesPerCta = 4;
+
+struct DeviceInfo {
+  std::once_flag once;
+  bool ok = false;
+  int sm_count = 0;
+  int smem_optin = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  DeviceInfo& d = g_dev[dev];
+  std::call_once(d.once, [&]() {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    // The kernels are built for sm_103a only.
+    if (major != 10 || minor != 3) return;
+    for (int D : {64, 128})
+      for (int G : {1, 2, 4, 8})
+        if (vh::prepare_decode_attn(D, G, d.smem_optin) != cudaSuccess) {
+          cudaGetLastError();
+          return;
+        }
+    d.ok = true;
+  });
+  return d.ok ? &d : nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_gqa(int Hq, int Hkv) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return false;
+  const int G = Hq / Hkv;
+  return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+bool valid_shape(int B, int Hq, int Hkv, int D, int P) {
+  return B >= 1 && B <= 65535 && valid_gqa(Hq, Hkv) && (D == 64 || D == 128) && P >= 16 &&
+         P <= 1024 && P % 16 == 0 && Hkv <= 1024;
+}
+
+// kv heads per CTA: the largest divisor of Hkv with Hc * D <= 1024 and Hc <= 8.
+int choose_hc(int Hkv, int D) {
+  int hc = std::min({Hkv, 1024 / D, 8});
+  while (Hkv % hc != 0) --hc;
+  return hc;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return dflt;
+  return std::atoi(s);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory plan; returns false if the shape cannot fit two stages.
+bool plan_attn(AttnParams& p, const DeviceInfo& dev) {
+  p.G = p.Hq / p.Hkv;
+  p.Hc = choose_hc(p.Hkv, p.D);
+  p.groups = p.Hkv / p.Hc;
+  p.row_copy_bytes = p.Hc * p.D * 2;
+  p.k_row_bytes = p.row_copy_bytes + 32;
+  p.v_row_bytes = p.row_copy_bytes;
+  p.stage_bytes = static_cast<int>(align_up(16 * (p.k_row_bytes + p.v_row_bytes), 128));
+  const int ksplit = 256 / p.D;
+  const size_t q_bytes = static_cast<size_t>(p.Hc) * p.G * p.D * 4;
+  const size_t p_bytes = static_cast<size_t>(p.Hc) * (16 * p.G + ksplit * 4) * 4;
+  const size_t cum_bytes = align_up(4 * (static_cast<size_t>(p.B) + 1), 16);
+  const size_t len_bytes = align_up(4 * static_cast<size_t>(p.B), 16);
+  const size_t fixed = q_bytes + p_bytes + cum_bytes + len_bytes + 16 * kMaxStages + 40 * 4 + 128;
+  const size_t budget = static_cast<size_t>(dev.smem_optin);
+  if (fixed + 2 * static_cast<size_t>(p.stage_bytes) > budget) return false;
+  int stages = static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes));
+  const int want = env_int("VH_DECODE_STAGES", 0);
+  if (want >= 2 && want < stages) stages = want;
+  p.stages = stages;
+  size_t off = static_cast<size_t>(stages) * p.stage_bytes;
+  p.q_off = static_cast<int>(off);
+  off += q_bytes;
+  p.p_off = static_cast<int>(off);
+  off = align_up(off + p_bytes, 16);
+  p.cum_off = static_cast<int>(off);
+  off += cum_bytes;
+  p.len_off = static_cast<int>(off);
+  off += len_bytes;
+  p.bar_off = static_cast<int>(align_up(off, 16));
+  off = p.bar_off + 16 * stages + 40 * 4;
+  p.smem_bytes = static_cast<int>(align_up(off, 128));
+  p.min_tiles = kMinTilesPerCta;
+  return static_cast<size_t>(p.smem_bytes) <= budget;
+}
+
+int auto_ctas(const AttnParams& p, const DeviceInfo& dev) {
+  int per_sm = 0;
+  if (vh::decode_attn_occupancy(p, &per_sm) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int want = env_int("VH_DECODE_CTAS_PER_SM", 0);
+  if (want >= 1 && want < per_sm) per_sm = want;
+  return std::max(1, dev.sm_count * per_sm / p.groups);
+}
+
+struct WsLayout {
+  size_t plan, lse, o, total;
+};
+
+WsLayout ws_layout(int B, int Hq, int D, int groups, int N) {
+  // part results: [groups][N][2][Hq/groups]; groups * (Hq/groups) == Hq
+  WsLayout w;
+  w.plan = 0;
+  w.lse = align_up(static_cast<size_t>(B) * 16, 256);
+  w.o = w.lse + align_up(static_cast<size_t>(N) * 2 * Hq * 4, 256);
+  w.total = w.o + static_cast<size_t>(N) * 2 * Hq * D * 4;
+  (void)groups;
+  return w;
+}
+
+bool too_many_tiles(int B, int max_pages_per_seq, int P) {
+  const long long max_len = static_cast<long long>(max_pages_per_seq) * P;
+  return max_len > (1LL << 24) || static_cast<long long>(B) * ((max_len + 15) / 16) >= (1LL << 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vh_status_string(int status) {
+  switch (status) {
+    case VH_OK: return "ok";
+    case VH_EINVAL: return "invalid argument (NULL pointer, unsupported shape or out-of-range scalar)";
+    case VH_EALIGN: return "pointer or stride not 16-byte aligned";
+    case VH_EWORKSPACE: return "workspace missing or too small";
+    case VH_ECUDA: return "CUDA launch error";
+    case VH_ENODEV: return "no usable sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void* stream) {
+  if (!cos_sin || max_pos < 1 || (head_dim != 64 && head_dim != 128) || !(theta > 0.0)) return VH_EINVAL;
+  if (!aligned16(cos_sin)) return VH_EALIGN;
+  if (!device_info()) return VH_ENODEV;
+  return vh::launch_rope_table(cos_sin, max_pos, head_dim, theta, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? VH_OK
+             : VH_ECUDA;
+}
+
+int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+                      const float* cos_sin, int max_pos, const int32_t* positions,
+                      vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride,
+                      int64_t token_stride, int num_pages,
+                      const int32_t* page_table, int max_pages_per_seq,
+                      const int32_t* seq_lens, const int32_t* active,
+                      float* q_rot, int32_t* err_flag,
+                      int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !page_table || !seq_lens || !active ||
+      !q_rot)
+    return VH_EINVAL;
+  if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
+      page_stride < 1 || token_stride < 1 || too_many_tiles(B, max_pages_per_seq, page_size))
+    return VH_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(q_rot) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+    return VH_EALIGN;
+  if (!device_info()) return VH_ENODEV;
+  vh::RopeAppendParams p{};
+  p.q = q;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.cos_sin = cos_sin;
+  p.max_pos = max_pos;
+  p.positions = positions;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.page_stride = page_stride;
+  p.token_stride = token_stride;
+  p.num_pages = num_pages;
+  p.page_table = page_table;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.seq_lens = seq_lens;
+  p.active = active;
+  p.q_rot = q_rot;
+  p.err_flag = err_flag;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.P = page_size;
+  return vh::launch_rope_kv_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK : VH_ECUDA;
+}
+
+int vh_decode_num_ctas(int B, int Hq, int Hkv, int D, int page_size) {
+  if (!valid_shape(B, Hq, Hkv, D, page_size)) return VH_EINVAL;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return VH_ENODEV;
+  AttnParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.P = page_size;
+  if (!plan_attn(p, *dev)) return VH_EINVAL;
+  return auto_ctas(p, *dev);
+}
+
+size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int num_ctas) {
+  if (!valid_shape(B, Hq, Hkv, D, page_size) || num_ctas < 0) return 0;
+  int N = num_ctas;
+  if (N == 0) {
+    N = vh_decode_num_ctas(B, Hq, Hkv, D, page_size);
+    if (N < 1) return 0;
+  }
+  return ws_layout(B, Hq, D, Hkv / choose_hc(Hkv, D), N).total;
+}
+
+int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
+                         int64_t page_stride, int64_t token_stride, int num_pages,
+                         const int32_t* page_table, int max_pages_per_seq,
+                         const int32_t* seq_lens, const int32_t* active,
+                         vh_bf16* out, float sm_scale, int num_ctas,
+                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                         int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out) return VH_EINVAL;
+  if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
+      token_stride < 1 || num_ctas < 0 || num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) ||
+      !(sm_scale == sm_scale))
+    return VH_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+    return VH_EALIGN;
+  if (!workspace) return VH_EWORKSPACE;
+  if (!aligned16(workspace)) return VH_EALIGN;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return VH_ENODEV;
+  AttnParams p{};
+  p.q_rot = q_rot;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.page_stride = page_stride;
+  p.token_stride = token_stride;
+  p.num_pages = num_pages;
+  p.page_table = page_table;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.seq_lens = seq_lens;
+  p.active = active;
+  p.out = out;
+  p.err_flag = err_flag;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.P = page_size;
+  if (!plan_attn(p, *dev)) return VH_EINVAL;
+  p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
+  const WsLayout w = ws_layout(B, Hq, D, p.groups, p.N);
+  if (workspace_bytes < w.total) return VH_EWORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.plan = reinterpret_cast<int4*>(ws + w.plan);
+  p.part_lse = reinterpret_cast<float*>(ws + w.lse);
+  p.part_o = reinterpret_cast<float*>(ws + w.o);
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK : VH_ECUDA;
+}
+
+int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
+                      int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!out || !valid_shape(B, Hq, Hkv, D, page_size) || num_ctas < 0 || num_ctas > 65535) return VH_EINVAL;
+  if (!aligned16(out)) return VH_EALIGN;
+  if (!workspace) return VH_EWORKSPACE;
+  if (!aligned16(workspace)) return VH_EALIGN;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return VH_ENODEV;
+  AttnParams a{};
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.P = page_size;
+  if (!plan_attn(a, *dev)) return VH_EINVAL;
+  const int N = num_ctas > 0 ? num_ctas : auto_ctas(a, *dev);
+  const WsLayout w = ws_layout(B, Hq, D, a.groups, N);
+  if (workspace_bytes < w.total) return VH_EWORKSPACE;
+  const unsigned char* ws = static_cast<const unsigned char*>(workspace);
+  vh::CombineParams p{};
+  p.plan = reinterpret_cast<const int4*>(ws + w.plan);
+  p.part_lse = reinterpret_cast<const float*>(ws + w.lse);
+  p.part_o = reinterpret_cast<const float*>(ws + w.o);
+  p.out = out;
+  p.B = B;
+  p.Hq = Hq;
+  p.D = D;
+  p.Hc = a.Hc;
+  p.G = a.G;
+  p.N = N;
+  return vh::launch_decode_combine(p, a.groups, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK
+                                                                                                 : VH_ECUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// vh_kernels.h -- parameter blocks and launchers shared by the host layer and
+// the kernel translation units (internal; the public interface is vh.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vh {
+
+struct RopeAppendParams {
+  const uint16_t* q;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const float* cos_sin;
+  int max_pos;
+  const int32_t* positions;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  long long page_stride;
+  long long token_stride;
+  int num_pages;
+  const int32_t* page_table;
+  int max_pages_per_seq;
+  const int32_t* seq_lens;
+  const int32_t* active;
+  float* q_rot;
+  int32_t* err_flag;
+  int B, Hq, Hkv, D, P;
+};
+
+// Shared-memory plan of the attention kernel (byte offsets from the dynamic
+// shared-memory base) and the split plan parameters.
+struct AttnParams {
+  const float* q_rot;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  long long page_stride;
+  long long token_stride;
+  int num_pages;
+  const int32_t* page_table;
+  int max_pages_per_seq;
+  const int32_t* seq_lens;
+  const int32_t* active;
+  uint16_t* out;
+  float scale_log2;   // softmax scale * log2(e)
+  int4* plan;         // [B]: first CTA, last CTA, slot used in the first CTA, tiles
+  float* part_o;      // [groups][N][2][Hc*G][D]
+  float* part_lse;    // [groups][N][2][Hc*G]   (base-2 log-sum-exp)
+  int32_t* err_flag;
+  int B, Hq, Hkv, D, G, P;
+  int Hc;             // kv heads per CTA = consumer warps
+  int groups;         // Hkv / Hc (gridDim.y)
+  int N;              // CTAs per group (gridDim.x)
+  int stages;
+  int min_tiles;      // lower bound on tiles per CTA when the work list is short
+  int k_row_bytes;    // padded shared-memory stride of a K row (token)
+  int v_row_bytes;    // shared-memory stride of a V row
+  int row_copy_bytes; // bytes copied per token row (Hc * D * 2)
+  int stage_bytes;
+  int q_off, p_off, cum_off, len_off, bar_off;
+  int smem_bytes;
+};
+
+struct CombineParams {
+  const int4* plan;
+  const float* part_o;
+  const float* part_lse;
+  uint16_t* out;
+  int B, Hq, D, Hc, G, N;
+};
+
+cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, cudaStream_t stream);
+cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream);
+cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device
+cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream_t stream);
+cudaError_t decode_attn_occupancy(const AttnParams& p, int* blocks_per_sm);
+
+}  // namespace vh

@@ -1,0 +1,163 @@
+"""Helpers for the GPU tests: run the CUDA path through the C interface and
+compare it with the float64 oracle on the same seeded inputs.
+
+Tolerance for float outputs (the attention output, bf16): elementwise
+|gpu - ref| <= 2e-3 + 1e-2 * |ref|.  The rotated q (fp32) must agree to
+1e-5 + 1e-5 * |ref| (fp32 RoPE with fp32 cos/sin against float64).  The KV
+append must be bit-exact, except rotated-key elements whose float64 value
+lies within the fp32 rotation's error bound of a bf16 rounding midpoint,
+where fp32 and float64 rotation may round to different neighbours.  For
+x' = x_i cos - x_{i+D/2} sin computed in fp32 (cos/sin rounded to fp32, two
+products, one subtraction) the error is below 3 * 2^-24 * (|x_i| + |x_{i+D/2}|);
+the exemption window is 2^-21 * (|x_i| + |x_{i+D/2}|), a margin of about 2.7.
+"""
+from __future__ import annotations
+
+import torch
+
+import oracle
+
+ATOL, RTOL = 2e-3, 1e-2
+QROT_ATOL, QROT_RTOL = 1e-5, 1e-5
+MIDPOINT_REL = 2.0 ** -21
+
+
+def vh():
+    import paged_len_decode_gb300 as v
+    return v
+
+
+def run_step(inp, *, num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, graph=False):
+    """Run RoPE+append, attention and combine on `inp` (CPU or CUDA DecodeInputs).
+
+    Returns dict(q_rot, out, pool_after, err) on the CPU; `inp` is not modified.
+    """
+    v = vh()
+    dev = torch.device("cuda")
+    g = inp.to(dev).clone()
+    B, Hq, Hkv, D, P = g.B, g.Hq, g.Hkv, g.D, g.P
+    max_pos = max_pos or g.max_pages_per_seq * P
+    cos_sin = torch.empty((max_pos, D), dtype=torch.float32, device=dev)
+    v.vh_rope_table(cos_sin, g.theta)
+    q_rot = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=dev)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = v.alloc_workspace(B, Hq, Hkv, D, P, num_ctas, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pos = positions.to(dev, torch.int32) if positions is not None else None
+    k_cache, v_cache = g.pool[:, 0], g.pool[:, 1]
+
+    def step():
+        v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
+                      g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
+                      err_flag=err)
+
+    if graph:
+        # first call outside capture (sets per-device launch attributes)
+        step()
+        torch.cuda.synchronize()
+        out.fill_(float("nan"))
+        cg = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(cg, stream=s):
+                step()
+        torch.cuda.current_stream().wait_stream(s)
+        cg.replay()
+    else:
+        step()
+    torch.cuda.synchronize()
+    return {"q_rot": q_rot.cpu(), "out": out.cpu(), "pool_after": g.pool.cpu(), "err": int(err.item())}
+
+
+def bits16(t):
+    return t.contiguous().view(torch.int16).to(torch.int32) & 0xFFFF
+
+
+def midpoint_mask(x: torch.Tensor, k_in: torch.Tensor) -> torch.Tensor:
+    """Elements of the rotated keys x (float64 [..., D]) that lie within the fp32
+    rotation error bound of a bf16 rounding midpoint; k_in are the keys before
+    rotation (bf16 [..., D]), whose pair magnitudes set the bound."""
+    ax = x.abs()
+    nz = ax > 0
+    e = torch.frexp(torch.where(nz, ax, torch.ones_like(ax))).exponent
+    ulp = torch.ldexp(torch.ones_like(ax), (e - 8).clamp(min=-133))
+    frac = torch.remainder(ax / ulp, 1.0)
+    k = k_in.double().abs()
+    h = k.shape[-1] // 2
+    pair = k[..., :h] + k[..., h:]
+    scale = torch.cat([pair, pair], dim=-1)
+    return nz & ((frac - 0.5).abs() * ulp <= MIDPOINT_REL * scale)
+
+
+def check_append(inp, ref, gpu_pool):
+    """Bit-exact placement: pool after the GPU append == pool after the oracle append,
+    except midpoint-exempt rotated-key elements.  Returns (number of exempt
+    elements, number that actually differ)."""
+    a, b = bits16(gpu_pool), bits16(ref["pool_after"])
+    diff = a != b
+    if not diff.any():
+        return 0, 0
+    # allowed differences: K elements of appended slots whose float64 value is a near-midpoint
+    allowed = torch.zeros_like(diff)
+    act = inp.active.cpu().bool()
+    lens = inp.seq_lens.cpu()
+    pt = inp.page_table.cpu()
+    mid = midpoint_mask(ref["k_rot"], inp.k_new.cpu())
+    n = 0
+    for bb in torch.nonzero(act).flatten().tolist():
+        L = int(lens[bb])
+        page, off = int(pt[bb, (L - 1) // inp.P]), (L - 1) % inp.P
+        allowed[page, 0, off] |= mid[bb]
+        n += int(mid[bb].sum())
+    bad = diff & ~allowed
+    assert not bad.any(), f"{int(bad.sum())} pool elements differ outside the midpoint exemption, " \
+                          f"first at {torch.nonzero(bad)[0].tolist()}"
+    # and the differing exempt elements are one bf16 step apart
+    d = (a[diff] - b[diff]).abs()
+    assert (d == 1).all()
+    return n, int(diff.sum())
+
+
+def check_out(inp, ref_out, gpu_out, rows=None):
+    act = inp.active.cpu().bool()
+    rows = list(range(inp.B)) if rows is None else rows
+    got = gpu_out.double()
+    for_rows = torch.tensor(rows, dtype=torch.long)
+    a = act[for_rows]
+    live = for_rows[a]
+    dead = for_rows[~a]
+    if len(dead):
+        assert torch.equal(gpu_out[dead], torch.zeros_like(gpu_out[dead])), "padding rows must be zero"
+    if len(live):
+        g_, r_ = got[live], ref_out[live]
+        assert torch.isfinite(g_).all(), "non-finite output in a live row"
+        err = (g_ - r_).abs()
+        tol = ATOL + RTOL * r_.abs()
+        worst = (err - tol).max().item()
+        assert worst <= 0, f"max |d| {err.max().item():.3e} exceeds tolerance by {worst:.3e}"
+        return err.max().item()
+    return 0.0
+
+
+def check_q_rot(inp, ref_q_rot, gpu_q_rot):
+    act = inp.active.cpu().bool()
+    g_, r_ = gpu_q_rot[act].double(), ref_q_rot[act]
+    if g_.numel() == 0:
+        return 0.0
+    err = (g_ - r_).abs()
+    assert (err <= QROT_ATOL + QROT_RTOL * r_.abs()).all(), f"q_rot max |d| {err.max().item():.3e}"
+    return err.max().item()
+
+
+def full_check(inp, *, num_ctas=0, rows=None, positions=None, sm_scale=0.0, graph=False, max_pos=None):
+    """Run the GPU path and the oracle on `inp`; check q_rot, append bits and out."""
+    cpu = inp.to("cpu")
+    ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale)
+    got = run_step(inp, num_ctas=num_ctas, positions=positions, sm_scale=sm_scale, graph=graph,
+                   max_pos=max_pos)
+    assert got["err"] == 0, f"device error flag {got['err']}"
+    exempt, n_diff = check_append(cpu, ref, got["pool_after"])
+    qerr = check_q_rot(cpu, ref["q_rot"], got["q_rot"])
+    oerr = check_out(cpu, ref["out"], got["out"], rows=rows)
+    return {"exempt": exempt, "n_diff": n_diff, "q_rot_err": qerr, "out_err": oerr, "got": got, "ref": ref}

@@ -1,0 +1,106 @@
+"""The C interface without a GPU: the library loads, exports every function
+include/vh.h declares, and rejects bad arguments on the host before any
+device work (only argument combinations that fail validation are used, so
+nothing here can launch a kernel)."""
+import ctypes
+import re
+
+import pytest
+
+import paged_len_decode_gb300 as v
+
+FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)        # misaligned
+
+
+def test_every_declared_function_is_exported():
+    names = v.header_functions()
+    assert set(names) >= {"vh_rope_table", "vh_rope_kv_append", "vh_decode_num_ctas",
+                          "vh_decode_workspace_bytes", "vh_paged_decode_attn", "vh_decode_combine",
+                          "vh_status_string"}
+    for n in names:
+        assert hasattr(v.lib, n), n
+
+
+def test_header_declares_extern_c_and_status_codes():
+    text = open(v.HEADER_PATH).read()
+    assert 'extern "C"' in text
+    for code, val in [("VH_OK", 0), ("VH_EINVAL", -1), ("VH_EALIGN", -2), ("VH_EWORKSPACE", -3),
+                      ("VH_ECUDA", -4), ("VH_ENODEV", -5)]:
+        assert re.search(rf"#define {code} \(?{val}\)?", text), code
+        assert getattr(v, code) == val
+
+
+def test_status_strings():
+    assert v.vh_status_string(0) == "ok"
+    assert "aligned" in v.vh_status_string(-2)
+    assert v.vh_status_string(12345) == "unknown status"
+
+
+def attn(**over):
+    a = dict(q_rot=FAKE, k=FAKE, vv=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10,
+             sl=FAKE, act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None,
+             B=4, Hq=16, Hkv=8, D=128, P=16)
+    a.update(over)
+    return v.lib.vh_paged_decode_attn(a["q_rot"], a["k"], a["vv"], a["ps"], a["ts"], a["npages"], a["pt"],
+                                      a["mps"], a["sl"], a["act"], a["out"], a["scale"], a["nctas"], a["ws"],
+                                      a["wsb"], a["err"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q_rot=None), v.VH_EINVAL),
+    (dict(out=None), v.VH_EINVAL),
+    (dict(Hq=12, Hkv=8), v.VH_EINVAL),        # Hq % Hkv != 0
+    (dict(Hq=24, Hkv=8), v.VH_EINVAL),        # G = 3
+    (dict(D=96), v.VH_EINVAL),
+    (dict(P=8), v.VH_EINVAL),
+    (dict(P=24), v.VH_EINVAL),
+    (dict(B=0), v.VH_EINVAL),
+    (dict(B=70000), v.VH_EINVAL),
+    (dict(mps=0), v.VH_EINVAL),
+    (dict(npages=0), v.VH_EINVAL),
+    (dict(nctas=-1), v.VH_EINVAL),
+    (dict(scale=float("nan")), v.VH_EINVAL),
+    (dict(mps=1 << 22), v.VH_EINVAL),         # lengths beyond 2^24 tokens
+    (dict(q_rot=ODD), v.VH_EALIGN),
+    (dict(k=ODD), v.VH_EALIGN),
+    (dict(ts=8 * 128 + 4), v.VH_EALIGN),      # stride not a multiple of 16 bytes
+    (dict(ws=None), v.VH_EWORKSPACE),
+    (dict(ws=ODD), v.VH_EALIGN),
+])
+def test_attention_argument_checks(over, code):
+    assert attn(**over) == code
+
+
+def test_valid_arguments_without_device_report_no_device():
+    # all host checks pass; the device query then fails on a GPU-less machine
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert attn() == v.VH_ENODEV
+
+
+def test_rope_append_argument_checks():
+    f = v.lib.vh_rope_kv_append
+    base = [FAKE, FAKE, FAKE, FAKE, 4096, None, FAKE, FAKE, 2 * 16 * 8 * 128, 8 * 128, 100, FAKE, 10, FAKE,
+            FAKE, FAKE, None, 4, 16, 8, 128, 16, None]
+    assert f(*base[:3], None, *base[4:]) == v.VH_EINVAL            # cos_sin NULL
+    b = list(base); b[4] = 0
+    assert f(*b) == v.VH_EINVAL                                     # max_pos < 1
+    b = list(base); b[0] = ODD
+    assert f(*b) == v.VH_EALIGN
+    b = list(base); b[15] = ODD
+    assert f(*b) == v.VH_EALIGN                                     # q_rot misaligned
+    b = list(base); b[20] = 80
+    assert f(*b) == v.VH_EINVAL                                     # head_dim
+
+
+def test_rope_table_and_combine_argument_checks():
+    assert v.lib.vh_rope_table(None, 10, 128, 10000.0, None) == v.VH_EINVAL
+    assert v.lib.vh_rope_table(FAKE, 10, 128, -1.0, None) == v.VH_EINVAL
+    assert v.lib.vh_rope_table(ODD, 10, 128, 10000.0, None) == v.VH_EALIGN
+    assert v.lib.vh_decode_combine(None, 0, FAKE, 0, 4, 16, 8, 128, 16, None) == v.VH_EWORKSPACE
+    assert v.lib.vh_decode_combine(FAKE, 1 << 30, ODD, 0, 4, 16, 8, 128, 16, None) == v.VH_EALIGN
+    assert v.lib.vh_decode_combine(FAKE, 1 << 30, FAKE, 0, 4, 12, 8, 128, 16, None) == v.VH_EINVAL
+    assert v.lib.vh_decode_workspace_bytes(4, 12, 8, 128, 16, 10) == 0
+    assert v.lib.vh_decode_workspace_bytes(4, 16, 8, 128, 16, 152) > 0
