@@ -78,6 +78,7 @@ typedef uint16_t vh_bf16;
 #define VH_EWORKSPACE (-3)  /* workspace NULL or smaller than required */
 #define VH_ECUDA (-4)       /* CUDA reported an error at launch */
 #define VH_ENODEV (-5)      /* no usable sm_103 device is current */
+#define VH_ESCRATCH (-6)    /* shape needs more scratch than VH_STATIC_SCRATCH_BYTES */
 
 /* device-side data-error bits, ORed into *err_flag */
 #define VH_ERR_SEQLEN 1     /* active row with seq_len outside [1, max_pages_per_seq*P]: row skipped */
@@ -168,6 +169,34 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
  * Errors: VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
 int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream);
+
+/* Attention plus combine for callers that cannot allocate device memory.
+ * The source pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory for a workspace (a runtime that only
+ * hands out preallocated arenas, a plug-in inside a host process that owns
+ * the CUDA context, a measurement that must not change the memory footprint).
+ * Same arguments and result as vh_paged_decode_attn followed by
+ * vh_decode_combine, except that there is no workspace: the split-K partial
+ * results go into one fixed array of VH_STATIC_SCRATCH_BYTES (8 MiB) compiled
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.  The call itself allocates and frees nothing.
+ *   - The first call on each device looks up that device's address of the
+ *     array (with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps whatever the last call left
+ *     there; nothing in it needs to start at zero.  Calls whose kernels can
+ *     overlap on the GPU (different streams, or different host threads) race
+ *     on the array and must be serialised by the caller.
+ *   - A shape whose scratch need (vh_decode_workspace_bytes) exceeds
+ *     VH_STATIC_SCRATCH_BYTES is rejected with VH_ESCRATCH before any launch.
+ * Errors: VH_EINVAL, VH_EALIGN, VH_ESCRATCH, VH_ENODEV, VH_ECUDA. */
+#define VH_STATIC_SCRATCH_BYTES (8u << 20)
+int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
+                                 int64_t page_stride, int64_t token_stride, int num_pages,
+                                 const int32_t* page_table, int max_pages_per_seq,
+                                 const int32_t* seq_lens, const int32_t* active,
+                                 vh_bf16* out, float sm_scale, int num_ctas, int32_t* err_flag,
+                                 int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
 /* Static text for a return code. */
 const char* vh_status_string(int status);

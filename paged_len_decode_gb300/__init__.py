@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libvh.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
 
 VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3, -4, -5
+VH_ESCRATCH = -6
 VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
 
 
@@ -56,6 +57,9 @@ def _load() -> ctypes.CDLL:
     lib.vh_paged_decode_attn.restype = I
     lib.vh_decode_combine.argtypes = [P, SZ, P, I, I, I, I, I, I, P]
     lib.vh_decode_combine.restype = I
+    lib.vh_paged_decode_attn_noalloc.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P,
+                                                 I, I, I, I, I, P]
+    lib.vh_paged_decode_attn_noalloc.restype = I
     return lib
 
 
@@ -171,6 +175,24 @@ def vh_decode_combine(workspace, out, Hkv: int, page_size: int, num_ctas: int = 
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _contig(out, torch.bfloat16, "out"), int(num_ctas), B, Hq, Hkv, D, page_size,
         _stream(stream)), "vh_decode_combine")
+
+
+def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, active, out,
+                                 sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
+                                 stream=None) -> None:
+    """Attention plus combine into `out` with the library's fixed scratch array,
+    for callers that cannot allocate a workspace (see include/vh.h)."""
+    B, Hq, D = q_rot.shape
+    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    if Dc != D or out.shape != (B, Hq, D):
+        raise ValueError("shape mismatch between q_rot, out and the cache")
+    _check(lib.vh_paged_decode_attn_noalloc(
+        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, NP,
+        _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
+        _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
+        None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
+        B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn_noalloc")
 
 
 def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas: int = 0,

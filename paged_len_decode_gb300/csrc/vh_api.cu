@@ -166,6 +166,7 @@ const char* vh_status_string(int status) {
     case VH_EWORKSPACE: return "workspace missing or too small";
     case VH_ECUDA: return "CUDA launch error";
     case VH_ENODEV: return "no usable sm_103 device is current";
+    case VH_ESCRATCH: return "shape needs more scratch than the built-in fixed scratch array holds";
     default: return "unknown status";
   }
 }
@@ -332,3 +333,111 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Attention without caller-provided scratch.
+//
+// Some callers have no way to allocate device memory for the workspace: code
+// running under an allocator they do not control (a serving runtime that
+// hands kernels only preallocated arenas), plug-ins whose host process owns
+// the CUDA context, or tools that must not change the memory footprint
+// between two measurements.  For them the split-K partial results go into
+// one fixed array that lives in this library's device image.  Every GPU
+// that loads the library keeps it, VH_STATIC_SCRATCH_BYTES bytes, until the
+// process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_static_scratch[VH_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+struct StaticScratch {
+  std::once_flag once;
+  void* ptr = nullptr;  // device address of g_static_scratch on this device
+};
+StaticScratch g_static[kMaxDevices];
+
+// Device address of the fixed scratch array on the current device.  Resolved
+// once per device, with that device current; in host code the array's name is
+// only a host-side stand-in and must never be handed to a kernel.
+void* static_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  StaticScratch& s = g_static[dev];
+  std::call_once(s.once, [&]() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    s.ptr = p;
+  });
+  return s.ptr;
+}
+
+}  // namespace
+
+extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
+                                            int64_t page_stride, int64_t token_stride, int num_pages,
+                                            const int32_t* page_table, int max_pages_per_seq,
+                                            const int32_t* seq_lens, const int32_t* active,
+                                            vh_bf16* out, float sm_scale, int num_ctas, int32_t* err_flag,
+                                            int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out) return VH_EINVAL;
+  if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
+      token_stride < 1 || num_ctas < 0 || num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) ||
+      !(sm_scale == sm_scale))
+    return VH_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+    return VH_EALIGN;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return VH_ENODEV;
+  AttnParams p{};
+  p.q_rot = q_rot;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.page_stride = page_stride;
+  p.token_stride = token_stride;
+  p.num_pages = num_pages;
+  p.page_table = page_table;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.seq_lens = seq_lens;
+  p.active = active;
+  p.out = out;
+  p.err_flag = err_flag;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.P = page_size;
+  if (!plan_attn(p, *dev)) return VH_EINVAL;
+  p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
+  const WsLayout w = ws_layout(B, Hq, D, p.groups, p.N);
+  if (w.total > static_cast<size_t>(VH_STATIC_SCRATCH_BYTES)) return VH_ESCRATCH;
+  unsigned char* ws = static_cast<unsigned char*>(static_scratch_address());
+  if (!ws) return VH_ECUDA;
+  // Nothing in the scratch has to start at zero: the attention kernel writes
+  // the per-row plan and every partial result before the combine reads them.
+  p.plan = reinterpret_cast<int4*>(ws + w.plan);
+  p.part_lse = reinterpret_cast<float*>(ws + w.lse);
+  p.part_o = reinterpret_cast<float*>(ws + w.o);
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (vh::launch_decode_attn(p, st) != cudaSuccess) return VH_ECUDA;
+  vh::CombineParams c{};
+  c.plan = p.plan;
+  c.part_lse = p.part_lse;
+  c.part_o = p.part_o;
+  c.out = out;
+  c.B = B;
+  c.Hq = Hq;
+  c.D = D;
+  c.Hc = p.Hc;
+  c.G = p.G;
+  c.N = p.N;
+  return vh::launch_decode_combine(c, p.groups, st) == cudaSuccess ? VH_OK : VH_ECUDA;
+}
