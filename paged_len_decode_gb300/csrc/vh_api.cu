@@ -71,17 +71,21 @@ bool valid_shape(int B, int Hq, int Hkv, int D, int P) {
          P <= 1024 && P % 16 == 0 && Hkv <= 1024;
 }
 
-// kv heads per CTA: the largest divisor of Hkv with Hc * D <= 1024 and Hc <= 8.
-int choose_hc(int Hkv, int D) {
-  int hc = std::min({Hkv, 1024 / D, 8});
-  while (Hkv % hc != 0) --hc;
-  return hc;
-}
-
 int env_int(const char* name, int dflt) {
   const char* s = std::getenv(name);
   if (!s || !*s) return dflt;
   return std::atoi(s);
+}
+
+// kv heads per CTA: the largest divisor of Hkv with Hc * D <= 1024 and Hc <= 8
+// (VH_DECODE_HC lowers the cap, for tuning).
+int choose_hc(int Hkv, int D) {
+  int cap = std::min(1024 / D, 8);
+  const int want = env_int("VH_DECODE_HC", 0);
+  if (want >= 1 && want < cap) cap = want;
+  int hc = std::min(Hkv, cap);
+  while (Hkv % hc != 0) --hc;
+  return hc;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
