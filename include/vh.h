@@ -86,6 +86,9 @@ typedef uint16_t vh_bf16;
 #define VH_ERR_POS 4        /* position outside [0, max_pos): the row is skipped by the append */
 #define VH_ERR_TIMEOUT 8    /* an internal pipeline wait ran out of time: the CTA gave up */
 
+/* launch flags of vh_decode_fused */
+#define VH_FLAG_PDL 1u      /* programmatic dependent launch, see vh_decode_fused */
+
 /* Fill the RoPE table used by vh_rope_kv_append.
  * cos_sin: float [max_pos][D]; row p holds cos(p * f_i) in columns 0..D/2-1
  * and sin(p * f_i) in columns D/2..D-1, f_i = theta^(-2i/D).  Angles and
@@ -129,9 +132,9 @@ int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_n
  * negative VH_E* status on bad shapes or when no device is usable. */
 int vh_decode_num_ctas(int B, int Hq, int Hkv, int D, int page_size);
 
-/* Bytes of workspace vh_paged_decode_attn / vh_decode_combine need for this
- * shape and CTA count (num_ctas == 0: the automatic count on the current
- * device).  Returns 0 on bad arguments. */
+/* Bytes of workspace vh_paged_decode_attn / vh_decode_combine / vh_decode_fused
+ * need for this shape and CTA count (num_ctas == 0: enough for the automatic
+ * count of either path on the current device).  Returns 0 on bad arguments. */
 size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int num_ctas);
 
 /* Paged GQA decode attention.
@@ -169,6 +172,40 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
  * Errors: VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
 int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream);
+
+/* The whole decode step of one layer in ONE launch: RoPE of q and of the new
+ * key, append of the new key/value into the cache, attention and the merge
+ * of split rows.  Same inputs and outputs as vh_rope_kv_append +
+ * vh_paged_decode_attn + vh_decode_combine (apart from q_rot, which is not
+ * written), with these differences:
+ *   - the workspace must be zero-filled before its first use with this call
+ *     (for example cudaMemsetAsync(workspace, 0, workspace_bytes)); it holds
+ *     per-row counters that every completed call returns to zero, so later
+ *     calls need no refill.  Refill it after a call that set VH_ERR_TIMEOUT;
+ *   - a row whose position (positions[b], or seq_len-1) falls outside
+ *     [0, max_pos) is treated like a padding row (zero output, no append) and
+ *     VH_ERR_POS is set;
+ *   - the new token's key is rotated and used by the CTA that owns the row's
+ *     last tile, which also writes it (and v) to the cache slot; no other CTA
+ *     reads that slot, so there is no ordering hazard inside the launch;
+ *   - flags: 0, or VH_FLAG_PDL to launch as a programmatic dependent of the
+ *     previous kernel on the stream, so that this launch's start-up (reading
+ *     seq_lens, active, positions and page_table, planning the split)
+ *     overlaps the end of that kernel.  Only valid when the kernel launched
+ *     immediately before on the same stream does not write seq_lens, active,
+ *     positions or page_table (host copies in between are fine); everything
+ *     else is read and written only after that kernel has completed.  The
+ *     kernel itself always lets a following dependent launch start early.
+ * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,
+ * VH_ENODEV, VH_ECUDA. */
+int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+                    const float* cos_sin, int max_pos, const int32_t* positions,
+                    vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride, int64_t token_stride,
+                    int num_pages, const int32_t* page_table, int max_pages_per_seq,
+                    const int32_t* seq_lens, const int32_t* active,
+                    vh_bf16* out, float sm_scale, int num_ctas,
+                    void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
+                    int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
 /* Attention plus combine for callers that cannot allocate device memory.
  * The source pages have no counterpart to this call; it exists for callers

@@ -9,7 +9,7 @@ library is missing or a call fails, an exception is raised.
 Functions mirror the C entry points by name:
     vh_rope_table, vh_rope_kv_append, vh_decode_num_ctas,
     vh_decode_workspace_bytes, vh_paged_decode_attn, vh_decode_combine,
-    vh_status_string
+    vh_decode_fused, vh_paged_decode_attn_noalloc, vh_status_string
 plus `decode_step`, which issues the three calls of one decode step.
 """
 from __future__ import annotations
@@ -27,6 +27,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
 VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3, -4, -5
 VH_ESCRATCH = -6
 VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
+VH_FLAG_PDL = 1
 
 
 class VHError(RuntimeError):
@@ -60,6 +61,9 @@ def _load() -> ctypes.CDLL:
     lib.vh_paged_decode_attn_noalloc.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P,
                                                  I, I, I, I, I, P]
     lib.vh_paged_decode_attn_noalloc.restype = I
+    lib.vh_decode_fused.argtypes = [P, P, P, P, I, P, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P,
+                                    ctypes.c_uint, I, I, I, I, I, P]
+    lib.vh_decode_fused.restype = I
     return lib
 
 
@@ -195,11 +199,34 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
         B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn_noalloc")
 
 
+def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, out,
+                    workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
+                    pdl: bool = False, stream=None) -> torch.Tensor:
+    """One whole decode step in one launch (RoPE, append, attention, merge).
+    `workspace` must be zero-filled before its first use (alloc_workspace does that).
+    pdl=True sets VH_FLAG_PDL (see include/vh.h for when that is allowed)."""
+    B, Hq, D = q.shape
+    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or out.shape != (B, Hq, D):
+        raise ValueError("shape mismatch between q, k_new, v_new, out and the cache")
+    _check(lib.vh_decode_fused(
+        _contig(q, torch.bfloat16, "q"), _contig(k_new, torch.bfloat16, "k_new"),
+        _contig(v_new, torch.bfloat16, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
+        cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
+        kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
+        _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
+        _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
+        VH_FLAG_PDL if pdl else 0, B, Hq, Hkv, D, P, _stream(stream)), "vh_decode_fused")
+    return out
+
+
 def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas: int = 0,
                     device=None) -> torch.Tensor:
-    """Device scratch for vh_paged_decode_attn / vh_decode_combine (torch allocation)."""
+    """Zero-filled device scratch for the attention calls (torch allocation)."""
     n = vh_decode_workspace_bytes(B, Hq, Hkv, D, page_size, num_ctas)
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def decode_step(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, q_rot,

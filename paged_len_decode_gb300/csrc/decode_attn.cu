@@ -1,34 +1,45 @@
-// decode_attn.cu -- paged GQA decode attention (q_len = 1) and the LSE combine.
+// decode_attn.cu -- paged GQA decode attention (q_len = 1), the fused decode
+// step, and the LSE combine.
 //
 // Operation ("Engineering TTS inference in vLLM-Omni", Fish Speech S2 Pro,
 // "model-specific attention kernel"): for every active row b and q head g,
 // with kv head h = g / G,
 //     s_j = scale * <q_rot[b,g], K[b,h,j]>,  j < L_b  (keys through the page table)
 //     o   = sum_j softmax(s)_j V[b,h,j]
-// in fp32 with a running max (online softmax); long rows are cut into
+// with a running max (online softmax) in fp32; long rows are cut into
 // segments whose partial (o, lse) are merged by the log-sum-exp recurrence.
+// The fused variant also applies RoPE to q and to the new key and appends
+// the new key/value to the cache ("Adding a Model", vox-serve, section 1:
+// write K/V into the paged cache, then attend), and merges split rows
+// itself, so one launch is one whole decode step of a layer.
 //
 // Design for GB300 (HBM-bound: 2-4 flops per byte of K/V):
 //  * Work list.  Every active row contributes ceil(L/16) tiles of 16 tokens;
 //    the list of all tiles in row order is cut into N equal contiguous
 //    ranges, one per CTA, on the device (each CTA prefix-sums the row tile
-//    counts in shared memory).  No host sync, static grid, and the load is
+//    counts in shared memory).  No host sync, a static grid, and the load is
 //    balanced to within one tile whatever the length mix; a row is split
 //    where its tiles straddle two CTAs (at most two partial segments per CTA).
 //  * Data movement.  One producer warp streams each tile into a ring of
 //    shared-memory stages with bulk asynchronous copies (one 16-byte-aligned
-//    copy per token row, K rows and V rows of the CTA's kv heads), completed
-//    on an mbarrier transaction count; consumers release a stage through a
-//    second mbarrier.  K rows get a 32-byte pad so the per-key reads of the
-//    score step are free of bank conflicts.
-//  * Compute.  One consumer warp per kv head.  Scores: a lane owns one key
-//    (and half of D), q is read from shared memory as a broadcast, bf16 K is
-//    widened with shifts and multiplied with packed two-lane fp32 FMAs.  The
-//    value step: a lane owns 8 output dims for a subset of the tile's keys.
-//    exp2 with log2(e) folded into the scale.
-//  * Stale slots (tail of the last page, slots never copied) are never used:
-//    their scores are replaced by -inf before the max and their V rows are
-//    skipped, so NaN or Inf bits there cannot reach the output.
+//    copy per token row, K and V rows of the CTA's kv heads) completed on an
+//    mbarrier transaction count; consumers release a stage through a second
+//    mbarrier.  The q rows of the next segment are copied the same way into a
+//    staging buffer while the current segment is still being consumed.
+//  * Math on tensor cores.  One consumer warp per kv head.  With 16 keys per
+//    tile and the G q heads of the kv head padded to 8, the scores are one
+//    m16n8 tile: S^T (keys x heads) = K (keys x D) . q^T, and the output is
+//    O^T (D x heads) += V^T (D x keys) . P^T (keys x heads), both as
+//    mma.sync m16n8k16 with bf16 operands and fp32 accumulation.  q and p are
+//    fp32 values: each is split into a bf16 high part and a bf16 residual
+//    (x = hi + lo to 2^-16 relative) and both parts are multiplied, so the
+//    products keep about 16 significant bits while K and V (bf16 already)
+//    enter exactly.  P goes from the score-fragment layout to the operand
+//    layout with movmatrix transposes.  K and V rows get a 16-byte pad so
+//    ldmatrix reads are free of bank conflicts.
+//  * Stale slots (tail of the last page, slots never copied) never reach the
+//    output: their scores are replaced by -inf before the max and their V rows
+//    are zeroed in shared memory before the value product.
 #include "vh_common.cuh"
 #include "vh_kernels.h"
 
@@ -37,16 +48,7 @@ namespace vh {
 namespace {
 
 constexpr int kMaxHc = 8;                    // kv heads (consumer warps) per CTA
-constexpr int kThreadsMax = 32 * (kMaxHc + 1);
-
-template <int D, int G>
-struct Lay {
-  static constexpr int KSPLIT = 256 / D;          // key groups in the value step
-  static constexpr int KPER = kTile / KSPLIT;     // keys per group
-  static constexpr int CHUNKS = D / 8;            // 16-byte chunks of a head row
-  static constexpr int PSTRIDE = kTile * G + KSPLIT * 4;  // floats of p per warp
-  __device__ static __forceinline__ int pidx(int k) { return k * G + (k / KPER) * 4; }
-};
+constexpr int kThreadsMax = 32 * (kMaxHc + 2);  // consumers, producer, merge warp
 
 __device__ __forceinline__ long long range_begin(int c, int n_eff, long long T) {
   return (static_cast<long long>(c) * T) / n_eff;
@@ -91,30 +93,134 @@ __device__ void block_inclusive_scan(int* cum, int n, int* warp_tot) {
   __syncthreads();
 }
 
-enum { kMiscWarpTot = 0, kMiscAbort = 32, kMiscInts = 40 };
+enum { kMiscWarpTot = 0, kMiscAbort = 32, kMiscNVerdict = 33, kMiscVerdict = 34, kMiscInts = 48 };
 
+__device__ __forceinline__ float bf16_at(const unsigned char* base, int idx) {
+  return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(base)[idx]) << 16);
+}
+
+// Merge the partial results of one row for the G q heads of one kv head (one
+// warp): piece j comes from CTA cf + j, slot `first_slot` for j == 0 and slot
+// 0 otherwise; lse in base 2.  M = max_j lse_j, w_j = 2^(lse_j - M),
+// o = sum_j w_j o_j / sum_j w_j.  Loads are issued a chunk of pieces at a
+// time (and bypass L1: other CTAs wrote them during this launch).
 template <int D, int G>
+__device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse, const float* __restrict__ part_o,
+                                             long long slot_base /* (gy * N) * 2 */, int HG, int wg /* w * G */,
+                                             int cf, int np, int first_slot, uint16_t* __restrict__ out_row,
+                                             int lane) {
+  constexpr int PER = D / 32;
+  constexpr int U = 16 / G;  // pieces per batch of loads
+  auto idx_of = [&](int j) -> long long {
+    return (slot_base + 2LL * (cf + j) + (j == 0 ? first_slot : 0)) * HG + wg;
+  };
+  float M[G];
+#pragma unroll
+  for (int n = 0; n < G; ++n) M[n] = __int_as_float(0xff800000);
+  for (int j = lane; j < np; j += 32) {
+    const long long ix = idx_of(j);
+#pragma unroll
+    for (int n = 0; n < G; ++n) M[n] = fmaxf(M[n], __ldcg(part_lse + ix + n));
+  }
+#pragma unroll
+  for (int n = 0; n < G; ++n)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M[n] = fmaxf(M[n], __shfl_xor_sync(0xffffffffu, M[n], off));
+  float o[G][PER], ws[G];
+#pragma unroll
+  for (int n = 0; n < G; ++n) {
+    ws[n] = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[n][i] = 0.f;
+  }
+  for (int j0 = 0; j0 < np; j0 += U) {
+    float lv[U][G], v[U][G][PER];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u;
+      const long long ix = j < np ? idx_of(j) : idx_of(j0);
+#pragma unroll
+      for (int n = 0; n < G; ++n) {
+        lv[u][n] = j < np ? __ldcg(part_lse + ix + n) : __int_as_float(0xff800000);
+        const float* src = part_o + (ix + n) * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+          v[u][n][0] = t.x;
+          v[u][n][1] = t.y;
+          v[u][n][2] = t.z;
+          v[u][n][3] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+          v[u][n][0] = t.x;
+          v[u][n][1] = t.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int n = 0; n < G; ++n) {
+        const float wgt = exp2f(lv[u][n] - M[n]);  // 0 for the padding entries of the last chunk
+        ws[n] += wgt;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) o[n][i] += wgt * v[u][n][i];
+      }
+  }
+#pragma unroll
+  for (int n = 0; n < G; ++n) {
+    const float iw = 1.f / ws[n];
+    uint16_t* dst = out_row + static_cast<long long>(n) * D + lane * PER;
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(o[n][0] * iw, o[n][1] * iw), pack_bf16x2(o[n][2] * iw, o[n][3] * iw));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[n][0] * iw, o[n][1] * iw);
+    }
+  }
+}
+
+template <int D, int G, bool FUSED>
 __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnParams p) {
-  using L_ = Lay<D, G>;
+  constexpr int KSTEPS = D / 16;  // k-steps of the score product = m-tiles of the value product
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hc = p.Hc, S = p.stages;
   const int c = blockIdx.x, gy = blockIdx.y;
+  const int HG = Hc * G;  // q heads of this CTA
   int* cum = reinterpret_cast<int*>(smem + p.cum_off);
   int* lens = reinterpret_cast<int*>(smem + p.len_off);
+  int* posv = reinterpret_cast<int*>(smem + p.pos_off);
+  long long* meta = reinterpret_cast<long long*>(smem + p.meta_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  int* misc = reinterpret_cast<int*>(smem + p.bar_off + 16 * S);
+  int* misc = reinterpret_cast<int*>(smem + p.bar_off + 8 * (2 * S + 4));
   volatile int* abort_flag = misc + kMiscAbort;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + S);
+  const uint32_t qfull = smem_addr(bars + 2 * S), qempty = smem_addr(bars + 2 * S + 1);
+  // fused merge: consumers -> merge warp ("partial result written"), merge warp -> consumers ("counted")
+  const uint32_t pready = smem_addr(bars + 2 * S + 2), mdone = smem_addr(bars + 2 * S + 3);
   const int max_len = p.max_pages_per_seq * p.P;
+  pdl_launch_dependents();  // the next kernel may start its CTAs as ours finish
 
   // ---- prologue: tile count of every row and their prefix sum -------------
+  // (lengths, flags, positions and, below, page ids are read before the wait
+  // for the previous kernel: they must not be written by that kernel; every
+  // other access comes after the wait)
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int a = p.active[b], L = p.seq_lens[b];
-    const int nt = row_tiles(a, L, max_len);
+    int nt = row_tiles(a, L, max_len);
+    if (a && nt == 0 && c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_SEQLEN);
+    if constexpr (FUSED) {
+      if (nt > 0) {
+        const int pos = p.positions ? p.positions[b] : L - 1;
+        if (pos < 0 || pos >= p.max_pos) {
+          nt = 0;
+          if (c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_POS);
+        }
+        posv[b] = pos;
+      }
+    }
     cum[1 + b] = nt;
     lens[b] = L;
-    if (a && nt == 0 && c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_SEQLEN);
   }
   if (tid == 0) {
     cum[0] = 0;
@@ -123,64 +229,204 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, Hc);
     }
+    mbar_init(qfull, 1);
+    mbar_init(qempty, Hc);
+    mbar_init(pready, Hc);
+    mbar_init(mdone, 1);
     fence_barrier_init();
   }
   __syncthreads();
   block_inclusive_scan(cum, p.B, misc + kMiscWarpTot);
   const long long T = cum[p.B];
-  const int n_eff = T == 0 ? 0 : static_cast<int>(min(static_cast<long long>(p.N), (T + p.min_tiles - 1) / p.min_tiles));
+  const int n_eff =
+      T == 0 ? 0 : static_cast<int>(min(static_cast<long long>(p.N), (T + p.min_tiles - 1) / p.min_tiles));
+
+  // This CTA's tile range and its first row.
+  const long long t0_pre = n_eff > 0 ? range_begin(c, n_eff, T) : 0;
+  const long long t1_pre = n_eff > 0 ? range_begin(c + 1, n_eff, T) : 0;
+  int b0_pre = 0;
+  if (c < n_eff) {
+    int lo = 0, hi = p.B - 1;  // first row with cum[b + 1] > t0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (cum[mid + 1] > t0_pre) hi = mid; else lo = mid + 1;
+    }
+    b0_pre = lo;
+  }
+  // The producer's first page ids are read before the wait as well.
+  const int tpp = p.P / kTile;  // tiles per page
+  auto tile_page = [&](long long tt) -> int {
+    if (tt >= t1_pre) return 0;
+    int lo = b0_pre, hi = p.B - 1;  // row of tile tt: first row with cum[row + 1] > tt
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (cum[mid + 1] > tt) hi = mid; else lo = mid + 1;
+    }
+    const int tk = static_cast<int>(tt - cum[lo]);
+    return p.page_table[static_cast<long long>(lo) * p.max_pages_per_seq + tk / tpp];
+  };
+  int win = 0, nxt = 0;
+  if (warp == Hc && c < n_eff) {
+    win = tile_page(t0_pre + lane);
+    nxt = tile_page(t0_pre + 32 + lane);
+  }
+  pdl_wait();
 
   // ---- per-row duties, rows b = c (mod N): split plan, zero padding rows ---
-  const int HG = Hc * G;  // q heads of this CTA
   for (int b = c; b < p.B; b += p.N) {
     const int nt = cum[b + 1] - cum[b];
     if (nt == 0) {
       uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.Hq + gy * HG) * D);
       for (int i = tid; i < HG * D / 8; i += blockDim.x) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (gy == 0 && tid == 0) p.plan[b] = make_int4(-1, -1, 0, 0);
-    } else if (gy == 0 && tid == 0) {
+      if (!FUSED && gy == 0 && tid == 0) p.plan[b] = make_int4(-1, -1, 0, 0);
+    } else if (!FUSED && gy == 0 && tid == 0) {
       const long long s0 = cum[b], s1 = cum[b + 1] - 1;
       const int cf = cta_of(s0, n_eff, T), cl = cta_of(s1, n_eff, T);
       p.plan[b] = make_int4(cf, cl, range_begin(cf, n_eff, T) == s0 ? 0 : 1, nt);
     }
   }
   if (c >= n_eff) return;
+  const long long t0 = t0_pre, t1 = t1_pre;
+  const int b0 = b0_pre;
 
-  const long long t0 = range_begin(c, n_eff, T), t1 = range_begin(c + 1, n_eff, T);
-  int b0;
-  {
-    int lo = 0, hi = p.B - 1;  // first row with cum[b + 1] > t0
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (cum[mid + 1] > t0) hi = mid; else lo = mid + 1;
+  if (FUSED && warp == Hc + 1) {
+    // ======================= merge warp (fused) ============================
+    // Counts this CTA's partial results per row, off the streaming path: the
+    // consumers only signal that a partial result is written.  A CTA has at
+    // most two partial segments: its first row, if it started or stops inside
+    // it, and its last row, if that is another row and stops inside it.
+    int b_last;
+    {
+      int lo = b0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid + 1] > t1 - 1) hi = mid; else lo = mid + 1;
+      }
+      b_last = lo;
     }
-    b0 = lo;
+    int rows[2], n = 0;
+    if (t0 > cum[b0] || t1 < cum[b0 + 1]) rows[n++] = b0;
+    if (b_last != b0 && t1 < cum[b_last + 1]) rows[n++] = b_last;
+    int done = 0;
+    for (int k = 0; k < n; ++k) {
+      if (!mbar_wait(pready, k & 1)) {
+        if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      if (lane == 0) {
+        const int rb = rows[k];
+        const long long s0 = cum[rb], s1 = cum[rb + 1] - 1;
+        const int cf = cta_of(s0, n_eff, T), cl = cta_of(s1, n_eff, T);
+        __threadfence();  // the consumers' partial writes (ordered by the barrier) before the count
+        int* counter = p.counters + static_cast<long long>(gy) * p.B + rb;
+        const int old = atomicAdd(counter, 1);
+        const int last = (old == cl - cf);
+        if (last) {
+          *counter = 0;  // every piece has arrived: ready for the next call
+          __threadfence();
+        }
+        int* v = misc + kMiscVerdict + 5 * k;
+        v[0] = last;
+        v[1] = rb;
+        v[2] = cf;
+        v[3] = cl;
+        v[4] = range_begin(cf, n_eff, T) == s0 ? 0 : 1;
+      }
+      ++done;
+    }
+    if (lane == 0) {
+      misc[kMiscNVerdict] = done;
+      mbar_arrive(mdone);
+    }
+    return;
   }
-  unsigned char* stage_base = smem;
 
   if (warp == Hc) {
     // ======================= producer warp =================================
+    // Everything a tile needs is computed before the wait for its stage, so
+    // that a released stage is refilled at once: the row walk is incremental,
+    // and the page ids come from a 32-tile window that is loaded (one
+    // coalesced load per lane) a whole window ahead of its use.
     const int h0 = gy * Hc;
     const unsigned char* kbase = reinterpret_cast<const unsigned char*>(p.k_cache + static_cast<long long>(h0) * D);
     const unsigned char* vbase = reinterpret_cast<const unsigned char*>(p.v_cache + static_cast<long long>(h0) * D);
+    long long wb = t0;
     int b = b0;
     long long rt0 = cum[b], rt1 = cum[b + 1];
-    int stage = 0, round = 0;
+    int tin_page = static_cast<int>((t0 - rt0) % tpp);  // tile index within its page
+    int stage = 0, round = 0, nseg = 0;
     long long issued = 0;
     bool aborted = false;
+    const int r = lane & 15;
     for (long long t = t0; t < t1; ++t, ++issued) {
+      bool new_seg = (t == t0);
+      if (t > t0 && ++tin_page == tpp) tin_page = 0;
       while (t >= rt1) {
         ++b;
         rt0 = rt1;
         rt1 = cum[b + 1];
+        new_seg = true;
+        tin_page = 0;
+      }
+      if (t == wb + 32) {
+        wb += 32;
+        win = nxt;
+        nxt = tile_page(wb + 32 + lane);
       }
       const int tok0 = static_cast<int>(t - rt0) * kTile;
       const int nvalid = min(kTile, lens[b] - tok0);
-      int page = p.page_table[static_cast<long long>(b) * p.max_pages_per_seq + tok0 / p.P];
-      if (page < 0 || page >= p.num_pages) {
+      const bool last_of_row = (t == rt1 - 1);
+      int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - wb));
+      const bool page_ok = page >= 0 && page < p.num_pages;
+      if (!page_ok) {
         if (lane == 0) flag_error(p.err_flag, VH_ERR_PAGE);
         page = 0;
       }
+      if (new_seg) {
+        // q rows of this segment's row (fused: bf16 q and the RoPE row of its
+        // position) into the staging buffer, once the consumers have taken
+        // the previous segment's q into registers.
+        if (nseg > 0 && !mbar_wait(qempty, (nseg - 1) & 1)) {
+          if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+          *abort_flag = 1;
+          aborted = true;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_bytes));
+          const long long qrow = static_cast<long long>(b) * p.Hq + static_cast<long long>(h0) * G;
+          if constexpr (FUSED) {
+            bulk_g2s(smem_addr(smem + p.q_off), p.q + qrow * D, HG * D * 2, qfull);
+            bulk_g2s(smem_addr(smem + p.q_off + HG * D * 2), p.cos_sin + static_cast<long long>(posv[b]) * D,
+                     D * 4, qfull);
+          } else {
+            bulk_g2s(smem_addr(smem + p.q_off), p.q_rot + qrow * D, HG * D * 4, qfull);
+          }
+        }
+        ++nseg;
+      }
+      // source and destination of this lane's row copy, and the append slot
+      const long long page_off = static_cast<long long>(page) * p.page_stride;
+      const void* src;
+      if (FUSED && last_of_row && r == nvalid - 1) {
+        // the new token: raw k (rotated by the consumers) and v straight from the inputs
+        const long long nrow = (static_cast<long long>(b) * p.Hkv + h0) * D;
+        src = lane < 16 ? static_cast<const void*>(p.k_new + nrow) : static_cast<const void*>(p.v_new + nrow);
+      } else {
+        const long long off = 2LL * (page_off + static_cast<long long>(tin_page * kTile + r) * p.token_stride);
+        src = (lane < 16 ? kbase : vbase) + off;
+      }
+      const uint32_t st = smem_addr(smem) + static_cast<uint32_t>(stage) * p.stage_bytes;
+      const uint32_t dst = lane < 16 ? st + r * p.k_row_bytes : st + kTile * p.k_row_bytes + r * p.v_row_bytes;
+      long long meta_val = -1;
+      if constexpr (FUSED) {
+        if (last_of_row && page_ok)
+          meta_val = page_off + static_cast<long long>(tin_page * kTile + nvalid - 1) * p.token_stride +
+                     static_cast<long long>(h0) * D;
+      }
+      const uint32_t tx = static_cast<uint32_t>(nvalid) * 2u * p.row_copy_bytes;
+
       if (issued >= S && !mbar_wait(empty0 + 8 * stage, (round - 1) & 1)) {
         if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
         *abort_flag = 1;
@@ -192,18 +438,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         break;
       }
       const uint32_t fb = full0 + 8 * stage;
-      if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nvalid) * 2u * p.row_copy_bytes);
-      __syncwarp();
-      const int r = lane & 15;
-      if (r < nvalid) {
-        const long long off = 2LL * (static_cast<long long>(page) * p.page_stride +
-                                     static_cast<long long>(tok0 % p.P + r) * p.token_stride);
-        unsigned char* st = stage_base + static_cast<long long>(stage) * p.stage_bytes;
-        if (lane < 16)
-          bulk_g2s(smem_addr(st + r * p.k_row_bytes), kbase + off, p.row_copy_bytes, fb);
-        else
-          bulk_g2s(smem_addr(st + kTile * p.k_row_bytes + r * p.v_row_bytes), vbase + off, p.row_copy_bytes, fb);
+      if (lane == 0) {
+        if constexpr (FUSED) meta[stage] = meta_val;
+        mbar_arrive_expect_tx(fb, tx);
       }
+      __syncwarp();
+      if (r < nvalid) bulk_g2s(dst, src, p.row_copy_bytes, fb);
       if (++stage == S) {
         stage = 0;
         ++round;
@@ -214,48 +454,92 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       const long long n = min(issued, static_cast<long long>(S));
       for (long long k = issued - n; k < issued; ++k)
         (void)mbar_wait(full0 + 8 * static_cast<int>(k % S), static_cast<uint32_t>((k / S) & 1));
+      if (nseg > 0) (void)mbar_wait(qfull, (nseg - 1) & 1);
     }
     return;
   }
 
   // ========================= consumer warps ==================================
-  const int w = warp;                 // kv head within the CTA
-  const int h = gy * Hc + w;          // kv head
-  float* qs = reinterpret_cast<float*>(smem + p.q_off) + w * G * D;
-  float* ps = reinterpret_cast<float*>(smem + p.p_off) + w * L_::PSTRIDE;
-  const int kt = lane >> 1, khalf = lane & 1;        // score step: key, half of D
-  const int chunk = lane % L_::CHUNKS, kp = lane / L_::CHUNKS;  // value step
+  const int w = warp;            // kv head within the CTA
+  const int h = gy * Hc + w;     // kv head
+  const int g4 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
   const float NEG_INF = __int_as_float(0xff800000);
+  // ldmatrix row/column of this lane: K tile (keys x dims) and V tile (transposed)
+  const int ka_row = (lane & 7) + 8 * ((lane >> 3) & 1), ka_col = 8 * (lane >> 4);
+  const int va_row = (lane & 7) + 8 * (lane >> 4), va_col = 8 * ((lane >> 3) & 1);
 
-  float m[G], lsum[G];
-  float2 acc[G][4];
+  uint32_t qh[KSTEPS][2], ql[KSTEPS][2];  // q^T operand fragments (high / residual parts)
+  float acc[KSTEPS][4];                   // O^T fragments: dims mt*16 + g4 (+8), heads 2 t4 (+1)
+  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+  float rc[(D / 2 + 31) / 32], rs[(D / 2 + 31) / 32];  // fused: RoPE row for the new key
+  (void)rc;
+  (void)rs;
+
   int b = b0;
   long long rt0 = cum[b], rt1 = cum[b + 1];
-  int seg = 0, stage = 0, round = 0;
+  int seg = 0, nseg = 0, stage = 0, round = 0, npart = 0;
   for (long long t = t0; t < t1; ++t) {
-    bool new_row = false;
+    bool new_seg = (t == t0), new_row = false;
     while (t >= rt1) {
       ++b;
       rt0 = rt1;
       rt1 = cum[b + 1];
       new_row = true;
+      new_seg = true;
     }
     if (new_row) ++seg;
     const long long sb = max(t0, rt0), se = min(t1, rt1);
-    if (t == sb) {
-      const float* qsrc = p.q_rot + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * G) * D;
-      __syncwarp();
-      for (int i = lane * 4; i < G * D; i += 128)
-        *reinterpret_cast<float4*>(qs + i) = __ldg(reinterpret_cast<const float4*>(qsrc + i));
-      __syncwarp();
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        m[g] = NEG_INF;
-        lsum[g] = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[g][q] = make_float2(0.f, 0.f);
+
+    if (new_seg) {
+      if (!mbar_wait(qfull, nseg & 1)) {
+        if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return;
       }
+      const unsigned char* qb = smem + p.q_off;
+      const int n = g4;  // q head (within the group) of this lane's operand column
+#pragma unroll
+      for (int k = 0; k < KSTEPS; ++k) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (n < G) {
+          const int dd[4] = {16 * k + 2 * t4, 16 * k + 2 * t4 + 1, 16 * k + 2 * t4 + 8, 16 * k + 2 * t4 + 9};
+          const int row = (w * G + n) * D;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if constexpr (FUSED) {
+              const float* cs = reinterpret_cast<const float*>(qb + HG * D * 2);
+              const int d = dd[e];
+              const int i = d < D / 2 ? d : d - D / 2;
+              const float cv = cs[i], sv = cs[D / 2 + i];
+              const float xv = bf16_at(qb, row + d);
+              const float yv = bf16_at(qb, row + (d < D / 2 ? d + D / 2 : d - D / 2));
+              x[e] = d < D / 2 ? xv * cv - yv * sv : xv * cv + yv * sv;
+            } else {
+              x[e] = reinterpret_cast<const float*>(qb)[row + dd[e]];
+            }
+          }
+        }
+        split_bf16x2(x[0], x[1], qh[k][0], ql[k][0]);
+        split_bf16x2(x[2], x[3], qh[k][1], ql[k][1]);
+      }
+      if constexpr (FUSED) {
+        const float* cs = reinterpret_cast<const float*>(qb + HG * D * 2);
+#pragma unroll
+        for (int j = 0; j < (D / 2 + 31) / 32; ++j) {
+          const int i = lane + 32 * j;
+          rc[j] = i < D / 2 ? cs[i] : 0.f;
+          rs[j] = i < D / 2 ? cs[D / 2 + i] : 0.f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty);
+      ++nseg;
+      m0 = m1 = NEG_INF;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     }
+
     const int tok0 = static_cast<int>(t - rt0) * kTile;
     const int nvalid = min(kTile, lens[b] - tok0);
     if (!mbar_wait(full0 + 8 * stage, round & 1)) {
@@ -263,118 +547,108 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       *abort_flag = 1;
       return;
     }
-    const unsigned char* st = stage_base + static_cast<long long>(stage) * p.stage_bytes;
+    unsigned char* kst = smem + static_cast<long long>(stage) * p.stage_bytes + w * D * 2;
+    unsigned char* vst = smem + static_cast<long long>(stage) * p.stage_bytes + kTile * p.k_row_bytes + w * D * 2;
+    bool touched = false;
 
-    // ---- scores: lane (kt, khalf) dots its key with all G q heads --------------
-    float s[G];
-    {
-      const unsigned char* krow = st + kt * p.k_row_bytes + w * D * 2;
-      float2 a0[G], a1[G];
+    if constexpr (FUSED) {
+      if (t == rt1 - 1) {
+        // the new token (row nvalid-1): rotate its key in place, then append k and v to the cache
+        uint16_t* kr = reinterpret_cast<uint16_t*>(kst + (nvalid - 1) * p.k_row_bytes);
+        const long long dst = meta[stage];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        a0[g] = make_float2(0.f, 0.f);
-        a1[g] = make_float2(0.f, 0.f);
-      }
-#pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
-        const int cc = 2 * j + khalf;
-        const uint4 kv = *reinterpret_cast<const uint4*>(krow + cc * 16);
-        const float2 k0 = bf16x2_to_float2(kv.x), k1 = bf16x2_to_float2(kv.y);
-        const float2 k2 = bf16x2_to_float2(kv.z), k3 = bf16x2_to_float2(kv.w);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + cc * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + cc * 8 + 4);
-          a0[g] = ffma2(k0, make_float2(qa.x, qa.y), a0[g]);
-          a1[g] = ffma2(k1, make_float2(qa.z, qa.w), a1[g]);
-          a0[g] = ffma2(k2, make_float2(qb.x, qb.y), a0[g]);
-          a1[g] = ffma2(k3, make_float2(qb.z, qb.w), a1[g]);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float v = (a0[g].x + a0[g].y) + (a1[g].x + a1[g].y);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        s[g] = kt < nvalid ? v * p.scale_log2 : NEG_INF;
-      }
-    }
-
-    // ---- online softmax update ----------------------------------------------
-    float alpha[G];
-    bool rescale = false;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float mx = s[g];
-#pragma unroll
-      for (int off = 2; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mn = fmaxf(m[g], mx);
-      alpha[g] = exp2f(m[g] - mn);
-      rescale |= (alpha[g] != 1.f);
-      s[g] = exp2f(s[g] - mn);  // p
-      lsum[g] = lsum[g] * alpha[g] + s[g];
-      m[g] = mn;
-    }
-    if (khalf == 0) {
-      float* dst = ps + L_::pidx(kt);
-      if constexpr (G == 1) {
-        dst[0] = s[0];
-      } else if constexpr (G == 2) {
-        *reinterpret_cast<float2*>(dst) = make_float2(s[0], s[1]);
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; g += 4)
-          *reinterpret_cast<float4*>(dst + g) = make_float4(s[g], s[g + 1], s[g + 2], s[g + 3]);
-      }
-    }
-    __syncwarp();
-
-    // ---- values: lane (chunk, kp) accumulates 8 dims over its keys -------------
-    if (rescale) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float2 a2 = make_float2(alpha[g], alpha[g]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[g][q] = fmul2(acc[g][q], a2);
-      }
-    }
-    {
-      const unsigned char* vcol = st + kTile * p.k_row_bytes + w * D * 2 + chunk * 16;
-#pragma unroll
-      for (int i = 0; i < L_::KPER; ++i) {
-        const int k = kp * L_::KPER + i;
-        if (k < nvalid) {
-          const uint4 vv = *reinterpret_cast<const uint4*>(vcol + k * p.v_row_bytes);
-          const float2 v0 = bf16x2_to_float2(vv.x), v1 = bf16x2_to_float2(vv.y);
-          const float2 v2 = bf16x2_to_float2(vv.z), v3 = bf16x2_to_float2(vv.w);
-          float pg[G];
-          const float* src = ps + L_::pidx(k);
-          if constexpr (G == 1) {
-            pg[0] = src[0];
-          } else if constexpr (G == 2) {
-            const float2 t2 = *reinterpret_cast<const float2*>(src);
-            pg[0] = t2.x;
-            pg[1] = t2.y;
-          } else {
-#pragma unroll
-            for (int g = 0; g < G; g += 4) {
-              const float4 t4 = *reinterpret_cast<const float4*>(src + g);
-              pg[g] = t4.x;
-              pg[g + 1] = t4.y;
-              pg[g + 2] = t4.z;
-              pg[g + 3] = t4.w;
+        for (int j = 0; j < (D / 2 + 31) / 32; ++j) {
+          const int i = lane + 32 * j;
+          if (i < D / 2) {
+            const float x = __uint_as_float(static_cast<uint32_t>(kr[i]) << 16);
+            const float y = __uint_as_float(static_cast<uint32_t>(kr[i + D / 2]) << 16);
+            const uint16_t xr = static_cast<uint16_t>(float_to_bf16_bits(x * rc[j] - y * rs[j]));
+            const uint16_t yr = static_cast<uint16_t>(float_to_bf16_bits(y * rc[j] + x * rs[j]));
+            kr[i] = xr;
+            kr[i + D / 2] = yr;
+            if (dst >= 0) {
+              p.k_cache_w[dst + static_cast<long long>(w) * D + i] = xr;
+              p.k_cache_w[dst + static_cast<long long>(w) * D + i + D / 2] = yr;
             }
           }
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float2 pp = make_float2(pg[g], pg[g]);
-            acc[g][0] = ffma2(v0, pp, acc[g][0]);
-            acc[g][1] = ffma2(v1, pp, acc[g][1]);
-            acc[g][2] = ffma2(v2, pp, acc[g][2]);
-            acc[g][3] = ffma2(v3, pp, acc[g][3]);
-          }
         }
+        if (dst >= 0 && lane < D / 8) {
+          const uint4 vv = *reinterpret_cast<const uint4*>(vst + (nvalid - 1) * p.v_row_bytes + lane * 16);
+          *reinterpret_cast<uint4*>(p.v_cache_w + dst + static_cast<long long>(w) * D + lane * 8) = vv;
+        }
+        touched = true;
       }
     }
+    if (nvalid < kTile) {
+      // stale V rows would meet p = 0 in the product; make them exact zeros
+      constexpr int CH = D / 8;
+      for (int r = nvalid + lane / CH; r < kTile; r += 32 / CH)
+        *reinterpret_cast<uint4*>(vst + r * p.v_row_bytes + (lane % CH) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      touched = true;
+    }
+    if (touched) __syncwarp();
+
+    // ---- scores S^T = K q^T on tensor cores ----------------------------------
+    float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const uint32_t ka = smem_addr(kst + ka_row * p.k_row_bytes + ka_col * 2);
+#pragma unroll
+      for (int k = 0; k < KSTEPS; ++k) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ka + 32 * k, a0, a1, a2, a3);
+        mma_bf16(sh, a0, a1, a2, a3, qh[k][0], qh[k][1]);
+        mma_bf16(sl, a0, a1, a2, a3, ql[k][0], ql[k][1]);
+      }
+    }
+    // lane holds keys g4 (s[0], s[1]) and g4 + 8 (s[2], s[3]), heads 2 t4 and 2 t4 + 1
+    const bool va = g4 < nvalid, vb = g4 + 8 < nvalid;
+    const float s0 = va ? (sh[0] + sl[0]) * p.scale_log2 : NEG_INF;
+    const float s1 = va ? (sh[1] + sl[1]) * p.scale_log2 : NEG_INF;
+    const float s2 = vb ? (sh[2] + sl[2]) * p.scale_log2 : NEG_INF;
+    const float s3 = vb ? (sh[3] + sl[3]) * p.scale_log2 : NEG_INF;
+
+    // ---- online softmax (per head; reduce over the 8 lanes sharing t4) -------
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    const float p0 = exp2f(s0 - mn0), p2 = exp2f(s2 - mn0);
+    const float p1 = exp2f(s1 - mn1), p3 = exp2f(s3 - mn1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+    uint32_t ph01, pl01, ph23, pl23;
+    split_bf16x2(p0, p1, ph01, pl01);
+    split_bf16x2(p2, p3, ph23, pl23);
+    const uint32_t bh0 = movm_t(ph01), bh1 = movm_t(ph23);
+    const uint32_t bl0 = movm_t(pl01), bl1 = movm_t(pl23);
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+    }
+
+    // ---- values O^T += V^T P^T on tensor cores ---------------------------------
+    {
+      const uint32_t vaddr = smem_addr(vst + va_row * p.v_row_bytes + va_col * 2);
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vaddr + 32 * mt, a0, a1, a2, a3);
+        mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+    if (touched) fence_proxy_async_smem();  // generic writes before the next bulk copy into this stage
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * stage);
     if (++stage == S) {
@@ -384,126 +658,115 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
 
     // ---- end of a segment: finished row or partial result ----------------------
     if (t == se - 1) {
+      float L0 = l0, L1 = l1;
 #pragma unroll
-      for (int off = L_::CHUNKS; off < 32; off <<= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[g][q].x += __shfl_xor_sync(0xffffffffu, acc[g][q].x, off);
-            acc[g][q].y += __shfl_xor_sync(0xffffffffu, acc[g][q].y, off);
-          }
+      for (int off = 4; off < 32; off <<= 1) {
+        L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+        L1 += __shfl_xor_sync(0xffffffffu, L1, off);
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int off = 2; off < 32; off <<= 1) lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], off);
-      }
+      const float il0 = 1.f / L0, il1 = 1.f / L1;
+      const int n0 = 2 * t4, n1 = 2 * t4 + 1;
       const bool full_row = (sb == rt0) && (se == rt1);
       if (full_row) {
-        if (kp == 0) {
+        uint16_t* o0 = p.out + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * G + n0) * D;
+        uint16_t* o1 = o0 + D;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float il = 1.f / lsum[g];
-            uint4 o;
-            o.x = pack_bf16x2(acc[g][0].x * il, acc[g][0].y * il);
-            o.y = pack_bf16x2(acc[g][1].x * il, acc[g][1].y * il);
-            o.z = pack_bf16x2(acc[g][2].x * il, acc[g][2].y * il);
-            o.w = pack_bf16x2(acc[g][3].x * il, acc[g][3].y * il);
-            *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.Hq + h * G + g) * D + chunk * 8) = o;
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          const int d = mt * 16 + g4;
+          if (n0 < G) {
+            o0[d] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][0] * il0));
+            o0[d + 8] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][2] * il0));
+          }
+          if (n1 < G) {
+            o1[d] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][1] * il1));
+            o1[d + 8] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][3] * il1));
           }
         }
       } else {
         const int slot = seg == 0 ? 0 : 1;
         const long long base = ((static_cast<long long>(gy) * p.N + c) * 2 + slot) * HG + w * G;
-        if (kp == 0) {
+        float* o0 = p.part_o + (base + n0) * D;
+        float* o1 = o0 + D;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float il = 1.f / lsum[g];
-            float* dst = p.part_o + (base + g) * D + chunk * 8;
-            *reinterpret_cast<float4*>(dst) =
-                make_float4(acc[g][0].x * il, acc[g][0].y * il, acc[g][1].x * il, acc[g][1].y * il);
-            *reinterpret_cast<float4*>(dst + 4) =
-                make_float4(acc[g][2].x * il, acc[g][2].y * il, acc[g][3].x * il, acc[g][3].y * il);
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          const int d = mt * 16 + g4;
+          if (n0 < G) {
+            o0[d] = acc[mt][0] * il0;
+            o0[d + 8] = acc[mt][2] * il0;
+          }
+          if (n1 < G) {
+            o1[d] = acc[mt][1] * il1;
+            o1[d + 8] = acc[mt][3] * il1;
           }
         }
-        if (lane == 0) {
-#pragma unroll
-          for (int g = 0; g < G; ++g) p.part_lse[base + g] = m[g] + log2f(lsum[g]);
+        if (g4 == 0) {
+          if (n0 < G) p.part_lse[base + n0] = m0 + log2f(L0);
+          if (n1 < G) p.part_lse[base + n1] = m1 + log2f(L1);
         }
+        if constexpr (FUSED) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pready);  // the merge warp counts it
+          ++npart;
+        }
+      }
+    }
+  }
+  if constexpr (FUSED) {
+    // Rows whose last partial result this CTA delivered: merge all pieces.
+    if (npart > 0) {
+      if (!mbar_wait(mdone, 0)) {
+        if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+        return;
+      }
+      const int nv = *reinterpret_cast<volatile int*>(misc + kMiscNVerdict);
+      for (int k = 0; k < nv; ++k) {
+        const int* v = misc + kMiscVerdict + 5 * k;
+        if (!v[0]) continue;
+        __threadfence();
+        merge_pieces<D, G>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, v[2],
+                           v[3] - v[2] + 1, v[4],
+                           p.out + (static_cast<long long>(v[1]) * p.Hq + static_cast<long long>(h) * G) * D, lane);
       }
     }
   }
 }
 
-// One CTA per (row, kv-head group); a warp per q head.  Rows that one CTA
-// finished (or padding rows) return at once.
-template <int D>
+// Three-call path: one CTA per (row, kv-head group), one warp per kv head of
+// the group (its G q heads).  Rows that one CTA finished, and padding rows,
+// return at once.
+template <int D, int G>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineParams p) {
+  pdl_wait();  // launched as a dependent of the attention kernel
   const int b = blockIdx.x, gy = blockIdx.y;
   const int4 pl = p.plan[b];
   if (pl.x < 0 || pl.x == pl.y) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int HG = p.Hc * p.G;
-  constexpr int PER = D / 32;
-  for (int lq = warp; lq < HG; lq += nw) {
-    float M = __int_as_float(0xff800000);
-    for (int cc = pl.x; cc <= pl.y; ++cc) {
-      const int slot = cc == pl.x ? pl.z : 0;
-      const long long idx = ((static_cast<long long>(gy) * p.N + cc) * 2 + slot) * HG + lq;
-      M = fmaxf(M, p.part_lse[idx]);
-    }
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
-    for (int cc = pl.x; cc <= pl.y; ++cc) {
-      const int slot = cc == pl.x ? pl.z : 0;
-      const long long idx = ((static_cast<long long>(gy) * p.N + cc) * 2 + slot) * HG + lq;
-      const float wgt = exp2f(p.part_lse[idx] - M);
-      wsum += wgt;
-      const float* o = p.part_o + idx * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(o);
-        acc[0] += wgt * v.x;
-        acc[1] += wgt * v.y;
-        acc[2] += wgt * v.z;
-        acc[3] += wgt * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(o);
-        acc[0] += wgt * v.x;
-        acc[1] += wgt * v.y;
-      }
-    }
-    const float iw = 1.f / wsum;
-    uint16_t* dst = p.out + (static_cast<long long>(b) * p.Hq + gy * HG + lq) * D + lane * PER;
-    if constexpr (PER == 4) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * iw, acc[1] * iw), pack_bf16x2(acc[2] * iw, acc[3] * iw));
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * iw, acc[1] * iw);
-    }
-  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int HG = p.Hc * G;
+  merge_pieces<D, G>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, pl.x, pl.y - pl.x + 1,
+                     pl.z, p.out + (static_cast<long long>(b) * p.Hq + static_cast<long long>(gy) * HG + w * G) * D,
+                     lane);
 }
 
 template <int D, int G>
-const void* attn_kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_attn_kernel<D, G>);
+const void* attn_kernel_ptr(bool fused) {
+  return fused ? reinterpret_cast<const void*>(&decode_attn_kernel<D, G, true>)
+               : reinterpret_cast<const void*>(&decode_attn_kernel<D, G, false>);
 }
 
-const void* select_attn_kernel(int D, int G) {
+const void* select_attn_kernel(int D, int G, bool fused) {
   if (D == 128) {
     switch (G) {
-      case 1: return attn_kernel_ptr<128, 1>();
-      case 2: return attn_kernel_ptr<128, 2>();
-      case 4: return attn_kernel_ptr<128, 4>();
-      case 8: return attn_kernel_ptr<128, 8>();
+      case 1: return attn_kernel_ptr<128, 1>(fused);
+      case 2: return attn_kernel_ptr<128, 2>(fused);
+      case 4: return attn_kernel_ptr<128, 4>(fused);
+      case 8: return attn_kernel_ptr<128, 8>(fused);
     }
   } else if (D == 64) {
     switch (G) {
-      case 1: return attn_kernel_ptr<64, 1>();
-      case 2: return attn_kernel_ptr<64, 2>();
-      case 4: return attn_kernel_ptr<64, 4>();
-      case 8: return attn_kernel_ptr<64, 8>();
+      case 1: return attn_kernel_ptr<64, 1>(fused);
+      case 2: return attn_kernel_ptr<64, 2>(fused);
+      case 4: return attn_kernel_ptr<64, 4>(fused);
+      case 8: return attn_kernel_ptr<64, 8>(fused);
     }
   }
   return nullptr;
@@ -512,34 +775,62 @@ const void* select_attn_kernel(int D, int G) {
 }  // namespace
 
 cudaError_t prepare_decode_attn(int D, int G, int max_smem) {
-  const void* k = select_attn_kernel(D, G);
-  if (!k) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  for (bool fused : {false, true}) {
+    const void* k = select_attn_kernel(D, G, fused);
+    if (!k) return cudaErrorInvalidValue;
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t decode_attn_occupancy(const AttnParams& p, int* blocks_per_sm) {
-  const void* k = select_attn_kernel(p.D, p.G);
+  const void* k = select_attn_kernel(p.D, p.G, p.fused != 0);
   if (!k) return cudaErrorInvalidValue;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, 32 * (p.Hc + 1), p.smem_bytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, 32 * (p.Hc + (p.fused ? 2 : 1)),
+                                                       p.smem_bytes);
 }
 
-cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream) {
-  const void* k = select_attn_kernel(p.D, p.G);
+cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pdl) {
+  const void* k = select_attn_kernel(p.D, p.G, p.fused != 0);
   if (!k) return cudaErrorInvalidValue;
-  dim3 grid(p.N, p.groups), block(32 * (p.Hc + 1));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.N, p.groups);
+  cfg.blockDim = dim3(32 * (p.Hc + (p.fused ? 2 : 1)));
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   void* args[] = {const_cast<AttnParams*>(&p)};
-  return cudaLaunchKernel(k, grid, block, args, static_cast<size_t>(p.smem_bytes), stream);
+  return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream_t stream) {
-  dim3 grid(p.B, groups);
-  const int HG = p.Hc * p.G;
-  const int threads = 32 * (HG < 8 ? HG : 8);
-  if (p.D == 128)
-    decode_combine_kernel<128><<<grid, threads, 0, stream>>>(p);
-  else
-    decode_combine_kernel<64><<<grid, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependent of the attention kernel that precedes it on the stream
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.B, groups);
+  cfg.blockDim = dim3(32 * p.Hc);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+#define VH_COMBINE_CASE(DD, GG) \
+  if (p.D == DD && p.G == GG) return cudaLaunchKernelEx(&cfg, decode_combine_kernel<DD, GG>, p);
+  VH_COMBINE_CASE(128, 1)
+  VH_COMBINE_CASE(128, 2)
+  VH_COMBINE_CASE(128, 4)
+  VH_COMBINE_CASE(128, 8)
+  VH_COMBINE_CASE(64, 1)
+  VH_COMBINE_CASE(64, 2)
+  VH_COMBINE_CASE(64, 4)
+  VH_COMBINE_CASE(64, 8)
+#undef VH_COMBINE_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace vh

@@ -90,38 +90,50 @@ int choose_hc(int Hkv, int D) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Shared-memory plan; returns false if the shape cannot fit two stages.
-bool plan_attn(AttnParams& p, const DeviceInfo& dev) {
+// Shared-memory plan of the attention kernel (fused or not).  Prefers at
+// least three pipeline stages: if they do not fit, fewer kv heads go to each
+// CTA.  Returns false if even one head per CTA cannot have two stages.
+bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
+  p.fused = fused ? 1 : 0;
   p.G = p.Hq / p.Hkv;
-  p.Hc = choose_hc(p.Hkv, p.D);
-  p.groups = p.Hkv / p.Hc;
-  p.row_copy_bytes = p.Hc * p.D * 2;
-  p.k_row_bytes = p.row_copy_bytes + 32;
-  p.v_row_bytes = p.row_copy_bytes;
-  p.stage_bytes = static_cast<int>(align_up(16 * (p.k_row_bytes + p.v_row_bytes), 128));
-  const int ksplit = 256 / p.D;
-  const size_t q_bytes = static_cast<size_t>(p.Hc) * p.G * p.D * 4;
-  const size_t p_bytes = static_cast<size_t>(p.Hc) * (16 * p.G + ksplit * 4) * 4;
-  const size_t cum_bytes = align_up(4 * (static_cast<size_t>(p.B) + 1), 16);
-  const size_t len_bytes = align_up(4 * static_cast<size_t>(p.B), 16);
-  const size_t fixed = q_bytes + p_bytes + cum_bytes + len_bytes + 16 * kMaxStages + 40 * 4 + 128;
   const size_t budget = static_cast<size_t>(dev.smem_optin);
-  if (fixed + 2 * static_cast<size_t>(p.stage_bytes) > budget) return false;
-  int stages = static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes));
+  int hc = choose_hc(p.Hkv, p.D);
+  size_t fixed = 0;
+  int stages = 0;
+  for (;;) {
+    p.Hc = hc;
+    p.row_copy_bytes = hc * p.D * 2;
+    p.k_row_bytes = p.row_copy_bytes + 16;  // 16-byte pad: conflict-free ldmatrix rows
+    p.v_row_bytes = p.row_copy_bytes + 16;
+    p.stage_bytes = static_cast<int>(align_up(16 * static_cast<size_t>(p.k_row_bytes + p.v_row_bytes), 128));
+    const size_t hg = static_cast<size_t>(hc) * p.G;
+    p.q_bytes = static_cast<int>(fused ? hg * p.D * 2 + p.D * 4 : hg * p.D * 4);
+    fixed = align_up(p.q_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
+            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256;
+    stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
+    if (stages >= 3 || hc == 1) break;
+    int next = hc - 1;
+    while (next > 1 && p.Hkv % next != 0) --next;
+    hc = next;
+  }
+  if (stages < 2) return false;
+  p.groups = p.Hkv / p.Hc;
   const int want = env_int("VH_DECODE_STAGES", 0);
   if (want >= 2 && want < stages) stages = want;
   p.stages = stages;
   size_t off = static_cast<size_t>(stages) * p.stage_bytes;
   p.q_off = static_cast<int>(off);
-  off += q_bytes;
-  p.p_off = static_cast<int>(off);
-  off = align_up(off + p_bytes, 16);
+  off += align_up(p.q_bytes, 128);
   p.cum_off = static_cast<int>(off);
-  off += cum_bytes;
+  off += align_up(4 * (static_cast<size_t>(p.B) + 1), 16);
   p.len_off = static_cast<int>(off);
-  off += len_bytes;
+  off += align_up(4 * static_cast<size_t>(p.B), 16);
+  p.pos_off = static_cast<int>(off);
+  off += align_up(4 * static_cast<size_t>(p.B), 16);
+  p.meta_off = static_cast<int>(off);
+  off += 8 * static_cast<size_t>(stages);
   p.bar_off = static_cast<int>(align_up(off, 16));
-  off = p.bar_off + 16 * stages + 40 * 4;
+  off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 4) + 48 * 4;
   p.smem_bytes = static_cast<int>(align_up(off, 128));
   p.min_tiles = kMinTilesPerCta;
   return static_cast<size_t>(p.smem_bytes) <= budget;
@@ -138,18 +150,20 @@ int auto_ctas(const AttnParams& p, const DeviceInfo& dev) {
   return std::max(1, dev.sm_count * per_sm / p.groups);
 }
 
+// Workspace: per-row split plan (int4 [B]); per-(head group, row) counters of
+// the fused merge (int [Hkv][B], an upper bound on groups); partial lse
+// [groups][N][2][Hq/groups] and partial outputs [...][D] (groups * Hq/groups == Hq).
 struct WsLayout {
-  size_t plan, lse, o, total;
+  size_t plan, counters, lse, o, total;
 };
 
-WsLayout ws_layout(int B, int Hq, int D, int groups, int N) {
-  // part results: [groups][N][2][Hq/groups]; groups * (Hq/groups) == Hq
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int N) {
   WsLayout w;
   w.plan = 0;
-  w.lse = align_up(static_cast<size_t>(B) * 16, 256);
+  w.counters = align_up(static_cast<size_t>(B) * 16, 256);
+  w.lse = w.counters + align_up(static_cast<size_t>(B) * Hkv * 4, 256);
   w.o = w.lse + align_up(static_cast<size_t>(N) * 2 * Hq * 4, 256);
   w.total = w.o + static_cast<size_t>(N) * 2 * Hq * D * 4;
-  (void)groups;
   return w;
 }
 
@@ -238,7 +252,7 @@ int vh_decode_num_ctas(int B, int Hq, int Hkv, int D, int page_size) {
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev)) return VH_EINVAL;
+  if (!plan_attn(p, *dev, false)) return VH_EINVAL;
   return auto_ctas(p, *dev);
 }
 
@@ -246,10 +260,21 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_ctas < 0) return 0;
   int N = num_ctas;
   if (N == 0) {
-    N = vh_decode_num_ctas(B, Hq, Hkv, D, page_size);
-    if (N < 1) return 0;
+    // large enough for the automatic CTA count of both the three-call and the fused path
+    const DeviceInfo* dev = device_info();
+    if (!dev) return 0;
+    for (bool fused : {false, true}) {
+      AttnParams p{};
+      p.B = B;
+      p.Hq = Hq;
+      p.Hkv = Hkv;
+      p.D = D;
+      p.P = page_size;
+      if (!plan_attn(p, *dev, fused)) return 0;
+      N = std::max(N, auto_ctas(p, *dev));
+    }
   }
-  return ws_layout(B, Hq, D, Hkv / choose_hc(Hkv, D), N).total;
+  return ws_layout(B, Hq, Hkv, D, N).total;
 }
 
 int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
@@ -289,9 +314,9 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev)) return VH_EINVAL;
+  if (!plan_attn(p, *dev, false)) return VH_EINVAL;
   p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
-  const WsLayout w = ws_layout(B, Hq, D, p.groups, p.N);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   p.plan = reinterpret_cast<int4*>(ws + w.plan);
@@ -299,7 +324,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
   p.part_o = reinterpret_cast<float*>(ws + w.o);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
-  return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK : VH_ECUDA;
+  return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? VH_OK : VH_ECUDA;
 }
 
 int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
@@ -316,9 +341,9 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
   a.Hkv = Hkv;
   a.D = D;
   a.P = page_size;
-  if (!plan_attn(a, *dev)) return VH_EINVAL;
+  if (!plan_attn(a, *dev, false)) return VH_EINVAL;
   const int N = num_ctas > 0 ? num_ctas : auto_ctas(a, *dev);
-  const WsLayout w = ws_layout(B, Hq, D, a.groups, N);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
   const unsigned char* ws = static_cast<const unsigned char*>(workspace);
   vh::CombineParams p{};
@@ -334,6 +359,69 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
   p.N = N;
   return vh::launch_decode_combine(p, a.groups, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK
                                                                                                  : VH_ECUDA;
+}
+
+int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+                    const float* cos_sin, int max_pos, const int32_t* positions,
+                    vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride, int64_t token_stride,
+                    int num_pages, const int32_t* page_table, int max_pages_per_seq,
+                    const int32_t* seq_lens, const int32_t* active,
+                    vh_bf16* out, float sm_scale, int num_ctas,
+                    void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
+                    int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !page_table || !seq_lens || !active ||
+      !out || (flags & ~static_cast<unsigned>(VH_FLAG_PDL)) != 0)
+    return VH_EINVAL;
+  if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
+      page_stride < 1 || token_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
+      too_many_tiles(B, max_pages_per_seq, page_size) || !(sm_scale == sm_scale))
+    return VH_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+    return VH_EALIGN;
+  if (!workspace) return VH_EWORKSPACE;
+  if (!aligned16(workspace)) return VH_EALIGN;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return VH_ENODEV;
+  AttnParams p{};
+  p.q = q;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.cos_sin = cos_sin;
+  p.max_pos = max_pos;
+  p.positions = positions;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_cache_w = k_cache;
+  p.v_cache_w = v_cache;
+  p.page_stride = page_stride;
+  p.token_stride = token_stride;
+  p.num_pages = num_pages;
+  p.page_table = page_table;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.seq_lens = seq_lens;
+  p.active = active;
+  p.out = out;
+  p.err_flag = err_flag;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.P = page_size;
+  if (!plan_attn(p, *dev, true)) return VH_EINVAL;
+  p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
+  if (workspace_bytes < w.total) return VH_EWORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.plan = reinterpret_cast<int4*>(ws + w.plan);
+  p.counters = reinterpret_cast<int*>(ws + w.counters);
+  p.part_lse = reinterpret_cast<float*>(ws + w.lse);
+  p.part_o = reinterpret_cast<float*>(ws + w.o);
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), (flags & VH_FLAG_PDL) != 0) == cudaSuccess
+             ? VH_OK
+             : VH_ECUDA;
 }
 
 }  // extern "C"
@@ -417,9 +505,9 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev)) return VH_EINVAL;
+  if (!plan_attn(p, *dev, false)) return VH_EINVAL;
   p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
-  const WsLayout w = ws_layout(B, Hq, D, p.groups, p.N);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (w.total > static_cast<size_t>(VH_STATIC_SCRATCH_BYTES)) return VH_ESCRATCH;
   unsigned char* ws = static_cast<unsigned char*>(static_scratch_address());
   if (!ws) return VH_ECUDA;
@@ -431,7 +519,7 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (vh::launch_decode_attn(p, st) != cudaSuccess) return VH_ECUDA;
+  if (vh::launch_decode_attn(p, st, false) != cudaSuccess) return VH_ECUDA;
   vh::CombineParams c{};
   c.plan = p.plan;
   c.part_lse = p.part_lse;

@@ -31,7 +31,8 @@ struct RopeAppendParams {
 // Shared-memory plan of the attention kernel (byte offsets from the dynamic
 // shared-memory base) and the split plan parameters.
 struct AttnParams {
-  const float* q_rot;
+  // attention over the cache (both kernels)
+  const float* q_rot;          // [B][Hq][D] fp32 rotated q (three-call path)
   const uint16_t* k_cache;
   const uint16_t* v_cache;
   long long page_stride;
@@ -42,23 +43,36 @@ struct AttnParams {
   const int32_t* seq_lens;
   const int32_t* active;
   uint16_t* out;
-  float scale_log2;   // softmax scale * log2(e)
-  int4* plan;         // [B]: first CTA, last CTA, slot used in the first CTA, tiles
-  float* part_o;      // [groups][N][2][Hc*G][D]
-  float* part_lse;    // [groups][N][2][Hc*G]   (base-2 log-sum-exp)
+  float scale_log2;            // softmax scale * log2(e)
+  int4* plan;                  // [B] split plan (three-call path)
+  int* counters;               // [groups][B] pieces delivered per row (fused path; zero between calls)
+  float* part_o;               // [groups][N][2][Hc*G][D]
+  float* part_lse;             // [groups][N][2][Hc*G]   (base-2 log-sum-exp)
   int32_t* err_flag;
+  // fused step only: RoPE of q and k, append of the new token, in-kernel combine
+  const uint16_t* q;           // [B][Hq][D] bf16 new queries
+  const uint16_t* k_new;       // [B][Hkv][D]
+  const uint16_t* v_new;       // [B][Hkv][D]
+  const float* cos_sin;        // [max_pos][D]
+  int max_pos;
+  const int32_t* positions;    // [B] or null (seq_len - 1)
+  uint16_t* k_cache_w;         // writable views of the cache for the append
+  uint16_t* v_cache_w;
+  // shapes and plan
   int B, Hq, Hkv, D, G, P;
-  int Hc;             // kv heads per CTA = consumer warps
-  int groups;         // Hkv / Hc (gridDim.y)
-  int N;              // CTAs per group (gridDim.x)
+  int Hc;                      // kv heads per CTA = consumer warps
+  int groups;                  // Hkv / Hc (gridDim.y)
+  int N;                       // CTAs per group (gridDim.x)
   int stages;
-  int min_tiles;      // lower bound on tiles per CTA when the work list is short
-  int k_row_bytes;    // padded shared-memory stride of a K row (token)
-  int v_row_bytes;    // shared-memory stride of a V row
-  int row_copy_bytes; // bytes copied per token row (Hc * D * 2)
+  int min_tiles;               // lower bound on tiles per CTA when the work list is short
+  int k_row_bytes;             // padded shared-memory stride of a K row (token)
+  int v_row_bytes;             // padded shared-memory stride of a V row
+  int row_copy_bytes;          // bytes copied per token row (Hc * D * 2)
   int stage_bytes;
-  int q_off, p_off, cum_off, len_off, bar_off;
+  int q_bytes;                 // bytes of the q staging buffer
+  int q_off, cum_off, len_off, pos_off, meta_off, bar_off;
   int smem_bytes;
+  int fused;
 };
 
 struct CombineParams {
@@ -71,8 +85,8 @@ struct CombineParams {
 
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, cudaStream_t stream);
 cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream);
-cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device
-cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
+cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device, both variants
+cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream_t stream);
 cudaError_t decode_attn_occupancy(const AttnParams& p, int* blocks_per_sm);
 

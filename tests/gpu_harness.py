@@ -27,9 +27,15 @@ def vh():
     return v
 
 
-def run_step(inp, *, num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, graph=False):
-    """Run RoPE+append, attention and combine on `inp` (CPU or CUDA DecodeInputs).
+PATHS = ("three", "fused")
 
+
+def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, graph=False,
+             repeat=1, pdl=False):
+    """Run one decode step on `inp` (CPU or CUDA DecodeInputs) through the C interface.
+
+    path "three": vh_rope_kv_append + vh_paged_decode_attn + vh_decode_combine;
+    path "fused": vh_decode_fused (one launch; q_rot is not produced).
     Returns dict(q_rot, out, pool_after, err) on the CPU; `inp` is not modified.
     """
     v = vh()
@@ -47,9 +53,15 @@ def run_step(inp, *, num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, gra
     k_cache, v_cache = g.pool[:, 0], g.pool[:, 1]
 
     def step():
-        v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
-                      g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
-                      err_flag=err)
+        for _ in range(repeat):
+            if path == "fused":
+                v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
+                                  g.active, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
+                                  err_flag=err, pdl=pdl)
+            else:
+                v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
+                              g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
+                              err_flag=err)
 
     if graph:
         # first call outside capture (sets per-device launch attributes)
@@ -150,14 +162,16 @@ def check_q_rot(inp, ref_q_rot, gpu_q_rot):
     return err.max().item()
 
 
-def full_check(inp, *, num_ctas=0, rows=None, positions=None, sm_scale=0.0, graph=False, max_pos=None):
-    """Run the GPU path and the oracle on `inp`; check q_rot, append bits and out."""
+def full_check(inp, *, path="three", num_ctas=0, rows=None, positions=None, sm_scale=0.0, graph=False,
+               max_pos=None, repeat=1, pdl=False):
+    """Run the GPU path and the oracle on `inp`; check q_rot (three-call path),
+    the append bits and the output."""
     cpu = inp.to("cpu")
     ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale)
-    got = run_step(inp, num_ctas=num_ctas, positions=positions, sm_scale=sm_scale, graph=graph,
-                   max_pos=max_pos)
+    got = run_step(inp, path=path, num_ctas=num_ctas, positions=positions, sm_scale=sm_scale, graph=graph,
+                   max_pos=max_pos, repeat=repeat, pdl=pdl)
     assert got["err"] == 0, f"device error flag {got['err']}"
     exempt, n_diff = check_append(cpu, ref, got["pool_after"])
-    qerr = check_q_rot(cpu, ref["q_rot"], got["q_rot"])
+    qerr = check_q_rot(cpu, ref["q_rot"], got["q_rot"]) if path == "three" else 0.0
     oerr = check_out(cpu, ref["out"], got["out"], rows=rows)
     return {"exempt": exempt, "n_diff": n_diff, "q_rot_err": qerr, "out_err": oerr, "got": got, "ref": ref}

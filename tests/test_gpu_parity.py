@@ -1,6 +1,8 @@
-"""Parity of the CUDA path (through the C interface) with the float64 oracle.
+"""Parity of the CUDA paths (through the C interface) with the float64 oracle.
 
-All five serving workloads at full size, plus edge cases: single-key rows,
+Both paths are checked: the three calls (RoPE + append, attention, combine)
+and the fused one-launch step.  All five serving workloads at full size,
+plus edge cases: single-key rows,
 exact-tile lengths, the maximum length, padding batches, every GQA group
 size, head_dim 64 and 128, several page sizes, head groups split across
 CTAs, forced split counts, explicit positions and scale, CUDA-graph replay,
@@ -18,25 +20,28 @@ pytestmark = pytest.mark.gpu
 
 # ---------------------------------------------------------------- the five workloads
 
+@pytest.mark.parametrize("path", H.PATHS)
 @pytest.mark.parametrize("name", ["tiny", "c64", "padded", "long"])
-def test_workload_full_parity(name):
+def test_workload_full_parity(name, path):
     inp = workloads.make_inputs(name, device="cuda")
-    r = H.full_check(inp)
+    r = H.full_check(inp, path=path)
     print(f"{name}: out max|d| {r['out_err']:.2e}, q_rot max|d| {r['q_rot_err']:.2e}, "
           f"midpoint-exempt K elements {r['exempt']} (differing {r['n_diff']})")
 
 
+@pytest.mark.parametrize("path", H.PATHS)
 @pytest.mark.parametrize("layer", [0, 13, 27])
-def test_high_concurrency_layers(layer):
+def test_high_concurrency_layers(layer, path):
     # 256 rows, pages of 64; every row checked (the oracle runs a layer in seconds)
     inp = workloads.make_inputs("high", layer=layer, device="cuda")
-    H.full_check(inp)
+    H.full_check(inp, path=path)
 
 
-def test_padded_live_pages_bit_identical_outside_appended_slots():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_padded_live_pages_bit_identical_outside_appended_slots(path):
     inp = workloads.make_inputs("padded", device="cuda")
     before = H.bits16(inp.pool.cpu())
-    got = H.run_step(inp)
+    got = H.run_step(inp, path=path)
     after = H.bits16(got["pool_after"])
     changed = before != after
     allowed = torch.zeros_like(changed)
@@ -57,47 +62,55 @@ def case(lens, *, active=None, Hq=8, Hkv=2, D=128, P=16, seed=1, mps=None, **kw)
                                max_pages_per_seq=mps, seed=seed, device="cuda", **kw)
 
 
-def test_single_key_rows_return_v_new_bit_exactly():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_single_key_rows_return_v_new_bit_exactly(path):
     inp = case([1, 1, 1, 1, 1], Hq=16, Hkv=8)
-    r = H.full_check(inp)
+    r = H.full_check(inp, path=path)
     G = inp.Hq // inp.Hkv
     v_new = inp.v_new.cpu()
     for g in range(inp.Hq):
         assert torch.equal(r["got"]["out"][:, g], v_new[:, g // G])
 
 
+@pytest.mark.parametrize("path", H.PATHS)
 @pytest.mark.parametrize("lens", [[16, 32, 48, 160], [15, 17, 31, 33], [2, 3, 4, 1000], [4096, 1, 77]])
-def test_tile_boundaries(lens):
-    H.full_check(case(lens, seed=sum(lens)))
+def test_tile_boundaries(lens, path):
+    H.full_check(case(lens, seed=sum(lens)), path=path)
 
 
+@pytest.mark.parametrize("path", H.PATHS)
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("D", [64, 128])
-def test_gqa_groups_and_head_dims(G, D):
+def test_gqa_groups_and_head_dims(G, D, path):
     Hkv = 2
-    H.full_check(case([37, 300, 129, 1], Hq=G * Hkv, Hkv=Hkv, D=D, seed=G * 10 + D))
+    H.full_check(case([37, 300, 129, 1], Hq=G * Hkv, Hkv=Hkv, D=D, seed=G * 10 + D), path=path)
 
 
+@pytest.mark.parametrize("path", H.PATHS)
 @pytest.mark.parametrize("P", [16, 32, 64, 128, 256])
-def test_page_sizes(P):
-    H.full_check(case([1, P - 1, P, P + 1, 3 * P + 5], P=P, Hq=8, Hkv=4, seed=P))
+def test_page_sizes(P, path):
+    H.full_check(case([1, P - 1, P, P + 1, 3 * P + 5], P=P, Hq=8, Hkv=4, seed=P), path=path)
 
 
-def test_head_groups_split_across_ctas():
-    # Hkv * D > 1024: two CTAs per tile range, each owning 8 kv heads
-    H.full_check(case([200, 513, 17], Hq=32, Hkv=16, D=128, seed=5))
-    H.full_check(case([90, 33], Hq=32, Hkv=32, D=64, seed=6))
+@pytest.mark.parametrize("path", H.PATHS)
+def test_head_groups_split_across_ctas(path):
+    # Hkv * D > 1024: several CTAs per tile range, each owning a group of kv heads
+    H.full_check(case([200, 513, 17], Hq=32, Hkv=16, D=128, seed=5), path=path)
+    H.full_check(case([90, 33], Hq=32, Hkv=32, D=64, seed=6), path=path)
+    H.full_check(case([300, 41], Hq=64, Hkv=8, D=128, seed=7), path=path)   # G = 8
 
 
-def test_maximum_length_row():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_maximum_length_row(path):
     mps = 64
-    H.full_check(case([mps * 16, 5, mps * 16 - 1], mps=mps, seed=7))
+    H.full_check(case([mps * 16, 5, mps * 16 - 1], mps=mps, seed=7), path=path)
 
 
+@pytest.mark.parametrize("path", H.PATHS)
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 1000])
-def test_forced_cta_counts_agree(num_ctas):
+def test_forced_cta_counts_agree(num_ctas, path):
     inp = workloads.make_inputs("c64", device="cuda")
-    H.full_check(inp, num_ctas=num_ctas)
+    H.full_check(inp, num_ctas=num_ctas, path=path)
 
 
 def test_split_count_changes_only_rounding():
@@ -108,37 +121,68 @@ def test_split_count_changes_only_rounding():
     assert ((a - b).abs() <= 2 * (H.ATOL + H.RTOL * a.abs())).all()
 
 
-def test_explicit_positions_and_scale():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_explicit_positions_and_scale(path):
     inp = case([40, 300, 2], seed=9)
     pos = torch.tensor([7, 1000, 0], dtype=torch.int32)
-    H.full_check(inp, positions=pos, sm_scale=0.05, max_pos=2048)
+    H.full_check(inp, positions=pos, sm_scale=0.05, max_pos=2048, path=path)
 
 
-def test_all_padding_batch():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_all_padding_batch(path):
     inp = case([1, 1, 1], active=[0, 0, 0], seed=10)
-    r = H.full_check(inp)
+    r = H.full_check(inp, path=path)
     assert not r["got"]["out"].any()
 
 
-def test_batch_of_one_and_deterministic():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_batch_of_one_and_deterministic(path):
     inp = case([777], seed=11)
-    a = H.run_step(inp)
-    b = H.run_step(inp)
-    assert torch.equal(a["out"], b["out"]) and torch.equal(a["q_rot"], b["q_rot"])
-    H.full_check(inp)
+    a = H.run_step(inp, path=path)
+    b = H.run_step(inp, path=path)
+    assert torch.equal(a["out"], b["out"])
+    if path == "three":
+        assert torch.equal(a["q_rot"], b["q_rot"])
+    H.full_check(inp, path=path)
 
 
-def test_cuda_graph_replay_matches():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_cuda_graph_replay_matches(path):
     inp = workloads.make_inputs("padded", device="cuda")
-    H.full_check(inp, graph=True)
+    H.full_check(inp, graph=True, path=path)
 
 
-def test_identical_keys_give_mean_of_values():
+def test_fused_repeated_calls_reuse_the_workspace():
+    # the per-row counters of the fused merge must come back to zero after each call
+    inp = workloads.make_inputs("long", device="cuda")
+    H.full_check(inp, path="fused", repeat=3)
+    H.full_check(inp, path="fused", repeat=2, num_ctas=500)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("name", ["c64", "long", "high"])
+def test_fused_programmatic_dependent_launch(name, graph):
+    # back-to-back fused launches, each a programmatic dependent of the previous one
+    inp = workloads.make_inputs(name, device="cuda")
+    H.full_check(inp, path="fused", repeat=3, pdl=True, graph=graph)
+
+
+def test_fused_and_three_call_paths_agree():
+    inp = workloads.make_inputs("c64", device="cuda")
+    a = H.run_step(inp, path="three")
+    b = H.run_step(inp, path="fused")
+    assert torch.equal(H.bits16(a["pool_after"]), H.bits16(b["pool_after"]))
+    d, r = a["out"].double(), b["out"].double()
+    assert ((d - r).abs() <= 2 * (H.ATOL + H.RTOL * r.abs())).all()
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_identical_keys_give_mean_of_values(path):
     inp = case([300, 45], seed=12, poison=True)
     # set every live cached key of kv head 0 to one vector; values stay random
     key = torch.randn(inp.D, device="cuda").to(torch.bfloat16)
     inp.pool[:, 0, :, 0] = torch.where(torch.isnan(inp.pool[:, 0, :, 0].float()), inp.pool[:, 0, :, 0], key)
-    H.full_check(inp)
+    H.full_check(inp, path=path)
 
 
 # ---------------------------------------------------------------- device-side data errors
@@ -147,11 +191,12 @@ def _err_run(inp, **kw):
     return H.run_step(inp, **kw)
 
 
-def test_seq_len_out_of_range_is_flagged_and_row_zeroed():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_seq_len_out_of_range_is_flagged_and_row_zeroed(path):
     inp = case([50, 60, 70], seed=13)
     inp.seq_lens[1] = inp.max_pages_per_seq * inp.P + 5
     inp.seq_lens[2] = 0
-    got = _err_run(inp)
+    got = _err_run(inp, path=path)
     assert got["err"] & 1
     assert not got["out"][1:].any()
     # the healthy row is still right
@@ -162,11 +207,12 @@ def test_seq_len_out_of_range_is_flagged_and_row_zeroed():
     H.check_out(workloads.DecodeInputs(**{**cpu.__dict__, "active": act}), ref["out"], got["out"], rows=[0])
 
 
-def test_page_id_out_of_range_is_flagged_without_writes():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_page_id_out_of_range_is_flagged_without_writes(path):
     inp = case([20, 20], seed=14)
     before = H.bits16(inp.pool.cpu())
     inp.page_table[1, 1] = inp.num_pages + 3   # the page of row 1's new token
-    got = _err_run(inp)
+    got = _err_run(inp, path=path)
     assert got["err"] & 2
     after = H.bits16(got["pool_after"])
     changed = (before != after).nonzero()
@@ -175,8 +221,11 @@ def test_page_id_out_of_range_is_flagged_without_writes():
     assert all(int(c[0]) == p0 and int(c[2]) == off0 for c in changed)
 
 
-def test_position_beyond_table_is_flagged():
+@pytest.mark.parametrize("path", H.PATHS)
+def test_position_beyond_table_is_flagged(path):
     inp = case([20, 30], seed=15)
     pos = torch.tensor([3, 10_000], dtype=torch.int32)
-    got = H.run_step(inp, positions=pos, max_pos=64)
+    got = H.run_step(inp, positions=pos, max_pos=64, path=path)
     assert got["err"] & 4
+    if path == "fused":
+        assert not got["out"][1].any(), "a row with an invalid position is treated as padding"
