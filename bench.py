@@ -1,28 +1,32 @@
-"""Benchmark of one paged q_len=1 decode step (RoPE + append, attention, combine).
+"""Benchmark of the paged q_len=1 decode step (RoPE + append, attention, merge).
 
 Default workload: the c=64 Talker decode batch (64 rows, 16 q / 8 kv heads,
 head_dim 128, pages of 16 tokens, lengths uniform in [200, 1200]).  A "step"
-is the whole path for one layer over the batch: vh_rope_kv_append,
-vh_paged_decode_attn and vh_decode_combine.  Metric: decode tokens/s (active
-rows per second per layer call) and achieved HBM GB/s.
+is the whole path for one layer over the batch.  The headline runs it as one
+launch (vh_decode_fused), each step a programmatic dependent of the previous
+one; the three-call form (vh_rope_kv_append, vh_paged_decode_attn,
+vh_decode_combine) is timed beside it.  Metric: decode tokens/s (active rows
+per layer call per second) and the achieved HBM GB/s of the step.
 
 Timing: inputs resident in HBM; K steps captured in CUDA graphs that cycle
 over enough KV-pool replicas to exceed 4x the L2 size, so every step reads
 its K/V from HBM; CUDA events on the launching stream, synchronize and a
-barrier on both sides, max over ranks.  The attention kernel alone is timed
-the same way for the roofline figure.  `e2e` goes through the public Python
-call with pinned host buffers: per step the new q/k/v, lengths, flags and
-page table are copied in and the output is copied out.
+barrier on both sides, max over ranks.  `e2e` goes through the public Python
+call with pinned host buffers: per step the new q/k/v, lengths, flags and page
+table are copied in and the output is copied out.
 
 --impl reference times the float64 CPU oracle on the host cores instead (each
-step one row of the same workload).
+step one row of the same workload).  --ncu-case runs a few eager launches on
+one pool only (for profiler captures).
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -38,6 +42,8 @@ import workloads  # noqa: E402
 METRIC = "decode-attn tokens/s and achieved HBM GB/s (% of GB300 peak) at c=64"
 WORKLOAD = "c64"
 FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["paged_len_decode_gb300/csrc/decode_attn.cu", "paged_len_decode_gb300/csrc/vh_common.cuh",
+                  "paged_len_decode_gb300/csrc/vh_kernels.h"]
 
 
 def parse():
@@ -49,10 +55,12 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ncu-case", action="store_true",
+                    help="eager launches of the fused and the three-call step on one pool (profiling)")
     return ap.parse_args()
 
 
-def dist_setup(n_gpus):
+def dist_setup():
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
     if world > 1:
         import torch.distributed as dist
@@ -77,16 +85,39 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 def peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        d = json.load(open(path))
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, path: str | None = None):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    if that capture was taken of the current kernel sources; else None."""
+    path = path or os.path.join(ROOT, "profiles", f"decode_fused_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]{16})", text)
+    val = re.search(r"dram bytes per launch \(read \+ write\):\s*([0-9]+)", text)
+    if not sha or not val or sha.group(1) != kernel_source_sha():
+        return None
+    return int(val.group(1))
+
+
 def step_bytes(inp) -> dict:
-    """Algorithmic bytes of one step and of one attention launch."""
+    """Algorithmic bytes of one decode step: K/V of every active row (L_b keys), the
+    new q/k/v, the appended k/v, the output, the page-table entries and the
+    lengths/flags; plus the attention-only variant (fp32 q_rot instead of q/k/v)."""
     lens = inp.seq_lens.cpu().long()
     act = inp.active.cpu().long()
     Lact = lens[act.bool()]
@@ -145,39 +176,61 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def run_ours(args, rank, world):
-    import paged_len_decode_gb300 as vh
+class Setup:
+    """Device buffers of one workload: R pool replicas and the step's outputs."""
 
+    def __init__(self, name: str, rank: int, dev, replicas: int | None = None):
+        import paged_len_decode_gb300 as vh
+        self.vh = vh
+        self.inp = inp = workloads.make_inputs(name, layer=rank, device=dev)
+        self.B, self.Hq, self.Hkv, self.D, self.P = inp.B, inp.Hq, inp.Hkv, inp.D, inp.P
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.pool_bytes = inp.pool.numel() * 2
+        self.R = replicas or max(2, math.ceil(4 * self.l2 / self.pool_bytes))
+        self.pools = [inp.pool] + [inp.pool.clone() for _ in range(self.R - 1)]
+        self.cos_sin = torch.empty((inp.max_pages_per_seq * self.P, self.D), dtype=torch.float32, device=dev)
+        vh.vh_rope_table(self.cos_sin, inp.theta)
+        self.q_rot = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=dev)
+        self.out = torch.empty((self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
+        self.ws3 = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
+        self.wsf = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
+        self.n_ctas = vh.vh_decode_num_ctas(self.B, self.Hq, self.Hkv, self.D, self.P)
+
+    def fused(self, r, pdl=True, src=None):
+        s = src or self.inp
+        self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
+                                s.page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl)
+
+    def three(self, r):
+        i = self.inp
+        self.vh.decode_step(i.q, i.k_new, i.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
+                            i.page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3)
+
+
+def run_ncu_case(args):
+    """A few eager launches on one pool: 3 fused, 3 three-call steps."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = Setup(args.workload, 0, dev, replicas=1)
+    for _ in range(3):
+        s.fused(0, pdl=False)
+    for _ in range(3):
+        s.three(0)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": args.workload, "ok": True}))
+
+
+def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
-    inp = workloads.make_inputs(args.workload, layer=rank, device=dev)
-    B, Hq, Hkv, D, P = inp.B, inp.Hq, inp.Hkv, inp.D, inp.P
+    s = Setup(args.workload, rank, dev)
+    inp, R = s.inp, s.R
     by = step_bytes(inp)
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool_bytes = inp.pool.numel() * 2
-    R = max(2, math.ceil(4 * l2 / pool_bytes))
-    pools = [inp.pool] + [inp.pool.clone() for _ in range(R - 1)]
-
-    max_pos = inp.max_pages_per_seq * P
-    cos_sin = torch.empty((max_pos, D), dtype=torch.float32, device=dev)
-    vh.vh_rope_table(cos_sin, inp.theta)
-    q_rot = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
-    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-    ws = vh.alloc_workspace(B, Hq, Hkv, D, P, device=dev)
-    n_ctas = vh.vh_decode_num_ctas(B, Hq, Hkv, D, P)
-
-    def step(r):
-        vh.decode_step(inp.q, inp.k_new, inp.v_new, cos_sin, pools[r][:, 0], pools[r][:, 1], inp.page_table,
-                       inp.seq_lens, inp.active, q_rot, out, ws)
-
-    def attn_only(r):
-        vh.vh_paged_decode_attn(q_rot, pools[r][:, 0], pools[r][:, 1], inp.page_table, inp.seq_lens,
-                                inp.active, out, ws)
-
-    for r in range(R):  # first calls outside capture; also fills every replica's new slot
-        step(r)
+    for r in range(R):  # first calls outside capture (launch attributes, every replica's new slot)
+        s.three(r)
+        s.fused(r, pdl=False)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
@@ -216,40 +269,40 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         ck = clocks.stop() if clocks else None
         barrier(world)
-        ms = e0.elapsed_time(e1)
-        return max_over_ranks(ms, world), ck
+        return max_over_ranks(e0.elapsed_time(e1), world), ck
 
-    # warm-up steps (untimed)
-    for i in range(args.warmup):
-        step(i % R)
+    for i in range(args.warmup):  # untimed warm-up steps
+        s.fused(i % R)
+        s.three(i % R)
     torch.cuda.synchronize()
 
     clocks = Clocks(dev.index)
-    ms_total, ck = timed(step, args.steps, clocks)
-    ms_step = ms_total / args.steps
-    ms_attn_total, _ = timed(attn_only, args.steps)
-    ms_attn = ms_attn_total / args.steps
+    ms_fused_total, ck = timed(s.fused, args.steps, clocks)
+    ms_step = ms_fused_total / args.steps
+    ms_three_total, _ = timed(s.three, args.steps)
+    ms_three = ms_three_total / args.steps
 
     tokens_per_s = by["active"] * world / (ms_step * 1e-3)
     step_gbs = by["step"] / (ms_step * 1e-3) / 1e9
-    attn_gbs = by["attn"] / (ms_attn * 1e-3) / 1e9
     peak, peak_kind = peaks()
 
-    # ---- e2e through the public call with host buffers ----
+    # ---- e2e through the public call with host buffers (one fused launch per step) ----
     pin = lambda t: t.cpu().pin_memory()
-    h_in = {k: pin(getattr(inp, k)) for k in ("q", "k_new", "v_new", "page_table", "seq_lens", "active")}
-    d_in = {k: torch.empty_like(getattr(inp, k)) for k in h_in}
-    h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    names = ("q", "k_new", "v_new", "page_table", "seq_lens", "active")
+    h_in = {k: pin(getattr(inp, k)) for k in names}
+    d_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
+        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool")},
+        **{k: torch.empty_like(getattr(inp, k)) for k in names}})
+    h_out = torch.empty((s.B, s.Hq, s.D), dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = h_out.numel() * h_out.element_size()
     K_e2e = min(args.steps, 2000)
 
     def e2e_step(r):
-        for k in h_in:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        vh.decode_step(d_in["q"], d_in["k_new"], d_in["v_new"], cos_sin, pools[r][:, 0], pools[r][:, 1],
-                       d_in["page_table"], d_in["seq_lens"], d_in["active"], q_rot, out, ws)
-        h_out.copy_(out, non_blocking=True)
+        for k in names:
+            getattr(d_in, k).copy_(h_in[k], non_blocking=True)
+        s.fused(r, pdl=False, src=d_in)
+        h_out.copy_(s.out, non_blocking=True)
 
     for i in range(10):
         e2e_step(i % R)
@@ -271,22 +324,28 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "accum_dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: B={B} (active {by['active']}), Hq={Hq}, Hkv={Hkv}, "
-                               f"D={D}, P={P}, lengths {w.dist} [{w.len_lo},{w.len_hi}]",
-                   "global_batch": B * world, "kv_bytes_per_step": by["kv"],
+        "config": {"workload": f"{args.workload}: B={s.B} (active {by['active']}), Hq={s.Hq}, Hkv={s.Hkv}, "
+                               f"D={s.D}, P={s.P}, lengths {w.dist} [{w.len_lo},{w.len_hi}]",
+                   "global_batch": s.B * world, "kv_bytes_per_step": by["kv"],
+                   "step": "one vh_decode_fused launch (RoPE+append+attention+merge), PDL between steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"{R} KV-pool replicas cycled ({R * pool_bytes / 1e6:.0f} MB >= 4x L2 "
-                         f"{l2 / 1e6:.0f} MB): inputs larger than L2",
-                   "ctas": n_ctas},
+                   "l2": f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB >= 4x L2 "
+                         f"{s.l2 / 1e6:.0f} MB): inputs larger than L2",
+                   "ctas": s.n_ctas},
         "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode_attn_kernel", "achieved": round(attn_gbs, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(attn_gbs / peak, 4), "traffic": None,
-                     "peak_kind": peak_kind, "ms_per_launch": round(ms_attn, 6),
-                     "algorithmic_bytes_per_launch": by["attn"]},
+        "roofline": {"bound": "hbm", "kernel": f"decode_attn_kernel<{s.D},{s.Hq // s.Hkv},1> (fused step)",
+                     "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(step_gbs / peak, 4), "traffic": recorded_traffic(args.workload),
+                     "peak_kind": peak_kind, "ms_per_launch": round(ms_step, 6),
+                     "algorithmic_bytes_per_launch": by["step"]},
+        "three_call": {"ms_per_step": round(ms_three, 6),
+                       "value": round(by["active"] * world / (ms_three * 1e-3), 1), "unit": "tokens/s",
+                       "launches_per_step": 3},
         "clocks": ck,
         "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": K_e2e},
-        "gpu_launches": 3 * args.steps,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": K_e2e,
+                "call": "paged_len_decode_gb300.vh_decode_fused, eager, pinned host buffers"},
+        "gpu_launches": args.steps,
     }
     return res, inp
 
@@ -316,12 +375,15 @@ def cpu_oracle_rate(inp_cpu, seconds: float, max_steps: int | None = None):
 
 def main():
     args = parse()
-    rank, world = dist_setup(args.gpus)
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
+    rank, world = dist_setup()
     if args.impl == "reference":
         if rank != 0:
             return
         inp = workloads.make_inputs(args.workload, device="cpu")
-        cpu_oracle_rate(inp, 0, max_steps=max(3, args.warmup) if args.warmup else 3)
+        cpu_oracle_rate(inp, 0, max_steps=max(3, args.warmup))
         rate, n, el, cores = cpu_oracle_rate(inp, 0, max_steps=args.steps)
         res = {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "tokens/s",
                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
