@@ -13,7 +13,9 @@ over enough KV-pool replicas to exceed 4x the L2 size, so every step reads
 its K/V from HBM; CUDA events on the launching stream, synchronize and a
 barrier on both sides, max over ranks.  `e2e` goes through the public Python
 call with pinned host buffers: per step the new q/k/v, lengths, flags and page
-table are copied in and the output is copied out.
+table (one input arena) are copied in and the output is copied out, captured
+as one CUDA graph per step the way a serving runtime replays its decode graph
+(`e2e.eager` issues the same copies and call from Python each step).
 
 --impl reference times the float64 CPU oracle on the host cores instead (each
 step one row of the same workload).  --ncu-case runs a few eager launches on
@@ -287,36 +289,64 @@ def run_ours(args, rank, world):
     peak, peak_kind = peaks()
 
     # ---- e2e through the public call with host buffers (one fused launch per step) ----
-    pin = lambda t: t.cpu().pin_memory()
+    # The step's inputs live in one pinned host arena and one device arena (the
+    # way a serving runtime stages a step), so each step is one host->device
+    # copy, the call, and one device->host copy of the output.
     names = ("q", "k_new", "v_new", "page_table", "seq_lens", "active")
-    h_in = {k: pin(getattr(inp, k)) for k in names}
+    offs, total = {}, 0
+    for k in names:
+        t = getattr(inp, k)
+        offs[k] = total
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    h_arena = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    d_arena = torch.zeros(total, dtype=torch.uint8, device=dev)
+    views = {}
+    for k in names:
+        t = getattr(inp, k)
+        n = t.numel() * t.element_size()
+        h_arena[offs[k]:offs[k] + n].copy_(t.contiguous().view(torch.uint8).view(-1).cpu())
+        views[k] = d_arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
     d_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
-        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool")},
-        **{k: torch.empty_like(getattr(inp, k)) for k in names}})
+        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool")}, **views})
     h_out = torch.empty((s.B, s.Hq, s.D), dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    h2d = total
     d2h = h_out.numel() * h_out.element_size()
     K_e2e = min(args.steps, 2000)
 
     def e2e_step(r):
-        for k in names:
-            getattr(d_in, k).copy_(h_in[k], non_blocking=True)
+        d_arena.copy_(h_arena, non_blocking=True)
         s.fused(r, pdl=False, src=d_in)
         h_out.copy_(s.out, non_blocking=True)
 
-    for i in range(10):
-        e2e_step(i % R)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(K_e2e):
-        e2e_step(i % R)
-    e1.record()
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world) / K_e2e
+    def e2e_time(run_step, K):
+        for i in range(3):
+            run_step(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(K):
+            run_step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        return max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world) / K
+
+    # eager: the Python call issued per step
+    e2e_eager_ms = e2e_time(lambda i: e2e_step(i % R), K_e2e)
+    # serving pattern: one CUDA graph per step (host->device copies of the step's
+    # inputs, the fused call, device->host copy of the output), replayed each step
+    graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                e2e_step(r)
+        torch.cuda.current_stream().wait_stream(stream)
+        graphs.append(g)
+    e2e_ms = e2e_time(lambda i: graphs[i % R].replay(), K_e2e)
     e2e_tps = by["active"] * world / (e2e_ms * 1e-3)
 
     res = {
@@ -344,7 +374,10 @@ def run_ours(args, rank, world):
         "clocks": ck,
         "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": K_e2e,
-                "call": "paged_len_decode_gb300.vh_decode_fused, eager, pinned host buffers"},
+                "call": "paged_len_decode_gb300.vh_decode_fused in a per-step CUDA graph with one "
+                        "pinned-host->device copy of the step's input arena and one output copy",
+                "eager": {"value": round(by["active"] * world / (e2e_eager_ms * 1e-3), 1),
+                          "ms_per_step": round(e2e_eager_ms, 6)}},
         "gpu_launches": args.steps,
     }
     return res, inp

@@ -95,15 +95,12 @@ __device__ void block_inclusive_scan(int* cum, int n, int* warp_tot) {
 
 enum { kMiscWarpTot = 0, kMiscAbort = 32, kMiscNVerdict = 33, kMiscVerdict = 34, kMiscInts = 48 };
 
-__device__ __forceinline__ float bf16_at(const unsigned char* base, int idx) {
-  return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(base)[idx]) << 16);
-}
-
 // Merge the partial results of one row for the G q heads of one kv head (one
 // warp): piece j comes from CTA cf + j, slot `first_slot` for j == 0 and slot
-// 0 otherwise; lse in base 2.  M = max_j lse_j, w_j = 2^(lse_j - M),
-// o = sum_j w_j o_j / sum_j w_j.  Loads are issued a chunk of pieces at a
-// time (and bypass L1: other CTAs wrote them during this launch).
+// 0 otherwise; lse in base 2.  o = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M)
+// with M the running max, so each batch of U pieces costs one round trip: its
+// lse and o loads are all issued before any is used (they bypass L1: other
+// CTAs wrote them during this launch).
 template <int D, int G>
 __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse, const float* __restrict__ part_o,
                                              long long slot_base /* (gy * N) * 2 */, int HG, int wg /* w * G */,
@@ -111,24 +108,14 @@ __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse,
                                              int lane) {
   constexpr int PER = D / 32;
   constexpr int U = 16 / G;  // pieces per batch of loads
+  const float NEG_INF = __int_as_float(0xff800000);
   auto idx_of = [&](int j) -> long long {
     return (slot_base + 2LL * (cf + j) + (j == 0 ? first_slot : 0)) * HG + wg;
   };
-  float M[G];
-#pragma unroll
-  for (int n = 0; n < G; ++n) M[n] = __int_as_float(0xff800000);
-  for (int j = lane; j < np; j += 32) {
-    const long long ix = idx_of(j);
-#pragma unroll
-    for (int n = 0; n < G; ++n) M[n] = fmaxf(M[n], __ldcg(part_lse + ix + n));
-  }
-#pragma unroll
-  for (int n = 0; n < G; ++n)
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M[n] = fmaxf(M[n], __shfl_xor_sync(0xffffffffu, M[n], off));
-  float o[G][PER], ws[G];
+  float M[G], o[G][PER], ws[G];
 #pragma unroll
   for (int n = 0; n < G; ++n) {
+    M[n] = NEG_INF;
     ws[n] = 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) o[n][i] = 0.f;
@@ -141,7 +128,7 @@ __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse,
       const long long ix = j < np ? idx_of(j) : idx_of(j0);
 #pragma unroll
       for (int n = 0; n < G; ++n) {
-        lv[u][n] = j < np ? __ldcg(part_lse + ix + n) : __int_as_float(0xff800000);
+        lv[u][n] = j < np ? __ldcg(part_lse + ix + n) : NEG_INF;
         const float* src = part_o + (ix + n) * D + lane * PER;
         if constexpr (PER == 4) {
           const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
@@ -157,14 +144,23 @@ __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse,
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int n = 0; n < G; ++n) {
+      float mb = M[n];
 #pragma unroll
-      for (int n = 0; n < G; ++n) {
-        const float wgt = exp2f(lv[u][n] - M[n]);  // 0 for the padding entries of the last chunk
+      for (int u = 0; u < U; ++u) mb = fmaxf(mb, lv[u][n]);
+      const float sc = exp2f(M[n] - mb);  // 0 on the first batch (M = -inf)
+      ws[n] *= sc;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) o[n][i] *= sc;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float wgt = exp2f(lv[u][n] - mb);  // 0 for the padding entries of the last batch
         ws[n] += wgt;
 #pragma unroll
         for (int i = 0; i < PER; ++i) o[n][i] += wgt * v[u][n][i];
       }
+      M[n] = mb;
+    }
   }
 #pragma unroll
   for (int n = 0; n < G; ++n) {
@@ -318,14 +314,13 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         const int rb = rows[k];
         const long long s0 = cum[rb], s1 = cum[rb + 1] - 1;
         const int cf = cta_of(s0, n_eff, T), cl = cta_of(s1, n_eff, T);
-        __threadfence();  // the consumers' partial writes (ordered by the barrier) before the count
+        // acquire-release at GPU scope: publishes the consumers' partial writes
+        // (ordered before it by the stage barrier) and, for the last arrival,
+        // makes every other piece visible to the merge that follows
         int* counter = p.counters + static_cast<long long>(gy) * p.B + rb;
-        const int old = atomicAdd(counter, 1);
+        const int old = atom_add_acq_rel_gpu(counter, 1);
         const int last = (old == cl - cf);
-        if (last) {
-          *counter = 0;  // every piece has arrived: ready for the next call
-          __threadfence();
-        }
+        if (last) *counter = 0;  // every piece has arrived: ready for the next call
         int* v = misc + kMiscVerdict + 5 * k;
         v[0] = last;
         v[1] = rb;
@@ -394,14 +389,15 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_bytes));
+          // the q rows of the segment's row (one contiguous copy) and, fused, the RoPE row
+          mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));
           const long long qrow = static_cast<long long>(b) * p.Hq + static_cast<long long>(h0) * G;
+          const uint32_t qdst = smem_addr(smem + p.q_off);
           if constexpr (FUSED) {
-            bulk_g2s(smem_addr(smem + p.q_off), p.q + qrow * D, HG * D * 2, qfull);
-            bulk_g2s(smem_addr(smem + p.q_off + HG * D * 2), p.cos_sin + static_cast<long long>(posv[b]) * D,
-                     D * 4, qfull);
+            bulk_g2s(qdst, p.q + qrow * D, HG * D * 2, qfull);
+            bulk_g2s(qdst + HG * p.q_row_bytes, p.cos_sin + static_cast<long long>(posv[b]) * D, D * 4, qfull);
           } else {
-            bulk_g2s(smem_addr(smem + p.q_off), p.q_rot + qrow * D, HG * D * 4, qfull);
+            bulk_g2s(qdst, p.q_rot + qrow * D, HG * D * 4, qfull);
           }
         }
         ++nseg;
@@ -497,33 +493,50 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         return;
       }
       const unsigned char* qb = smem + p.q_off;
-      const int n = g4;  // q head (within the group) of this lane's operand column
+      const float* cs = reinterpret_cast<const float*>(qb + HG * p.q_row_bytes);  // fused: RoPE row
+      // fused: (1) all 32 lanes rotate this warp's G q rows (rotate-half RoPE in
+      // fp32, pairs (i, i + D/2)) into padded per-warp fp32 rows (D*4 + 32 bytes)
+      // so that (2) every lane reads its operand pairs without bank conflicts.
+      // Three-call path: the staged rows are fp32 already and are read directly.
+      constexpr int QS_ROW = D * 4 + 32;
+      const unsigned char* qsrc;
+      int qstride;
+      if constexpr (FUSED) {
+        unsigned char* qs = smem + p.qs_off + w * G * QS_ROW;
+        for (int e = lane; e < G * D / 4; e += 32) {  // two pairs per step
+          const int n = e / (D / 4);
+          const int i = (e % (D / 4)) * 2;            // i, i+1 in [0, D/2)
+          const unsigned char* row = qb + (w * G + n) * p.q_row_bytes;
+          const float2 xv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * i));
+          const float2 yv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * (i + D / 2)));
+          const float2 cv = *reinterpret_cast<const float2*>(cs + i);
+          const float2 sv = *reinterpret_cast<const float2*>(cs + D / 2 + i);
+          float* dst = reinterpret_cast<float*>(qs + n * QS_ROW);
+          *reinterpret_cast<float2*>(dst + i) = make_float2(xv.x * cv.x - yv.x * sv.x, xv.y * cv.y - yv.y * sv.y);
+          *reinterpret_cast<float2*>(dst + i + D / 2) =
+              make_float2(yv.x * cv.x + xv.x * sv.x, yv.y * cv.y + xv.y * sv.y);
+        }
+        __syncwarp();
+        qsrc = qs;
+        qstride = QS_ROW;
+      } else {
+        qsrc = qb + w * G * p.q_row_bytes;
+        qstride = p.q_row_bytes;
+      }
+      // (2) each lane takes its operand pairs: head g4, dims 16k + 2 t4 (+1) and +8 (+9)
+      const int n = g4;
+      const float* qrow = reinterpret_cast<const float*>(qsrc + (n < G ? n : 0) * qstride);
 #pragma unroll
       for (int k = 0; k < KSTEPS; ++k) {
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 a = make_float2(0.f, 0.f), c2 = make_float2(0.f, 0.f);
         if (n < G) {
-          const int dd[4] = {16 * k + 2 * t4, 16 * k + 2 * t4 + 1, 16 * k + 2 * t4 + 8, 16 * k + 2 * t4 + 9};
-          const int row = (w * G + n) * D;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if constexpr (FUSED) {
-              const float* cs = reinterpret_cast<const float*>(qb + HG * D * 2);
-              const int d = dd[e];
-              const int i = d < D / 2 ? d : d - D / 2;
-              const float cv = cs[i], sv = cs[D / 2 + i];
-              const float xv = bf16_at(qb, row + d);
-              const float yv = bf16_at(qb, row + (d < D / 2 ? d + D / 2 : d - D / 2));
-              x[e] = d < D / 2 ? xv * cv - yv * sv : xv * cv + yv * sv;
-            } else {
-              x[e] = reinterpret_cast<const float*>(qb)[row + dd[e]];
-            }
-          }
+          a = *reinterpret_cast<const float2*>(qrow + 16 * k + 2 * t4);
+          c2 = *reinterpret_cast<const float2*>(qrow + 16 * k + 2 * t4 + 8);
         }
-        split_bf16x2(x[0], x[1], qh[k][0], ql[k][0]);
-        split_bf16x2(x[2], x[3], qh[k][1], ql[k][1]);
+        split_bf16x2(a.x, a.y, qh[k][0], ql[k][0]);
+        split_bf16x2(c2.x, c2.y, qh[k][1], ql[k][1]);
       }
       if constexpr (FUSED) {
-        const float* cs = reinterpret_cast<const float*>(qb + HG * D * 2);
 #pragma unroll
         for (int j = 0; j < (D / 2 + 31) / 32; ++j) {
           const int i = lane + 32 * j;
@@ -722,7 +735,6 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       for (int k = 0; k < nv; ++k) {
         const int* v = misc + kMiscVerdict + 5 * k;
         if (!v[0]) continue;
-        __threadfence();
         merge_pieces<D, G>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, v[2],
                            v[3] - v[2] + 1, v[4],
                            p.out + (static_cast<long long>(v[1]) * p.Hq + static_cast<long long>(h) * G) * D, lane);

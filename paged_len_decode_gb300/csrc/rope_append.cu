@@ -33,11 +33,11 @@ __global__ void rope_table_kernel(float* __restrict__ cos_sin, int max_pos, int 
   }
 }
 
-// One CTA per row.  Work units: each thread rotates 4 consecutive pairs
+// One CTA per row (up to 1024 threads).  Work units: each thread rotates 4 consecutive pairs
 // (elements i..i+3 and i+D/2..i+D/2+3) of one head; heads 0..Hq-1 are q heads
 // (written to q_rot), heads Hq..Hq+Hkv-1 are the new k (written to the cache).
 // V is copied 16 bytes per thread.
-__global__ void __launch_bounds__(128) rope_kv_append_kernel(RopeAppendParams p) {
+__global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p) {
   const int b = blockIdx.x;
   if (!p.active[b]) return;
   const int L = p.seq_lens[b];
@@ -117,7 +117,11 @@ cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, 
 }
 
 cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream) {
-  rope_kv_append_kernel<<<p.B, 128, 0, stream>>>(p);
+  // one pass over all heads of a row when it fits in one CTA (a thread per 4 rotation pairs)
+  const int units = (p.Hq + p.Hkv) * (p.D / 8);
+  int threads = ((units + 31) / 32) * 32;
+  threads = threads < 128 ? 128 : (threads > 1024 ? 1024 : threads);
+  rope_kv_append_kernel<<<p.B, threads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -107,8 +107,12 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
     p.v_row_bytes = p.row_copy_bytes + 16;
     p.stage_bytes = static_cast<int>(align_up(16 * static_cast<size_t>(p.k_row_bytes + p.v_row_bytes), 128));
     const size_t hg = static_cast<size_t>(hc) * p.G;
-    p.q_bytes = static_cast<int>(fused ? hg * p.D * 2 + p.D * 4 : hg * p.D * 4);
-    fixed = align_up(p.q_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
+    // staged q rows, contiguous: one bulk copy per segment
+    p.q_row_bytes = fused ? p.D * 2 : p.D * 4;
+    p.q_tx_bytes = static_cast<int>(fused ? hg * p.D * 2 + p.D * 4 : hg * p.D * 4);
+    p.q_bytes = static_cast<int>(hg * p.q_row_bytes + (fused ? p.D * 4 : 0));
+    const size_t qs_bytes = fused ? static_cast<size_t>(hc) * p.G * (p.D * 4 + 32) : 0;
+    fixed = align_up(p.q_bytes, 128) + align_up(qs_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
             2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256;
     stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
     if (stages >= 3 || hc == 1) break;
@@ -124,6 +128,8 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   size_t off = static_cast<size_t>(stages) * p.stage_bytes;
   p.q_off = static_cast<int>(off);
   off += align_up(p.q_bytes, 128);
+  p.qs_off = static_cast<int>(off);
+  if (fused) off += align_up(static_cast<size_t>(p.Hc) * p.G * (p.D * 4 + 32), 128);
   p.cum_off = static_cast<int>(off);
   off += align_up(4 * (static_cast<size_t>(p.B) + 1), 16);
   p.len_off = static_cast<int>(off);

@@ -69,8 +69,11 @@ struct AttnParams {
   int v_row_bytes;             // padded shared-memory stride of a V row
   int row_copy_bytes;          // bytes copied per token row (Hc * D * 2)
   int stage_bytes;
-  int q_bytes;                 // bytes of the q staging buffer
+  int q_bytes;                 // bytes reserved for the q staging buffer
+  int q_row_bytes;             // padded shared-memory stride of a staged q row
+  int q_tx_bytes;              // bytes the q copies deliver
   int q_off, cum_off, len_off, pos_off, meta_off, bar_off;
+  int qs_off;                  // per-warp fp32 q rows (rotated), padded: G * (D*4 + 32) bytes per warp
   int smem_bytes;
   int fused;
 };

@@ -160,7 +160,7 @@ def test_fused_repeated_calls_reuse_the_workspace():
 
 
 @pytest.mark.parametrize("graph", [False, True])
-@pytest.mark.parametrize("name", ["c64", "long", "high"])
+@pytest.mark.parametrize("name", ["tiny", "c64", "padded", "long", "high"])
 def test_fused_programmatic_dependent_launch(name, graph):
     # back-to-back fused launches, each a programmatic dependent of the previous one
     inp = workloads.make_inputs(name, device="cuda")

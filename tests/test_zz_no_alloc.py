@@ -75,13 +75,22 @@ def test_noalloc_matches_workspace_path_on_two_calls_in_a_row():
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     v = H.vh()
-    # 256 q heads of dim 128 need far more than the fixed array for their partials
-    B, Hq, Hkv, D, P = 4, 256, 32, 128, 16
-    need = v.vh_decode_workspace_bytes(B, Hq, Hkv, D, P)
-    assert need > 8 << 20
-    z = torch.zeros(64, dtype=torch.int32, device="cuda")
-    f = v.lib.vh_paged_decode_attn_noalloc
-    p = z.data_ptr()
-    status = f(p, p, p, 2 * P * Hkv * D, Hkv * D, 1, p, 1, p, p, p, 0.0, 0, None, B, Hq, Hkv, D, P, None)
-    assert status == v.VH_ESCRATCH
-    assert "scratch" in v.vh_status_string(status)
+    # 4096 rows x 1024 kv heads: the per-(row, kv head) counters alone
+    # (4096 * 1024 * 4 bytes = 16 MiB) exceed the 8 MiB array whatever the CTA
+    # count, while the shape still fits the kernel's shared-memory plan, so the
+    # call is rejected on the host with VH_ESCRATCH.  Every buffer is still
+    # allocated at its full size, so even a wrong verdict could only launch
+    # over all-padding rows into valid memory.
+    B, Hq, Hkv, D, P = 4096, 1024, 1024, 64, 16
+    assert B * Hkv * 4 > 8 << 20
+    dev = "cuda"
+    q_rot = torch.zeros((B, Hq, D), dtype=torch.float32, device=dev)
+    pool = torch.zeros((1, 2, P, Hkv, D), dtype=torch.bfloat16, device=dev)
+    page_table = torch.zeros((B, 1), dtype=torch.int32, device=dev)
+    seq_lens = torch.ones(B, dtype=torch.int32, device=dev)
+    active = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(v.VHError) as e:
+        v.vh_paged_decode_attn_noalloc(q_rot, pool[:, 0], pool[:, 1], page_table, seq_lens, active, out)
+    assert e.value.status == v.VH_ESCRATCH
+    assert "scratch" in v.vh_status_string(v.VH_ESCRATCH)
