@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer calls per step (default: the workload's own count, 28 for 'high')")
     ap.add_argument("--ncu-case", action="store_true",
                     help="eager launches of the fused and the three-call step on one pool (profiling)")
     return ap.parse_args()
@@ -179,17 +181,34 @@ class Clocks:
 
 
 class Setup:
-    """Device buffers of one workload: R pool replicas and the step's outputs."""
+    """Device buffers of one workload: KV pools and the step's outputs.
 
-    def __init__(self, name: str, rank: int, dev, replicas: int | None = None):
+    One layer: R replicas of the pool, cycled so that their total exceeds 4x L2.
+    Several layers (the high-concurrency workload has 28): one pool and one set
+    of inputs per layer, each drawn with its own layer seed; a step runs all
+    layers in order."""
+
+    def __init__(self, name: str, rank: int, dev, replicas: int | None = None, layers: int | None = None):
         import paged_len_decode_gb300 as vh
         self.vh = vh
-        self.inp = inp = workloads.make_inputs(name, layer=rank, device=dev)
+        self.L = layers or workloads.WORKLOADS[name].layers
+        if self.L > 1:
+            self.layer_inputs = [workloads.make_inputs(name, layer=rank * self.L + l, device=dev)
+                                 for l in range(self.L)]
+            inp = self.layer_inputs[0]
+        else:
+            self.layer_inputs = None
+            inp = workloads.make_inputs(name, layer=rank, device=dev)
+        self.inp = inp
         self.B, self.Hq, self.Hkv, self.D, self.P = inp.B, inp.Hq, inp.Hkv, inp.D, inp.P
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.pool_bytes = inp.pool.numel() * 2
-        self.R = replicas or max(2, math.ceil(4 * self.l2 / self.pool_bytes))
-        self.pools = [inp.pool] + [inp.pool.clone() for _ in range(self.R - 1)]
+        if self.layer_inputs:
+            self.pools = [li.pool for li in self.layer_inputs]
+            self.R = self.L
+        else:
+            self.R = replicas or max(2, math.ceil(4 * self.l2 / self.pool_bytes))
+            self.pools = [inp.pool] + [inp.pool.clone() for _ in range(self.R - 1)]
         self.cos_sin = torch.empty((inp.max_pages_per_seq * self.P, self.D), dtype=torch.float32, device=dev)
         vh.vh_rope_table(self.cos_sin, inp.theta)
         self.q_rot = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=dev)
@@ -198,13 +217,22 @@ class Setup:
         self.wsf = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.n_ctas = vh.vh_decode_num_ctas(self.B, self.Hq, self.Hkv, self.D, self.P)
 
+    def inputs(self, r):
+        return self.layer_inputs[r] if self.layer_inputs else self.inp
+
+    def step_bytes(self) -> dict:
+        if not self.layer_inputs:
+            return step_bytes(self.inp)
+        per = [step_bytes(li) for li in self.layer_inputs]
+        return {k: (sum(x[k] for x in per) if k != "active" else per[0][k]) for k in per[0]}
+
     def fused(self, r, pdl=True, src=None):
-        s = src or self.inp
+        s = src or self.inputs(r)
         self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
                                 s.page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl)
 
     def three(self, r):
-        i = self.inp
+        i = self.inputs(r)
         self.vh.decode_step(i.q, i.k_new, i.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
                             i.page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3)
 
@@ -213,7 +241,7 @@ def run_ncu_case(args):
     """A few eager launches on one pool: 3 fused, 3 three-call steps."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    s = Setup(args.workload, 0, dev, replicas=1)
+    s = Setup(args.workload, 0, dev, replicas=1, layers=1)
     for _ in range(3):
         s.fused(0, pdl=False)
     for _ in range(3):
@@ -222,73 +250,8 @@ def run_ncu_case(args):
     print(json.dumps({"ncu_case": args.workload, "ok": True}))
 
 
-def run_ours(args, rank, world):
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w = workloads.WORKLOADS[args.workload]
-    s = Setup(args.workload, rank, dev)
-    inp, R = s.inp, s.R
-    by = step_bytes(inp)
-
-    for r in range(R):  # first calls outside capture (launch attributes, every replica's new slot)
-        s.three(r)
-        s.fused(r, pdl=False)
-    torch.cuda.synchronize()
-
-    stream = torch.cuda.Stream(device=dev)
-
-    def capture(fn, n):
-        g = torch.cuda.CUDAGraph()
-        stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    fn(i % R)
-        torch.cuda.current_stream().wait_stream(stream)
-        return g
-
-    chunk = R * max(1, 240 // R)  # steps per graph replay (a multiple of the replica count)
-
-    def timed(fn, K, clocks=None):
-        full = capture(fn, chunk)
-        rem = K % chunk
-        tail = capture(fn, rem) if rem else None
-        with torch.cuda.stream(stream):
-            full.replay()  # warm the graph itself
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        if clocks:
-            clocks.start()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(K // chunk):
-                full.replay()
-            if tail is not None:
-                tail.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ck = clocks.stop() if clocks else None
-        barrier(world)
-        return max_over_ranks(e0.elapsed_time(e1), world), ck
-
-    for i in range(args.warmup):  # untimed warm-up steps
-        s.fused(i % R)
-        s.three(i % R)
-    torch.cuda.synchronize()
-
-    clocks = Clocks(dev.index)
-    ms_fused_total, ck = timed(s.fused, args.steps, clocks)
-    ms_step = ms_fused_total / args.steps
-    ms_three_total, _ = timed(s.three, args.steps)
-    ms_three = ms_three_total / args.steps
-
-    tokens_per_s = by["active"] * world / (ms_step * 1e-3)
-    step_gbs = by["step"] / (ms_step * 1e-3) / 1e9
-    peak, peak_kind = peaks()
-
-    # ---- e2e through the public call with host buffers (one fused launch per step) ----
+def e2e_measure(s, inp, R, by, args, world, dev, stream):
+    """e2e through the public call with host buffers (one fused launch per step)."""
     # The step's inputs live in one pinned host arena and one device arena (the
     # way a serving runtime stages a step), so each step is one host->device
     # copy, the call, and one device->host copy of the output.
@@ -349,6 +312,84 @@ def run_ours(args, rank, world):
     e2e_ms = e2e_time(lambda i: graphs[i % R].replay(), K_e2e)
     e2e_tps = by["active"] * world / (e2e_ms * 1e-3)
 
+    return {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": K_e2e,
+            "call": "paged_len_decode_gb300.vh_decode_fused in a per-step CUDA graph with one "
+                    "pinned-host->device copy of the step's input arena and one output copy",
+            "eager": {"value": round(by["active"] * world / (e2e_eager_ms * 1e-3), 1),
+                      "ms_per_step": round(e2e_eager_ms, 6)}}
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    s = Setup(args.workload, rank, dev, layers=args.layers)
+    inp, R, L = s.inp, s.R, s.L
+    by = s.step_bytes()
+
+    for r in range(R):  # first calls outside capture (launch attributes, every replica's new slot)
+        s.three(r)
+        s.fused(r, pdl=False)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    fn(i % R)
+        torch.cuda.current_stream().wait_stream(stream)
+        return g
+
+    chunk = R * max(1, 240 // R)  # steps per graph replay (a multiple of the replica count)
+
+    def timed(fn, K, clocks=None):
+        full = capture(fn, chunk)
+        rem = K % chunk
+        tail = capture(fn, rem) if rem else None
+        with torch.cuda.stream(stream):
+            full.replay()  # warm the graph itself
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K // chunk):
+                full.replay()
+            if tail is not None:
+                tail.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ck = clocks.stop() if clocks else None
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world), ck
+
+    for i in range(args.warmup):  # untimed warm-up steps
+        s.fused(i % R)
+        s.three(i % R)
+    torch.cuda.synchronize()
+
+    clocks = Clocks(dev.index)
+    ms_fused_total, ck = timed(s.fused, args.steps * L, clocks)  # L layer calls per step
+    ms_step = ms_fused_total / args.steps
+    ms_three_total, _ = timed(s.three, args.steps * L)
+    ms_three = ms_three_total / args.steps
+
+    tokens_per_s = by["active"] * world / (ms_step * 1e-3)
+    step_gbs = by["step"] / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+
+    e2e = None
+    if L == 1:
+        e2e = e2e_measure(s, inp, R, by, args, world, dev, stream)
+
     res = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
@@ -357,28 +398,28 @@ def run_ours(args, rank, world):
         "config": {"workload": f"{args.workload}: B={s.B} (active {by['active']}), Hq={s.Hq}, Hkv={s.Hkv}, "
                                f"D={s.D}, P={s.P}, lengths {w.dist} [{w.len_lo},{w.len_hi}]",
                    "global_batch": s.B * world, "kv_bytes_per_step": by["kv"],
-                   "step": "one vh_decode_fused launch (RoPE+append+attention+merge), PDL between steps",
+                   "step": (f"{L} layer calls, " if L > 1 else "") +
+                           "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
+                           "PDL between launches",
+                   "layers": L,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB >= 4x L2 "
-                         f"{s.l2 / 1e6:.0f} MB): inputs larger than L2",
+                   "l2": (f"{L} KV pools, one per layer ({L * s.pool_bytes / 1e9:.1f} GB)" if L > 1 else
+                          f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB")
+                         + f" >= 4x L2 {s.l2 / 1e6:.0f} MB): inputs larger than L2",
                    "ctas": s.n_ctas},
         "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
         "roofline": {"bound": "hbm", "kernel": f"decode_attn_kernel<{s.D},{s.Hq // s.Hkv},1> (fused step)",
                      "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(step_gbs / peak, 4), "traffic": recorded_traffic(args.workload),
-                     "peak_kind": peak_kind, "ms_per_launch": round(ms_step, 6),
-                     "algorithmic_bytes_per_launch": by["step"]},
+                     "peak_kind": peak_kind, "ms_per_launch": round(ms_step / L, 6),
+                     "algorithmic_bytes_per_launch": by["step"] // L},
         "three_call": {"ms_per_step": round(ms_three, 6),
                        "value": round(by["active"] * world / (ms_three * 1e-3), 1), "unit": "tokens/s",
-                       "launches_per_step": 3},
+                       "launches_per_step": 3 * L},
         "clocks": ck,
-        "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": K_e2e,
-                "call": "paged_len_decode_gb300.vh_decode_fused in a per-step CUDA graph with one "
-                        "pinned-host->device copy of the step's input arena and one output copy",
-                "eager": {"value": round(by["active"] * world / (e2e_eager_ms * 1e-3), 1),
-                          "ms_per_step": round(e2e_eager_ms, 6)}},
-        "gpu_launches": args.steps,
+        "e2e": e2e if e2e is not None else {"value": None, "unit": "tokens/s",
+                                            "note": "measured for single-layer steps only"},
+        "gpu_launches": args.steps * L,
     }
     return res, inp
 

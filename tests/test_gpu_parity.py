@@ -229,3 +229,15 @@ def test_position_beyond_table_is_flagged(path):
     assert got["err"] & 4
     if path == "fused":
         assert not got["out"][1].any(), "a row with an invalid position is treated as padding"
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_large_batch_of_short_rows(path):
+    # 2048 rows: the prologue scans eight rows per thread; many rows per CTA
+    g = torch.Generator().manual_seed(17)
+    lens = torch.randint(1, 48, (2048,), generator=g).tolist()
+    active = (torch.rand(2048, generator=g) > 0.1).to(torch.int64).tolist()
+    lens = [L if a else 1 for L, a in zip(lens, active)]
+    inp = workloads.make_case(B=2048, Hq=8, Hkv=4, D=128, P=16, seq_lens=lens, active=active, seed=18,
+                              device="cuda", max_pages_per_seq=3)
+    H.full_check(inp, path=path)
