@@ -47,8 +47,8 @@ def _load():
             lib.oracle_bf16_to_double.restype = D
             lib.oracle_num_threads.restype = I
             lib.oracle_set_num_threads.argtypes = [I]
-            lib.oracle_rope_kv_append.argtypes = [P, P, P, P, P, P, I64, I64, P, I, I, P, P, P, P,
-                                                  I, I, I, I, I, D]
+            lib.oracle_rope_kv_append.argtypes = [P, P, P, P, P, P, D, P, P, I64, I64, P, I, I, P, P, P, P,
+                                                  P, I, I, I, I, I, D]
             lib.oracle_rope_kv_append.restype = I
             lib.oracle_decode_attn.argtypes = [P, P, P, I64, I64, P, I, P, P, P, P, D, P, I,
                                                I, I, I, I, I]
@@ -91,13 +91,16 @@ def bf16_to_double(bits: int) -> float:
 
 
 def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, theta,
-                   positions=None, num_pages=None, return_k_rot=False, in_place=False):
+                   positions=None, num_pages=None, return_k_rot=False, in_place=False,
+                   q_norm_w=None, k_norm_w=None, norm_eps=1e-6, return_k_pre=False):
     """RoPE + append on a copy of `pool` ([NP, 2, P, Hkv, D] bf16), or on `pool`
     itself when in_place (a contiguous CPU tensor).
 
     Returns (q_rot float64 [B, Hq, D], pool_after bf16, n_bad), plus the
-    unrounded rotated keys float64 [B, Hkv, D] if return_k_rot.  Rows with
-    active == 0 keep q_rot = 0 and write nothing.
+    unrounded rotated keys float64 [B, Hkv, D] if return_k_rot, plus the keys
+    fed to RoPE if return_k_pre.  Rows with active == 0 keep q_rot = 0 and
+    write nothing.  q_norm_w / k_norm_w (length-D weights, or None) switch on
+    the per-head RMSNorm before RoPE.
     """
     lib = _load()
     B, Hq, D = q.shape
@@ -111,6 +114,9 @@ def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, th
     bits = pool_after.view(torch.int16)
     q_rot = torch.zeros((B, Hq, D), dtype=torch.float64)
     k_rot = torch.zeros((B, Hkv, D), dtype=torch.float64)
+    k_pre = torch.zeros((B, Hkv, D), dtype=torch.float64)
+    qw = None if q_norm_w is None else torch.as_tensor(q_norm_w).detach().to("cpu", torch.float64).contiguous()
+    kw = None if k_norm_w is None else torch.as_tensor(k_norm_w).detach().to("cpu", torch.float64).contiguous()
     qb = q.detach().to("cpu").contiguous().view(torch.int16)
     kb = k_new.detach().to("cpu").contiguous().view(torch.int16)
     vb = v_new.detach().to("cpu").contiguous().view(torch.int16)
@@ -122,15 +128,18 @@ def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, th
     token_stride = Hkv * D
     k_ptr = bits.data_ptr()
     v_ptr = bits.data_ptr() + P * Hkv * D * 2
-    bad = lib.oracle_rope_kv_append(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pos),
-                                    ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+    bad = lib.oracle_rope_kv_append(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pos), _ptr(qw), _ptr(kw),
+                                    float(norm_eps), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                                     page_stride, token_stride, _ptr(pt), pt.shape[1],
                                     NP if num_pages is None else num_pages,
-                                    _ptr(sl), _ptr(ac), _ptr(q_rot), _ptr(k_rot),
+                                    _ptr(sl), _ptr(ac), _ptr(q_rot), _ptr(k_rot), _ptr(k_pre),
                                     B, Hq, Hkv, D, P, float(theta))
+    res = (q_rot, pool_after, int(bad))
     if return_k_rot:
-        return q_rot, pool_after, int(bad), k_rot
-    return q_rot, pool_after, int(bad)
+        res = res + (k_rot,)
+    if return_k_pre:
+        res = res + (k_pre,)
+    return res
 
 
 def decode_attn(q_rot, pool, page_table, seq_lens, active, *, P, sm_scale=0.0, rows=None,
@@ -190,17 +199,19 @@ def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor):
     return o, float(lse)
 
 
-def reference_step(inp, positions=None, rows=None, sm_scale=0.0):
+def reference_step(inp, positions=None, rows=None, sm_scale=0.0, q_norm_w=None, k_norm_w=None,
+                   norm_eps=1e-6):
     """Whole step on one layer's inputs (any object with the DecodeInputs fields).
 
-    Returns dict(q_rot, k_rot, pool_after, out, n_bad): RoPE + append, then
-    attention over the appended cache.  k_rot is the rotated key before its
-    bf16 rounding.
+    Returns dict(q_rot, k_rot, k_pre, pool_after, out, n_bad): (RMSNorm +) RoPE
+    + append, then attention over the appended cache.  k_rot is the rotated key
+    before its bf16 rounding, k_pre the key fed to RoPE.
     """
-    q_rot, pool_after, bad, k_rot = rope_kv_append(inp.q, inp.k_new, inp.v_new, inp.pool,
-                                                   inp.page_table, inp.seq_lens, inp.active,
-                                                   P=inp.P, theta=inp.theta, positions=positions,
-                                                   num_pages=inp.num_pages, return_k_rot=True)
+    q_rot, pool_after, bad, k_rot, k_pre = rope_kv_append(
+        inp.q, inp.k_new, inp.v_new, inp.pool, inp.page_table, inp.seq_lens, inp.active, P=inp.P,
+        theta=inp.theta, positions=positions, num_pages=inp.num_pages, return_k_rot=True,
+        q_norm_w=q_norm_w, k_norm_w=k_norm_w, norm_eps=norm_eps, return_k_pre=True)
     out = decode_attn(q_rot, pool_after, inp.page_table, inp.seq_lens, inp.active, P=inp.P,
                       rows=rows, sm_scale=sm_scale)
-    return {"q_rot": q_rot, "k_rot": k_rot, "pool_after": pool_after, "out": out, "n_bad": bad}
+    return {"q_rot": q_rot, "k_rot": k_rot, "k_pre": k_pre, "pool_after": pool_after, "out": out,
+            "n_bad": bad}

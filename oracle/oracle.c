@@ -6,7 +6,8 @@
  * header, table or helper with the CUDA library and includes none of it.
  *
  * What it computes (each function below cites the passage it follows):
- *   oracle_rope_kv_append  -- RoPE on the new q and k of every active row at
+ *   oracle_rope_kv_append  -- optional per-head RMSNorm, then RoPE on the new
+ *                             q and k of every active row at
  *                             position seq_len-1, then the append of the
  *                             rotated k (rounded to bf16) and of v into the
  *                             row's current page;
@@ -91,6 +92,20 @@ void oracle_set_num_threads(int n) {
 #endif
 }
 
+/* ---- RMSNorm ----------------------------------------------------------- */
+
+/* Per-head RMSNorm with float64 variance (the pages keep "RMSNorm variance" in
+ * fp32 or better for alignment, "Engineering TTS inference in vLLM-Omni",
+ * Qwen3-TTS section 4):  x_d <- w_d * x_d / sqrt(mean_e(x_e^2) + eps).
+ * w == NULL: no normalisation. */
+static void rms_norm(double* x, int D, const double* w, double eps) {
+    if (!w) return;
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d) ss += x[d] * x[d];
+    double r = 1.0 / sqrt(ss / (double)D + eps);
+    for (int d = 0; d < D; ++d) x[d] = w[d] * (x[d] * r);
+}
+
 /* ---- RoPE + append ---------------------------------------------------- */
 
 /* Rotate one head vector x[0..D) in place by position pos ("rotate half"):
@@ -121,20 +136,25 @@ static void rope_rotate(double* x, int D, double pos, double theta) {
  *
  * q, k_new, v_new: bf16 [B][Hq][D], [B][Hkv][D], [B][Hkv][D].
  * positions: NULL means seq_len - 1.
+ * q_norm_w, k_norm_w: per-dim RMSNorm weights [D] applied to every q / new-k
+ *   head before RoPE, or NULL for none; norm_eps is the epsilon.
  * q_rot: float64 [B][Hq][D] out; rows with active == 0 are left untouched.
  * k_rot: float64 [B][Hkv][D] out or NULL: the rotated key before its bf16
  *        rounding (rows that are skipped are left untouched).
+ * k_pre: float64 [B][Hkv][D] out or NULL: the key fed to RoPE (after the
+ *        RMSNorm when there is one).
  * Returns the number of active rows whose slot could not be placed
  * (seq_len outside [1, MPS*P] or a page id outside [0, num_pages)); those
  * rows write nothing.
  */
 int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                           const int32_t* positions,
+                          const double* q_norm_w, const double* k_norm_w, double norm_eps,
                           uint16_t* k_cache, uint16_t* v_cache,
                           int64_t page_stride, int64_t token_stride,
                           const int32_t* page_table, int max_pages_per_seq, int num_pages,
                           const int32_t* seq_lens, const int32_t* active,
-                          double* q_rot, double* k_rot,
+                          double* q_rot, double* k_rot, double* k_pre,
                           int B, int Hq, int Hkv, int D, int P, double theta) {
     int bad = 0;
     double* tmp = (double*)malloc(sizeof(double) * (size_t)D);
@@ -146,6 +166,7 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
         for (int g = 0; g < Hq; ++g) {
             const uint16_t* src = q + ((size_t)b * Hq + g) * D;
             for (int d = 0; d < D; ++d) tmp[d] = bf16_to_double(src[d]);
+            rms_norm(tmp, D, q_norm_w, norm_eps);
             rope_rotate(tmp, D, pos, theta);
             memcpy(q_rot + ((size_t)b * Hq + g) * D, tmp, sizeof(double) * (size_t)D);
         }
@@ -157,6 +178,8 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
             const uint16_t* ks = k_new + ((size_t)b * Hkv + h) * D;
             const uint16_t* vs = v_new + ((size_t)b * Hkv + h) * D;
             for (int d = 0; d < D; ++d) tmp[d] = bf16_to_double(ks[d]);
+            rms_norm(tmp, D, k_norm_w, norm_eps);
+            if (k_pre) memcpy(k_pre + ((size_t)b * Hkv + h) * D, tmp, sizeof(double) * (size_t)D);
             rope_rotate(tmp, D, pos, theta);
             if (k_rot) memcpy(k_rot + ((size_t)b * Hkv + h) * D, tmp, sizeof(double) * (size_t)D);
             uint16_t* kd = k_cache + (int64_t)page * page_stride + (int64_t)off * token_stride + (int64_t)h * D;

@@ -57,6 +57,14 @@ def bf16_round_bits(x: float) -> int:
     return sign | r
 
 
+def rms_norm(x: list[float], w, eps: float) -> list[float]:
+    """w_d * x_d / sqrt(mean(x^2) + eps); w None: unchanged."""
+    if w is None:
+        return list(x)
+    r = 1.0 / math.sqrt(math.fsum(v * v for v in x) / len(x) + eps)
+    return [wd * (v * r) for wd, v in zip(w, x)]
+
+
 def rope(x: list[float], pos: float, theta: float) -> list[float]:
     """Rotate-half RoPE: pair (i, i + D/2), angle pos * theta^(-2i/D)."""
     D = len(x)
@@ -71,7 +79,7 @@ def rope(x: list[float], pos: float, theta: float) -> list[float]:
 
 
 def step(q, k_new, v_new, pool, page_table, seq_lens, active, P, theta, sm_scale=None,
-         positions=None):
+         positions=None, q_norm_w=None, k_norm_w=None, eps=1e-6):
     """Whole step on nested lists of bf16 bit patterns.
 
     q: [B][Hq][D], k_new/v_new: [B][Hkv][D], pool: [NP][2][P][Hkv][D] (bits, mutated
@@ -92,12 +100,12 @@ def step(q, k_new, v_new, pool, page_table, seq_lens, active, P, theta, sm_scale
         L = seq_lens[b]
         pos = positions[b] if positions is not None else L - 1
         for g in range(Hq):
-            q_rot[b][g] = rope([bf16_bits_to_float(v) for v in q[b][g]], pos, theta)
+            q_rot[b][g] = rope(rms_norm([bf16_bits_to_float(v) for v in q[b][g]], q_norm_w, eps), pos, theta)
         slot = L - 1
         page = page_table[b][slot // P]
         off = slot % P
         for h in range(Hkv):
-            kr = rope([bf16_bits_to_float(v) for v in k_new[b][h]], pos, theta)
+            kr = rope(rms_norm([bf16_bits_to_float(v) for v in k_new[b][h]], k_norm_w, eps), pos, theta)
             pool[page][0][off][h] = [bf16_round_bits(v) for v in kr]
             pool[page][1][off][h] = list(v_new[b][h])
     for b in range(B):

@@ -415,3 +415,67 @@ def test_oracle_matches_brute_force_on_tiny_workload_rows():
                             inp.P, inp.theta)
     assert torch.allclose(r["out"], torch.tensor(out, dtype=torch.float64), atol=1e-12, rtol=0)
     assert _nested(r["pool_after"]) == pool
+
+
+# ---------------------------------------------------------------- RMSNorm (fused before RoPE)
+
+def _norm_weights(D, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (1.0 + 0.1 * torch.randn(D, generator=g)).to(torch.float32)
+
+
+def _q_path(q_bf16, pos, w, eps):
+    B, H, D = q_bf16.shape
+    k = torch.zeros((B, 1, D), dtype=torch.bfloat16)
+    pool = torch.zeros((3, 2, 16, 1, D), dtype=torch.bfloat16)
+    q_rot, _, bad = oracle.rope_kv_append(q_bf16, k, k, pool, torch.ones((B, 1), dtype=torch.int32),
+                                          torch.ones(B, dtype=torch.int32), torch.ones(B, dtype=torch.int32),
+                                          P=16, theta=10000.0, positions=torch.full((B,), pos), q_norm_w=w,
+                                          norm_eps=eps)
+    assert bad == 0
+    return q_rot
+
+
+def test_rms_norm_matches_torch_rms_norm():
+    g = torch.Generator().manual_seed(30)
+    for D in (64, 128):
+        q = torch.randn((3, 4, D), generator=g).to(torch.bfloat16)
+        w = _norm_weights(D, D)
+        got = _q_path(q, 0, w, 1e-6)  # position 0: RoPE is the identity
+        ref = torch.nn.functional.rms_norm(q.double(), (D,), weight=w.double(), eps=1e-6)
+        assert torch.allclose(got, ref, atol=1e-14, rtol=1e-14)
+
+
+def test_rms_norm_closed_forms():
+    D = 64
+    w = _norm_weights(D, 1)
+    c = torch.full((1, 1, D), -3.0).to(torch.bfloat16)  # constant vector: rms = |c|
+    got = _q_path(c, 0, w, 0.0)[0, 0]
+    assert torch.allclose(got, -w.double(), atol=1e-15)
+    # invariance to positive scaling (eps = 0), and unit RMS with unit weights
+    x = torch.randn((1, 2, D), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    a = _q_path(x, 0, torch.ones(D), 0.0)
+    b = _q_path((x.float() * 4).to(torch.bfloat16), 0, torch.ones(D), 0.0)
+    assert torch.allclose(a, b, atol=1e-15)
+    assert torch.allclose(a.pow(2).mean(-1), torch.ones((1, 2), dtype=torch.float64), atol=1e-14)
+    # RoPE after the norm keeps the unit RMS (a rotation)
+    r = _q_path(x, 777, torch.ones(D), 0.0)
+    assert torch.allclose(r.pow(2).mean(-1), torch.ones((1, 2), dtype=torch.float64), atol=1e-14)
+
+
+def test_rms_norm_step_matches_brute_force():
+    inp = _small_case([17, 5, 33], Hq=4, Hkv=2, D=8, P=16, seed=31)
+    qw, kw = _norm_weights(8, 3), _norm_weights(8, 4)
+    r = oracle.reference_step(inp, q_norm_w=qw, k_norm_w=kw, norm_eps=1e-5)
+    pool = _nested(inp.pool)
+    q_rot, out = brute.step(_nested(inp.q), _nested(inp.k_new), _nested(inp.v_new), pool,
+                            inp.page_table.tolist(), inp.seq_lens.tolist(), inp.active.tolist(),
+                            inp.P, inp.theta, q_norm_w=qw.double().tolist(), k_norm_w=kw.double().tolist(),
+                            eps=1e-5)
+    assert torch.allclose(r["q_rot"], torch.tensor(q_rot, dtype=torch.float64), atol=1e-12, rtol=0)
+    assert torch.allclose(r["out"], torch.tensor(out, dtype=torch.float64), atol=1e-12, rtol=0)
+    assert _nested(r["pool_after"]) == pool
+    # and the key fed to RoPE is the normalised key
+    kp = r["k_pre"][0, 1]
+    ref = torch.nn.functional.rms_norm(inp.k_new[0, 1].double().view(1, -1), (8,), weight=kw.double(), eps=1e-5)
+    assert torch.allclose(kp, ref.view(-1), atol=1e-14)
