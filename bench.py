@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--qk-norm", action="store_true",
+                    help="per-head RMSNorm of q and the new key before RoPE (unit weights, eps 1e-6)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layer calls per step (default: the workload's own count, 28 for 'high')")
     ap.add_argument("--ncu-case", action="store_true",
@@ -188,7 +190,8 @@ class Setup:
     of inputs per layer, each drawn with its own layer seed; a step runs all
     layers in order."""
 
-    def __init__(self, name: str, rank: int, dev, replicas: int | None = None, layers: int | None = None):
+    def __init__(self, name: str, rank: int, dev, replicas: int | None = None, layers: int | None = None,
+                 qk_norm: bool = False):
         import paged_len_decode_gb300 as vh
         self.vh = vh
         self.L = layers or workloads.WORKLOADS[name].layers
@@ -216,6 +219,10 @@ class Setup:
         self.ws3 = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.wsf = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.n_ctas = vh.vh_decode_num_ctas(self.B, self.Hq, self.Hkv, self.D, self.P)
+        self.norm = {}
+        if qk_norm:
+            w = torch.ones(self.D, dtype=torch.float32, device=dev)
+            self.norm = {"q_norm_w": w, "k_norm_w": w, "norm_eps": 1e-6}
 
     def inputs(self, r):
         return self.layer_inputs[r] if self.layer_inputs else self.inp
@@ -229,12 +236,12 @@ class Setup:
     def fused(self, r, pdl=True, src=None):
         s = src or self.inputs(r)
         self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
-                                s.page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl)
+                                s.page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl, **self.norm)
 
     def three(self, r):
         i = self.inputs(r)
         self.vh.decode_step(i.q, i.k_new, i.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
-                            i.page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3)
+                            i.page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3, **self.norm)
 
 
 def run_ncu_case(args):
@@ -324,7 +331,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
-    s = Setup(args.workload, rank, dev, layers=args.layers)
+    s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm)
     inp, R, L = s.inp, s.R, s.L
     by = s.step_bytes()
 
@@ -401,7 +408,7 @@ def run_ours(args, rank, world):
                    "step": (f"{L} layer calls, " if L > 1 else "") +
                            "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
                            "PDL between launches",
-                   "layers": L,
+                   "layers": L, "qk_norm": bool(args.qk_norm),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": (f"{L} KV pools, one per layer ({L * s.pool_bytes / 1e9:.1f} GB)" if L > 1 else
                           f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB")

@@ -104,6 +104,10 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
  * v_new  bf16 [B][Hkv][D]  new values, stored bit for bit
  * cos_sin float [max_pos][D] from vh_rope_table
  * positions int32 [B] or NULL; NULL means position = seq_lens[b] - 1
+ * q_norm_w, k_norm_w float [D] or NULL: per-head RMSNorm applied to every q
+ *        head / new k head before RoPE, x <- w * x / sqrt(mean(x^2) + norm_eps),
+ *        in fp32 (the pages keep "RMSNorm variance" in fp32 for alignment);
+ *        NULL skips it.  16-byte aligned.  norm_eps >= 0.
  * k_cache, v_cache, page_stride, token_stride: the layer's paged cache
  * num_pages: pages in the pool, used only to bounds-check page ids (> 0)
  * page_table int32 [B][max_pages_per_seq]; seq_lens, active int32 [B]
@@ -120,6 +124,7 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
  * or a stride not 16-byte aligned), VH_ECUDA. */
 int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
                       const float* cos_sin, int max_pos, const int32_t* positions,
+                      const float* q_norm_w, const float* k_norm_w, float norm_eps,
                       vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride,
                       int64_t token_stride, int num_pages,
                       const int32_t* page_table, int max_pages_per_seq,
@@ -173,9 +178,9 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
 int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
-/* The whole decode step of one layer in ONE launch: RoPE of q and of the new
- * key, append of the new key/value into the cache, attention and the merge
- * of split rows.  Same inputs and outputs as vh_rope_kv_append +
+/* The whole decode step of one layer in ONE launch: optional per-head RMSNorm
+ * and RoPE of q and of the new key, append of the new key/value into the
+ * cache, attention and the merge of split rows.  Same inputs and outputs as vh_rope_kv_append +
  * vh_paged_decode_attn + vh_decode_combine (apart from q_rot, which is not
  * written), with these differences:
  *   - the workspace must be zero-filled before its first use with this call
@@ -200,6 +205,7 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
  * VH_ENODEV, VH_ECUDA. */
 int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
                     const float* cos_sin, int max_pos, const int32_t* positions,
+                    const float* q_norm_w, const float* k_norm_w, float norm_eps,
                     vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride, int64_t token_stride,
                     int num_pages, const int32_t* page_table, int max_pages_per_seq,
                     const int32_t* seq_lens, const int32_t* active,

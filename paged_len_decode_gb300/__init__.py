@@ -46,7 +46,7 @@ def _load() -> ctypes.CDLL:
     lib.vh_status_string.restype = ctypes.c_char_p
     lib.vh_rope_table.argtypes = [P, I, I, D, P]
     lib.vh_rope_table.restype = I
-    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, I64, I64, I, P, I, P, P, P, P,
+    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I, P, I, P, P, P, P,
                                       I, I, I, I, I, P]
     lib.vh_rope_kv_append.restype = I
     lib.vh_decode_num_ctas.argtypes = [I, I, I, I, I]
@@ -61,8 +61,8 @@ def _load() -> ctypes.CDLL:
     lib.vh_paged_decode_attn_noalloc.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P,
                                                  I, I, I, I, I, P]
     lib.vh_paged_decode_attn_noalloc.restype = I
-    lib.vh_decode_fused.argtypes = [P, P, P, P, I, P, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P,
-                                    ctypes.c_uint, I, I, I, I, I, P]
+    lib.vh_decode_fused.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ,
+                                    P, ctypes.c_uint, I, I, I, I, I, P]
     lib.vh_decode_fused.restype = I
     return lib
 
@@ -126,8 +126,17 @@ def vh_rope_table(cos_sin: torch.Tensor, theta: float = 10000.0, stream=None) ->
     return cos_sin
 
 
+def _norm_w(t, D, name):
+    if t is None:
+        return None
+    if t.shape != (D,):
+        raise ValueError(f"{name} must have shape ({D},)")
+    return _contig(t, torch.float32, name)
+
+
 def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
-                      q_rot, positions=None, err_flag=None, stream=None) -> None:
+                      q_rot, positions=None, err_flag=None, q_norm_w=None, k_norm_w=None,
+                      norm_eps: float = 1e-6, stream=None) -> None:
     B, Hq, D = q.shape
     kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or q_rot.shape != (B, Hq, D):
@@ -136,6 +145,7 @@ def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, se
         _contig(q, torch.bfloat16, "q"), _contig(k_new, torch.bfloat16, "k_new"),
         _contig(v_new, torch.bfloat16, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
+        _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
         kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(q_rot, torch.float32, "q_rot"),
@@ -201,7 +211,8 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
 
 def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, out,
                     workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
-                    pdl: bool = False, stream=None) -> torch.Tensor:
+                    pdl: bool = False, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
+                    stream=None) -> torch.Tensor:
     """One whole decode step in one launch (RoPE, append, attention, merge).
     `workspace` must be zero-filled before its first use (alloc_workspace does that).
     pdl=True sets VH_FLAG_PDL (see include/vh.h for when that is allowed)."""
@@ -213,6 +224,7 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
         _contig(q, torch.bfloat16, "q"), _contig(k_new, torch.bfloat16, "k_new"),
         _contig(v_new, torch.bfloat16, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
+        _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
         kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
@@ -231,10 +243,12 @@ def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas:
 
 def decode_step(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, q_rot,
                 out, workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0,
-                err_flag=None, stream=None) -> torch.Tensor:
-    """One decode step of one layer: RoPE + append, attention, combine."""
+                err_flag=None, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
+                stream=None) -> torch.Tensor:
+    """One decode step of one layer: (RMSNorm +) RoPE + append, attention, combine."""
     vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
-                      q_rot, positions=positions, err_flag=err_flag, stream=stream)
+                      q_rot, positions=positions, err_flag=err_flag, q_norm_w=q_norm_w,
+                      k_norm_w=k_norm_w, norm_eps=norm_eps, stream=stream)
     vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
                          sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, stream=stream)
     vh_decode_combine(workspace, out, k_cache.shape[2], k_cache.shape[1], num_ctas=num_ctas,

@@ -464,6 +464,37 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
   const int ka_row = (lane & 7) + 8 * ((lane >> 3) & 1), ka_col = 8 * (lane >> 4);
   const int va_row = (lane & 7) + 8 * (lane >> 4), va_col = 8 * ((lane >> 3) & 1);
 
+  // fused: per-lane RMSNorm weights (q: the lane's fixed elements in step (1) of
+  // the fragment build; k: the lane's pairs in the append patch)
+  constexpr int NQU = D / 4;              // 4-element units per q head (32 or 16)
+  constexpr int KPAIRS = (D / 2 + 31) / 32;
+  float wq[4] = {1.f, 1.f, 1.f, 1.f}, wk[2 * KPAIRS];
+#pragma unroll
+  for (int j = 0; j < 2 * KPAIRS; ++j) wk[j] = 1.f;
+  if constexpr (FUSED) {
+    const int iq = 2 * (lane % NQU);
+    if (p.q_norm_w) {
+      const float2 a = *reinterpret_cast<const float2*>(p.q_norm_w + iq);
+      const float2 c2 = *reinterpret_cast<const float2*>(p.q_norm_w + D / 2 + iq);
+      wq[0] = a.x;
+      wq[1] = a.y;
+      wq[2] = c2.x;
+      wq[3] = c2.y;
+    }
+    if (p.k_norm_w) {
+#pragma unroll
+      for (int j = 0; j < KPAIRS; ++j) {
+        const int i = lane + 32 * j;
+        if (i < D / 2) {
+          wk[2 * j] = p.k_norm_w[i];
+          wk[2 * j + 1] = p.k_norm_w[i + D / 2];
+        }
+      }
+    }
+  }
+  (void)wq;
+  (void)wk;
+
   uint32_t qh[KSTEPS][2], ql[KSTEPS][2];  // q^T operand fragments (high / residual parts)
   float acc[KSTEPS][4];                   // O^T fragments: dims mt*16 + g4 (+8), heads 2 t4 (+1)
   float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
@@ -503,18 +534,35 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       int qstride;
       if constexpr (FUSED) {
         unsigned char* qs = smem + p.qs_off + w * G * QS_ROW;
-        for (int e = lane; e < G * D / 4; e += 32) {  // two pairs per step
-          const int n = e / (D / 4);
-          const int i = (e % (D / 4)) * 2;            // i, i+1 in [0, D/2)
+        // every lane runs each round (the per-head RMS reduction shuffles)
+        for (int e0 = 0; e0 < G * NQU; e0 += 32) {
+          const int e = e0 + lane;
+          const bool valid = e < G * NQU;
+          const int n = valid ? e / NQU : 0;
+          const int i = (e % NQU) * 2;  // i, i+1 in [0, D/2)
           const unsigned char* row = qb + (w * G + n) * p.q_row_bytes;
-          const float2 xv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * i));
-          const float2 yv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * (i + D / 2)));
-          const float2 cv = *reinterpret_cast<const float2*>(cs + i);
-          const float2 sv = *reinterpret_cast<const float2*>(cs + D / 2 + i);
-          float* dst = reinterpret_cast<float*>(qs + n * QS_ROW);
-          *reinterpret_cast<float2*>(dst + i) = make_float2(xv.x * cv.x - yv.x * sv.x, xv.y * cv.y - yv.y * sv.y);
-          *reinterpret_cast<float2*>(dst + i + D / 2) =
-              make_float2(yv.x * cv.x + xv.x * sv.x, yv.y * cv.y + xv.y * sv.y);
+          float2 xv = make_float2(0.f, 0.f), yv = make_float2(0.f, 0.f);
+          if (valid) {
+            xv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * i));
+            yv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * (i + D / 2)));
+          }
+          if (p.q_norm_w) {
+            // RMSNorm in fp32: the NQU lanes of a head hold its D elements
+            float ss = xv.x * xv.x + xv.y * xv.y + yv.x * yv.x + yv.y * yv.y;
+#pragma unroll
+            for (int off = 1; off < NQU; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float r = rsqrtf(ss / static_cast<float>(D) + p.norm_eps);
+            xv = make_float2(wq[0] * (xv.x * r), wq[1] * (xv.y * r));
+            yv = make_float2(wq[2] * (yv.x * r), wq[3] * (yv.y * r));
+          }
+          if (valid) {
+            const float2 cv = *reinterpret_cast<const float2*>(cs + i);
+            const float2 sv = *reinterpret_cast<const float2*>(cs + D / 2 + i);
+            float* dst = reinterpret_cast<float*>(qs + n * QS_ROW);
+            *reinterpret_cast<float2*>(dst + i) = make_float2(xv.x * cv.x - yv.x * sv.x, xv.y * cv.y - yv.y * sv.y);
+            *reinterpret_cast<float2*>(dst + i + D / 2) =
+                make_float2(yv.x * cv.x + xv.x * sv.x, yv.y * cv.y + xv.y * sv.y);
+          }
         }
         __syncwarp();
         qsrc = qs;
@@ -569,12 +617,32 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         // the new token (row nvalid-1): rotate its key in place, then append k and v to the cache
         uint16_t* kr = reinterpret_cast<uint16_t*>(kst + (nvalid - 1) * p.k_row_bytes);
         const long long dst = meta[stage];
+        float kx[KPAIRS], ky[KPAIRS];
+        float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < (D / 2 + 31) / 32; ++j) {
+        for (int j = 0; j < KPAIRS; ++j) {
+          const int i = lane + 32 * j;
+          kx[j] = i < D / 2 ? __uint_as_float(static_cast<uint32_t>(kr[i]) << 16) : 0.f;
+          ky[j] = i < D / 2 ? __uint_as_float(static_cast<uint32_t>(kr[i + D / 2]) << 16) : 0.f;
+          ss += kx[j] * kx[j] + ky[j] * ky[j];
+        }
+        if (p.k_norm_w) {
+          // RMSNorm of the new key in fp32 (the warp holds its D elements)
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+          const float r = rsqrtf(ss / static_cast<float>(D) + p.norm_eps);
+#pragma unroll
+          for (int j = 0; j < KPAIRS; ++j) {
+            kx[j] = wk[2 * j] * (kx[j] * r);
+            ky[j] = wk[2 * j + 1] * (ky[j] * r);
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < KPAIRS; ++j) {
           const int i = lane + 32 * j;
           if (i < D / 2) {
-            const float x = __uint_as_float(static_cast<uint32_t>(kr[i]) << 16);
-            const float y = __uint_as_float(static_cast<uint32_t>(kr[i + D / 2]) << 16);
+            const float x = kx[j], y = ky[j];
             const uint16_t xr = static_cast<uint16_t>(float_to_bf16_bits(x * rc[j] - y * rs[j]));
             const uint16_t yr = static_cast<uint16_t>(float_to_bf16_bits(y * rc[j] + x * rs[j]));
             kr[i] = xr;

@@ -3,11 +3,13 @@
 // Operation ("Adding a Model", vox-serve docs, section "1. The model code":
 // keys and values are written into the paged cache before attention; RoPE is
 // applied to q/k first; "Engineering TTS inference in vLLM-Omni", Qwen3-TTS
-// section 4: RoPE cos/sin in fp32): for each active row b at position
-// pos = seq_len - 1 (or positions[b]),
-//   q_rot[b]            = rope(q[b], pos)                 (fp32 out)
-//   cache slot (L - 1)  = bf16_rne(rope(k_new[b], pos)), v_new[b]
-// Rotation pairs element i with i + D/2, angle pos * theta^(-2i/D).
+// section 4: RMSNorm variance and RoPE cos/sin in fp32): for each active row b
+// at position pos = seq_len - 1 (or positions[b]),
+//   q_rot[b]            = rope(norm_q(q[b]), pos)                 (fp32 out)
+//   cache slot (L - 1)  = bf16_rne(rope(norm_k(k_new[b]), pos)), v_new[b]
+// norm_*(x) = w * x / sqrt(mean(x^2) + eps) per head, in fp32, when weights
+// are given (identity otherwise).  Rotation pairs element i with i + D/2,
+// angle pos * theta^(-2i/D).
 //
 // The work is tiny (a few hundred KB per call) and latency-bound: one CTA per
 // row, 16-byte vector loads and stores, cos/sin read from a table built once
@@ -59,35 +61,58 @@ __global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p
                              static_cast<long long>(slot % p.P) * p.token_stride;
 
   const int D = p.D, half = D / 2;
-  const int quads = half / 4;                  // 4-pair units per head
+  const int quads = half / 4;                  // 4-pair units per head (16 or 8: a head's units share a warp)
   const int heads = p.Hq + (page_ok ? p.Hkv : 0);
   const float* cs = p.cos_sin + static_cast<long long>(pos) * D;
+  const int total = heads * quads;
 
-  for (int u = threadIdx.x; u < heads * quads; u += blockDim.x) {
-    const int h = u / quads;
-    const int i = (u % quads) * 4;
+  // every lane of a warp runs each round, so the per-head RMS reduction can shuffle
+  for (int base = 0; base < total; base += blockDim.x) {
+    const int u = base + threadIdx.x;
+    const bool valid = u < total;
+    const int h = valid ? u / quads : 0;
+    const int i = valid ? (u % quads) * 4 : 0;
+    const bool is_q = h < p.Hq;
+    float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+      const uint16_t* src = is_q ? p.q + (static_cast<long long>(b) * p.Hq + h) * D
+                                 : p.k_new + (static_cast<long long>(b) * p.Hkv + (h - p.Hq)) * D;
+      const uint2 lo = *reinterpret_cast<const uint2*>(src + i);
+      const uint2 hi = *reinterpret_cast<const uint2*>(src + half + i);
+      const float2 x01 = bf16x2_to_float2(lo.x), x23 = bf16x2_to_float2(lo.y);
+      const float2 y01 = bf16x2_to_float2(hi.x), y23 = bf16x2_to_float2(hi.y);
+      x[0] = x01.x; x[1] = x01.y; x[2] = x23.x; x[3] = x23.y;
+      y[0] = y01.x; y[1] = y01.y; y[2] = y23.x; y[3] = y23.y;
+    }
+    const float* nw = is_q ? p.q_norm_w : p.k_norm_w;
+    // RMSNorm (fp32): the quads lanes of a head hold its D elements
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ss += x[k] * x[k] + y[k] * y[k];
+    for (int off = 1; off < quads; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (valid && nw != nullptr) {
+      const float r = rsqrtf(ss / static_cast<float>(D) + p.norm_eps);
+      const float4 wa = *reinterpret_cast<const float4*>(nw + i);
+      const float4 wb = *reinterpret_cast<const float4*>(nw + half + i);
+      const float wx[4] = {wa.x, wa.y, wa.z, wa.w}, wy[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[k] = wx[k] * (x[k] * r);
+        y[k] = wy[k] * (y[k] * r);
+      }
+    }
+    if (!valid) continue;
     const float4 c = *reinterpret_cast<const float4*>(cs + i);
     const float4 s = *reinterpret_cast<const float4*>(cs + half + i);
-    const uint16_t* src;
-    if (h < p.Hq)
-      src = p.q + (static_cast<long long>(b) * p.Hq + h) * D;
-    else
-      src = p.k_new + (static_cast<long long>(b) * p.Hkv + (h - p.Hq)) * D;
-    const uint2 lo = *reinterpret_cast<const uint2*>(src + i);
-    const uint2 hi = *reinterpret_cast<const uint2*>(src + half + i);
-    const float2 x01 = bf16x2_to_float2(lo.x), x23 = bf16x2_to_float2(lo.y);
-    const float2 y01 = bf16x2_to_float2(hi.x), y23 = bf16x2_to_float2(hi.y);
-    const float x[4] = {x01.x, x01.y, x23.x, x23.y};
-    const float y[4] = {y01.x, y01.y, y23.x, y23.y};
     const float cc[4] = {c.x, c.y, c.z, c.w};
-    const float ss[4] = {s.x, s.y, s.z, s.w};
+    const float ss4[4] = {s.x, s.y, s.z, s.w};
     float rx[4], ry[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      rx[k] = x[k] * cc[k] - y[k] * ss[k];
-      ry[k] = y[k] * cc[k] + x[k] * ss[k];
+      rx[k] = x[k] * cc[k] - y[k] * ss4[k];
+      ry[k] = y[k] * cc[k] + x[k] * ss4[k];
     }
-    if (h < p.Hq) {
+    if (is_q) {
       float* dst = p.q_rot + (static_cast<long long>(b) * p.Hq + h) * D;
       *reinterpret_cast<float4*>(dst + i) = make_float4(rx[0], rx[1], rx[2], rx[3]);
       *reinterpret_cast<float4*>(dst + half + i) = make_float4(ry[0], ry[1], ry[2], ry[3]);

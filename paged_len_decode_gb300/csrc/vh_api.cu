@@ -206,6 +206,7 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
 
 int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
                       const float* cos_sin, int max_pos, const int32_t* positions,
+                      const float* q_norm_w, const float* k_norm_w, float norm_eps,
                       vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride,
                       int64_t token_stride, int num_pages,
                       const int32_t* page_table, int max_pages_per_seq,
@@ -218,11 +219,16 @@ int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_n
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
       page_stride < 1 || token_stride < 1 || too_many_tiles(B, max_pages_per_seq, page_size))
     return VH_EINVAL;
+  if (!(norm_eps >= 0.f) || !(norm_eps < 1e30f)) return VH_EINVAL;
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin) || !aligned16(k_cache) ||
-      !aligned16(v_cache) || !aligned16(q_rot) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+      !aligned16(v_cache) || !aligned16(q_rot) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0 ||
+      !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return VH_EALIGN;
   if (!device_info()) return VH_ENODEV;
   vh::RopeAppendParams p{};
+  p.q_norm_w = q_norm_w;
+  p.k_norm_w = k_norm_w;
+  p.norm_eps = norm_eps;
   p.q = q;
   p.k_new = k_new;
   p.v_new = v_new;
@@ -369,6 +375,7 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
 
 int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
                     const float* cos_sin, int max_pos, const int32_t* positions,
+                    const float* q_norm_w, const float* k_norm_w, float norm_eps,
                     vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride, int64_t token_stride,
                     int num_pages, const int32_t* page_table, int max_pages_per_seq,
                     const int32_t* seq_lens, const int32_t* active,
@@ -382,14 +389,19 @@ int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new
       page_stride < 1 || token_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
       too_many_tiles(B, max_pages_per_seq, page_size) || !(sm_scale == sm_scale))
     return VH_EINVAL;
+  if (!(norm_eps >= 0.f) || !(norm_eps < 1e30f)) return VH_EINVAL;
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin) || !aligned16(k_cache) ||
-      !aligned16(v_cache) || !aligned16(out) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+      !aligned16(v_cache) || !aligned16(out) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0 ||
+      !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return VH_EALIGN;
   if (!workspace) return VH_EWORKSPACE;
   if (!aligned16(workspace)) return VH_EALIGN;
   const DeviceInfo* dev = device_info();
   if (!dev) return VH_ENODEV;
   AttnParams p{};
+  p.q_norm_w = q_norm_w;
+  p.k_norm_w = k_norm_w;
+  p.norm_eps = norm_eps;
   p.q = q;
   p.k_new = k_new;
   p.v_new = v_new;

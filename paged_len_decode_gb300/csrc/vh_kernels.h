@@ -25,6 +25,9 @@ struct RopeAppendParams {
   const int32_t* active;
   float* q_rot;
   int32_t* err_flag;
+  const float* q_norm_w;       // [D] RMSNorm weights of q heads, or null
+  const float* k_norm_w;       // [D] RMSNorm weights of the new k heads, or null
+  float norm_eps;
   int B, Hq, Hkv, D, P;
 };
 
@@ -58,6 +61,9 @@ struct AttnParams {
   const int32_t* positions;    // [B] or null (seq_len - 1)
   uint16_t* k_cache_w;         // writable views of the cache for the append
   uint16_t* v_cache_w;
+  const float* q_norm_w;       // [D] per-head RMSNorm weights before RoPE, or null
+  const float* k_norm_w;
+  float norm_eps;
   // shapes and plan
   int B, Hq, Hkv, D, G, P;
   int Hc;                      // kv heads per CTA = consumer warps

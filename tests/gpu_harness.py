@@ -20,6 +20,7 @@ import oracle
 ATOL, RTOL = 2e-3, 1e-2
 QROT_ATOL, QROT_RTOL = 1e-5, 1e-5
 MIDPOINT_REL = 2.0 ** -21
+MIDPOINT_REL_NORM = 2.0 ** -20  # with the RMSNorm before RoPE (a few more fp32 roundings)
 
 
 def vh():
@@ -31,7 +32,7 @@ PATHS = ("three", "fused")
 
 
 def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, graph=False,
-             repeat=1, pdl=False):
+             repeat=1, pdl=False, norm=None):
     """Run one decode step on `inp` (CPU or CUDA DecodeInputs) through the C interface.
 
     path "three": vh_rope_kv_append + vh_paged_decode_attn + vh_decode_combine;
@@ -51,17 +52,23 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     pos = positions.to(dev, torch.int32) if positions is not None else None
     k_cache, v_cache = g.pool[:, 0], g.pool[:, 1]
+    nq = nk = None
+    eps = 1e-6
+    if norm is not None:
+        nq = None if norm["q"] is None else norm["q"].to(dev)
+        nk = None if norm["k"] is None else norm["k"].to(dev)
+        eps = norm["eps"]
 
     def step():
         for _ in range(repeat):
             if path == "fused":
                 v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
                                   g.active, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
-                                  err_flag=err, pdl=pdl)
+                                  err_flag=err, pdl=pdl, q_norm_w=nq, k_norm_w=nk, norm_eps=eps)
             else:
                 v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
                               g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
-                              err_flag=err)
+                              err_flag=err, q_norm_w=nq, k_norm_w=nk, norm_eps=eps)
 
     if graph:
         # first call outside capture (sets per-device launch attributes)
@@ -86,10 +93,10 @@ def bits16(t):
     return t.contiguous().view(torch.int16).to(torch.int32) & 0xFFFF
 
 
-def midpoint_mask(x: torch.Tensor, k_in: torch.Tensor) -> torch.Tensor:
+def midpoint_mask(x: torch.Tensor, k_in: torch.Tensor, rel: float = MIDPOINT_REL) -> torch.Tensor:
     """Elements of the rotated keys x (float64 [..., D]) that lie within the fp32
-    rotation error bound of a bf16 rounding midpoint; k_in are the keys before
-    rotation (bf16 [..., D]), whose pair magnitudes set the bound."""
+    rotation error bound of a bf16 rounding midpoint; k_in are the keys fed to
+    the rotation, whose pair magnitudes set the bound."""
     ax = x.abs()
     nz = ax > 0
     e = torch.frexp(torch.where(nz, ax, torch.ones_like(ax))).exponent
@@ -99,10 +106,10 @@ def midpoint_mask(x: torch.Tensor, k_in: torch.Tensor) -> torch.Tensor:
     h = k.shape[-1] // 2
     pair = k[..., :h] + k[..., h:]
     scale = torch.cat([pair, pair], dim=-1)
-    return nz & ((frac - 0.5).abs() * ulp <= MIDPOINT_REL * scale)
+    return nz & ((frac - 0.5).abs() * ulp <= rel * scale)
 
 
-def check_append(inp, ref, gpu_pool):
+def check_append(inp, ref, gpu_pool, rel=MIDPOINT_REL):
     """Bit-exact placement: pool after the GPU append == pool after the oracle append,
     except midpoint-exempt rotated-key elements.  Returns (number of exempt
     elements, number that actually differ)."""
@@ -115,7 +122,7 @@ def check_append(inp, ref, gpu_pool):
     act = inp.active.cpu().bool()
     lens = inp.seq_lens.cpu()
     pt = inp.page_table.cpu()
-    mid = midpoint_mask(ref["k_rot"], inp.k_new.cpu())
+    mid = midpoint_mask(ref["k_rot"], ref["k_pre"], rel)
     n = 0
     for bb in torch.nonzero(act).flatten().tolist():
         L = int(lens[bb])
@@ -163,15 +170,16 @@ def check_q_rot(inp, ref_q_rot, gpu_q_rot):
 
 
 def full_check(inp, *, path="three", num_ctas=0, rows=None, positions=None, sm_scale=0.0, graph=False,
-               max_pos=None, repeat=1, pdl=False):
+               max_pos=None, repeat=1, pdl=False, norm=None):
     """Run the GPU path and the oracle on `inp`; check q_rot (three-call path),
-    the append bits and the output."""
+    the append bits and the output.  norm: dict(q, k, eps) of RMSNorm weights."""
     cpu = inp.to("cpu")
-    ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale)
+    nk = {} if norm is None else {"q_norm_w": norm["q"], "k_norm_w": norm["k"], "norm_eps": norm["eps"]}
+    ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale, **nk)
     got = run_step(inp, path=path, num_ctas=num_ctas, positions=positions, sm_scale=sm_scale, graph=graph,
-                   max_pos=max_pos, repeat=repeat, pdl=pdl)
+                   max_pos=max_pos, repeat=repeat, pdl=pdl, norm=norm)
     assert got["err"] == 0, f"device error flag {got['err']}"
-    exempt, n_diff = check_append(cpu, ref, got["pool_after"])
+    exempt, n_diff = check_append(cpu, ref, got["pool_after"], MIDPOINT_REL if norm is None else MIDPOINT_REL_NORM)
     qerr = check_q_rot(cpu, ref["q_rot"], got["q_rot"]) if path == "three" else 0.0
     oerr = check_out(cpu, ref["out"], got["out"], rows=rows)
     return {"exempt": exempt, "n_diff": n_diff, "q_rot_err": qerr, "out_err": oerr, "got": got, "ref": ref}

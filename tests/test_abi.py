@@ -82,17 +82,48 @@ def test_valid_arguments_without_device_report_no_device():
 
 def test_rope_append_argument_checks():
     f = v.lib.vh_rope_kv_append
-    base = [FAKE, FAKE, FAKE, FAKE, 4096, None, FAKE, FAKE, 2 * 16 * 8 * 128, 8 * 128, 100, FAKE, 10, FAKE,
-            FAKE, FAKE, None, 4, 16, 8, 128, 16, None]
-    assert f(*base[:3], None, *base[4:]) == v.VH_EINVAL            # cos_sin NULL
-    b = list(base); b[4] = 0
-    assert f(*b) == v.VH_EINVAL                                     # max_pos < 1
-    b = list(base); b[0] = ODD
-    assert f(*b) == v.VH_EALIGN
-    b = list(base); b[15] = ODD
-    assert f(*b) == v.VH_EALIGN                                     # q_rot misaligned
-    b = list(base); b[20] = 80
-    assert f(*b) == v.VH_EINVAL                                     # head_dim
+
+    def call(**over):
+        a = dict(q=FAKE, k=FAKE, vv=FAKE, cs=FAKE, max_pos=4096, pos=None, qw=None, kw=None, eps=1e-6,
+                 kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10, sl=FAKE,
+                 act=FAKE, q_rot=FAKE, err=None, B=4, Hq=16, Hkv=8, D=128, P=16)
+        a.update(over)
+        return f(a["q"], a["k"], a["vv"], a["cs"], a["max_pos"], a["pos"], a["qw"], a["kw"], a["eps"], a["kc"],
+                 a["vc"], a["ps"], a["ts"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["q_rot"],
+                 a["err"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
+
+    assert call(cs=None) == v.VH_EINVAL
+    assert call(max_pos=0) == v.VH_EINVAL
+    assert call(D=80) == v.VH_EINVAL
+    assert call(eps=-1.0) == v.VH_EINVAL
+    assert call(eps=float("nan")) == v.VH_EINVAL
+    assert call(q=ODD) == v.VH_EALIGN
+    assert call(q_rot=ODD) == v.VH_EALIGN
+    assert call(qw=ODD) == v.VH_EALIGN
+    assert call(kw=ODD) == v.VH_EALIGN
+
+
+def test_fused_argument_checks():
+    f = v.lib.vh_decode_fused
+
+    def call(**over):
+        a = dict(q=FAKE, k=FAKE, vv=FAKE, cs=FAKE, max_pos=4096, pos=None, qw=None, kw=None, eps=1e-6,
+                 kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10, sl=FAKE,
+                 act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None, flags=0,
+                 B=4, Hq=16, Hkv=8, D=128, P=16)
+        a.update(over)
+        return f(a["q"], a["k"], a["vv"], a["cs"], a["max_pos"], a["pos"], a["qw"], a["kw"], a["eps"], a["kc"],
+                 a["vc"], a["ps"], a["ts"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["out"], a["scale"],
+                 a["nctas"], a["ws"], a["wsb"], a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
+                 None)
+
+    assert call(q=None) == v.VH_EINVAL
+    assert call(flags=4) == v.VH_EINVAL            # unknown flag
+    assert call(Hq=24) == v.VH_EINVAL
+    assert call(eps=-0.5) == v.VH_EINVAL
+    assert call(out=ODD) == v.VH_EALIGN
+    assert call(kw=ODD) == v.VH_EALIGN
+    assert call(ws=None) == v.VH_EWORKSPACE
 
 
 def test_rope_table_and_combine_argument_checks():

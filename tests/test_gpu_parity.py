@@ -241,3 +241,33 @@ def test_large_batch_of_short_rows(path):
     inp = workloads.make_case(B=2048, Hq=8, Hkv=4, D=128, P=16, seq_lens=lens, active=active, seed=18,
                               device="cuda", max_pages_per_seq=3)
     H.full_check(inp, path=path)
+
+
+# ---------------------------------------------------------------- per-head RMSNorm before RoPE
+
+def _norm(D, seed, eps=1e-6):
+    g = torch.Generator().manual_seed(seed)
+    return {"q": (1.0 + 0.2 * torch.randn(D, generator=g)).float(),
+            "k": (1.0 + 0.2 * torch.randn(D, generator=g)).float(), "eps": eps}
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("name", ["tiny", "c64", "long", "high"])
+def test_qk_rms_norm_parity(name, path):
+    inp = workloads.make_inputs(name, device="cuda")
+    H.full_check(inp, path=path, norm=_norm(inp.D, 40 + inp.D))
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_qk_rms_norm_groups_and_dims(G, D, path):
+    inp = case([37, 300, 129, 1], Hq=G * 2, Hkv=2, D=D, seed=G * 10 + D + 1)
+    H.full_check(inp, path=path, norm=_norm(D, G + D, eps=1e-5))
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_qk_rms_norm_of_q_only(path):
+    inp = case([77, 16, 5], seed=41)
+    nm = _norm(inp.D, 41)
+    H.full_check(inp, path=path, norm={"q": nm["q"], "k": None, "eps": 1e-6})
