@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
 CPU-baseline leg are the only callers.  Nothing here imports or links the
 CUDA library, and the CUDA library never calls into this package.
 
-All functions take CPU torch tensors: bf16 tensors are read as their bit
-patterns, float64 tensors are used as is.  See oracle.c for what each step
+All functions take CPU torch tensors: bf16 / fp16 tensors are read as their
+bit patterns (the element type is taken from the tensor's dtype), float64
+tensors are used as is.  See oracle.c for what each step
 computes and which passage it follows.
 """
 from __future__ import annotations
@@ -45,16 +46,20 @@ def _load():
             lib.oracle_bf16_from_double.restype = ctypes.c_uint16
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_double.restype = D
+            lib.oracle_f16_from_double.argtypes = [D]
+            lib.oracle_f16_from_double.restype = ctypes.c_uint16
+            lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_double.restype = D
             lib.oracle_num_threads.restype = I
             lib.oracle_set_num_threads.argtypes = [I]
             lib.oracle_rope_kv_append.argtypes = [P, P, P, P, P, P, D, P, P, I64, I64, P, I, I, P, P, P, P,
-                                                  P, I, I, I, I, I, D]
+                                                  P, I, I, I, I, I, D, I, I]
             lib.oracle_rope_kv_append.restype = I
             lib.oracle_decode_attn.argtypes = [P, P, P, I64, I64, P, I, P, P, P, P, D, P, I,
-                                               I, I, I, I, I]
+                                               I, I, I, I, I, I]
             lib.oracle_decode_attn.restype = None
             lib.oracle_decode_attn_split.argtypes = [P, P, P, I64, I64, P, I, P, P, P, D, I,
-                                                     I, I, I, I, I]
+                                                     I, I, I, I, I, I]
             lib.oracle_decode_attn_split.restype = None
             lib.oracle_lse_combine.argtypes = [P, P, I, I, P]
             lib.oracle_lse_combine.restype = D
@@ -90,19 +95,40 @@ def bf16_to_double(bits: int) -> float:
     return float(_load().oracle_bf16_to_double(bits & 0xFFFF))
 
 
+def f16_from_double(x: float) -> int:
+    """IEEE binary16 bit pattern nearest to x (ties to even), one rounding step."""
+    return int(_load().oracle_f16_from_double(float(x)))
+
+
+def f16_to_double(bits: int) -> float:
+    return float(_load().oracle_f16_to_double(bits & 0xFFFF))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return 1
+    assert t.dtype == torch.bfloat16, t.dtype
+    return 0
+
+
 def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, theta,
                    positions=None, num_pages=None, return_k_rot=False, in_place=False,
-                   q_norm_w=None, k_norm_w=None, norm_eps=1e-6, return_k_pre=False):
-    """RoPE + append on a copy of `pool` ([NP, 2, P, Hkv, D] bf16), or on `pool`
-    itself when in_place (a contiguous CPU tensor).
+                   q_norm_w=None, k_norm_w=None, norm_eps=1e-6, return_k_pre=False,
+                   interleaved=False):
+    """RoPE + append on a copy of `pool` ([NP, 2, P, Hkv, D] bf16 or fp16, the
+    type of q, k_new and v_new), or on `pool` itself when in_place (a
+    contiguous CPU tensor).
 
     Returns (q_rot float64 [B, Hq, D], pool_after bf16, n_bad), plus the
     unrounded rotated keys float64 [B, Hkv, D] if return_k_rot, plus the keys
     fed to RoPE if return_k_pre.  Rows with active == 0 keep q_rot = 0 and
     write nothing.  q_norm_w / k_norm_w (length-D weights, or None) switch on
-    the per-head RMSNorm before RoPE.
+    the per-head RMSNorm before RoPE.  interleaved pairs elements (2i, 2i+1)
+    instead of (i, i + D/2).
     """
     lib = _load()
+    dt = _dtype_code(q)
+    assert k_new.dtype == q.dtype and v_new.dtype == q.dtype and pool.dtype == q.dtype
     B, Hq, D = q.shape
     Hkv = k_new.shape[1]
     if in_place:
@@ -133,7 +159,7 @@ def rope_kv_append(q, k_new, v_new, pool, page_table, seq_lens, active, *, P, th
                                     page_stride, token_stride, _ptr(pt), pt.shape[1],
                                     NP if num_pages is None else num_pages,
                                     _ptr(sl), _ptr(ac), _ptr(q_rot), _ptr(k_rot), _ptr(k_pre),
-                                    B, Hq, Hkv, D, P, float(theta))
+                                    B, Hq, Hkv, D, P, float(theta), dt, int(bool(interleaved)))
     res = (q_rot, pool_after, int(bad))
     if return_k_rot:
         res = res + (k_rot,)
@@ -146,7 +172,7 @@ def decode_attn(q_rot, pool, page_table, seq_lens, active, *, P, sm_scale=0.0, r
                 return_lse=False):
     """Softmax attention of every (or the listed) row over its paged keys.
 
-    q_rot: float64 [B, Hq, D]; pool: bf16 [NP, 2, P, Hkv, D].
+    q_rot: float64 [B, Hq, D]; pool: bf16 or fp16 [NP, 2, P, Hkv, D].
     Returns float64 out [B, Hq, D] (rows not listed stay zero), and the
     natural-log lse [B, Hq] if return_lse.
     """
@@ -165,7 +191,7 @@ def decode_attn(q_rot, pool, page_table, seq_lens, active, *, P, sm_scale=0.0, r
                            ctypes.c_void_p(bits.data_ptr() + P * Hkv * D * 2),
                            2 * P * Hkv * D, Hkv * D, _ptr(pt), pt.shape[1], _ptr(sl), _ptr(ac),
                            _ptr(out), _ptr(lse), float(sm_scale), _ptr(rw),
-                           0 if rw is None else rw.numel(), B, Hq, Hkv, D, P)
+                           0 if rw is None else rw.numel(), B, Hq, Hkv, D, P, _dtype_code(pool))
     return (out, lse) if return_lse else out
 
 
@@ -184,7 +210,7 @@ def decode_attn_split(q_rot, pool, page_table, seq_lens, active, *, P, n_splits,
                                  ctypes.c_void_p(bits.data_ptr() + P * Hkv * D * 2),
                                  2 * P * Hkv * D, Hkv * D, _ptr(pt), pt.shape[1], _ptr(sl),
                                  _ptr(ac), _ptr(out), float(sm_scale), int(n_splits),
-                                 B, Hq, Hkv, D, P)
+                                 B, Hq, Hkv, D, P, _dtype_code(pool))
     return out
 
 
@@ -200,17 +226,18 @@ def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor):
 
 
 def reference_step(inp, positions=None, rows=None, sm_scale=0.0, q_norm_w=None, k_norm_w=None,
-                   norm_eps=1e-6):
+                   norm_eps=1e-6, interleaved=False):
     """Whole step on one layer's inputs (any object with the DecodeInputs fields).
 
     Returns dict(q_rot, k_rot, k_pre, pool_after, out, n_bad): (RMSNorm +) RoPE
     + append, then attention over the appended cache.  k_rot is the rotated key
-    before its bf16 rounding, k_pre the key fed to RoPE.
+    before its rounding to the cache type, k_pre the key fed to RoPE.
     """
     q_rot, pool_after, bad, k_rot, k_pre = rope_kv_append(
         inp.q, inp.k_new, inp.v_new, inp.pool, inp.page_table, inp.seq_lens, inp.active, P=inp.P,
         theta=inp.theta, positions=positions, num_pages=inp.num_pages, return_k_rot=True,
-        q_norm_w=q_norm_w, k_norm_w=k_norm_w, norm_eps=norm_eps, return_k_pre=True)
+        q_norm_w=q_norm_w, k_norm_w=k_norm_w, norm_eps=norm_eps, return_k_pre=True,
+        interleaved=interleaved)
     out = decode_attn(q_rot, pool_after, inp.page_table, inp.seq_lens, inp.active, P=inp.P,
                       rows=rows, sm_scale=sm_scale)
     return {"q_rot": q_rot, "k_rot": k_rot, "k_pre": k_pre, "pool_after": pool_after, "out": out,

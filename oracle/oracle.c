@@ -32,7 +32,7 @@
  *   - q head g reads kv head g / (Hq/Hkv);
  *   - rows with active == 0 produce an all-zero output and write nothing.
  *
- * bf16 arrays are passed as uint16_t bit patterns.  Strides are in elements.
+ * bf16 / fp16 arrays are passed as uint16_t bit patterns.  Strides are in elements.
  */
 #include <math.h>
 #include <stdint.h>
@@ -76,6 +76,46 @@ uint16_t oracle_bf16_from_double(double x) {
 
 double oracle_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
 
+/* ---- fp16 (IEEE binary16) <-> double ---------------------------------- */
+
+static double f16_to_double(uint16_t h) {
+    int sign = h >> 15, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0x1F) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, -24);            /* subnormal: m * 2^-24 */
+    else v = ldexp((double)(m | 0x400), e - 25);            /* (1.m) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Nearest binary16 to a double (ties to even), one rounding step: 11
+ * significant bits, exponent range [-14, 15], subnormal quantum 2^-24. */
+uint16_t oracle_f16_from_double(double x) {
+    if (isnan(x)) return 0x7E00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                     /* a in [2^(e-1), 2^e) */
+    int qexp = e - 11;
+    if (qexp < -24) qexp = -24;
+    double r = nearbyint(ldexp(a, -qexp));
+    double y = ldexp(r, qexp);
+    if (y >= 65520.0) return sign | 0x7C00;  /* beyond max (65504) + half ulp: inf */
+    /* encode y exactly */
+    if (y < ldexp(1.0, -14)) return sign | (uint16_t)nearbyint(ldexp(y, 24));
+    int ey;
+    double fy = frexp(y, &ey);        /* y = fy * 2^ey, fy in [0.5, 1) */
+    int E = ey - 1 + 15;
+    int M = (int)nearbyint(ldexp(fy, 11)) - 1024;
+    return sign | (uint16_t)(E << 10) | (uint16_t)M;
+}
+
+double oracle_f16_to_double(uint16_t h) { return f16_to_double(h); }
+
+/* element type of q / k / v / cache / out: 0 = bf16, 1 = fp16 */
+static double elem_to_double(uint16_t h, int dtype) { return dtype ? f16_to_double(h) : bf16_to_double(h); }
+static uint16_t elem_from_double(double x, int dtype) { return dtype ? oracle_f16_from_double(x) : oracle_bf16_from_double(x); }
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -108,21 +148,23 @@ static void rms_norm(double* x, int D, const double* w, double eps) {
 
 /* ---- RoPE + append ---------------------------------------------------- */
 
-/* Rotate one head vector x[0..D) in place by position pos ("rotate half"):
- *   a_i = pos * theta^(-2i/D)
- *   x'_i       = x_i cos a_i - x_{i+D/2} sin a_i
- *   x'_{i+D/2} = x_{i+D/2} cos a_i + x_i sin a_i
+/* Rotate one head vector x[0..D) in place by position pos.  Pair i of
+ * frequency a_i = pos * theta^(-2i/D) is (i, i + D/2) ("rotate half") or, with
+ * interleaved, (2i, 2i + 1):
+ *   x'_first  = x_first cos a_i - x_second sin a_i
+ *   x'_second = x_second cos a_i + x_first sin a_i
  * The pages ask for RoPE cos/sin in fp32 or better for alignment with the
  * reference model ("Engineering TTS inference in vLLM-Omni", Qwen3-TTS,
  * section 4 "numerical precision: fp32 alignment"); here they are float64. */
-static void rope_rotate(double* x, int D, double pos, double theta) {
+static void rope_rotate(double* x, int D, double pos, double theta, int interleaved) {
     int half = D / 2;
     for (int i = 0; i < half; ++i) {
         double a = pos * pow(theta, -2.0 * (double)i / (double)D);
         double c = cos(a), s = sin(a);
-        double lo = x[i], hi = x[i + half];
-        x[i] = lo * c - hi * s;
-        x[i + half] = hi * c + lo * s;
+        int i0 = interleaved ? 2 * i : i, i1 = interleaved ? 2 * i + 1 : i + half;
+        double lo = x[i0], hi = x[i1];
+        x[i0] = lo * c - hi * s;
+        x[i1] = hi * c + lo * s;
     }
 }
 
@@ -134,7 +176,9 @@ static void rope_rotate(double* x, int D, double pos, double theta) {
  * written into the paged cache, then attention runs over it), and its rule
  * that padding entries write nothing (section "How a program runs").
  *
- * q, k_new, v_new: bf16 [B][Hq][D], [B][Hkv][D], [B][Hkv][D].
+ * q, k_new, v_new: [B][Hq][D], [B][Hkv][D], [B][Hkv][D] of the element type
+ *   dtype (0 = bf16, 1 = fp16; the Fish kernel takes fp16 or bf16); the
+ *   rotated key is rounded to that type.  interleaved selects the RoPE pairing.
  * positions: NULL means seq_len - 1.
  * q_norm_w, k_norm_w: per-dim RMSNorm weights [D] applied to every q / new-k
  *   head before RoPE, or NULL for none; norm_eps is the epsilon.
@@ -155,7 +199,7 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
                           const int32_t* page_table, int max_pages_per_seq, int num_pages,
                           const int32_t* seq_lens, const int32_t* active,
                           double* q_rot, double* k_rot, double* k_pre,
-                          int B, int Hq, int Hkv, int D, int P, double theta) {
+                          int B, int Hq, int Hkv, int D, int P, double theta, int dtype, int interleaved) {
     int bad = 0;
     double* tmp = (double*)malloc(sizeof(double) * (size_t)D);
     for (int b = 0; b < B; ++b) {
@@ -165,9 +209,9 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
         double pos = positions ? (double)positions[b] : (double)(L - 1);
         for (int g = 0; g < Hq; ++g) {
             const uint16_t* src = q + ((size_t)b * Hq + g) * D;
-            for (int d = 0; d < D; ++d) tmp[d] = bf16_to_double(src[d]);
+            for (int d = 0; d < D; ++d) tmp[d] = elem_to_double(src[d], dtype);
             rms_norm(tmp, D, q_norm_w, norm_eps);
-            rope_rotate(tmp, D, pos, theta);
+            rope_rotate(tmp, D, pos, theta, interleaved);
             memcpy(q_rot + ((size_t)b * Hq + g) * D, tmp, sizeof(double) * (size_t)D);
         }
         int slot = L - 1;
@@ -177,15 +221,15 @@ int oracle_rope_kv_append(const uint16_t* q, const uint16_t* k_new, const uint16
         for (int h = 0; h < Hkv; ++h) {
             const uint16_t* ks = k_new + ((size_t)b * Hkv + h) * D;
             const uint16_t* vs = v_new + ((size_t)b * Hkv + h) * D;
-            for (int d = 0; d < D; ++d) tmp[d] = bf16_to_double(ks[d]);
+            for (int d = 0; d < D; ++d) tmp[d] = elem_to_double(ks[d], dtype);
             rms_norm(tmp, D, k_norm_w, norm_eps);
             if (k_pre) memcpy(k_pre + ((size_t)b * Hkv + h) * D, tmp, sizeof(double) * (size_t)D);
-            rope_rotate(tmp, D, pos, theta);
+            rope_rotate(tmp, D, pos, theta, interleaved);
             if (k_rot) memcpy(k_rot + ((size_t)b * Hkv + h) * D, tmp, sizeof(double) * (size_t)D);
             uint16_t* kd = k_cache + (int64_t)page * page_stride + (int64_t)off * token_stride + (int64_t)h * D;
             uint16_t* vd = v_cache + (int64_t)page * page_stride + (int64_t)off * token_stride + (int64_t)h * D;
             for (int d = 0; d < D; ++d) {
-                kd[d] = oracle_bf16_from_double(tmp[d]);
+                kd[d] = elem_from_double(tmp[d], dtype);
                 vd[d] = vs[d];
             }
         }
@@ -209,12 +253,12 @@ static const uint16_t* key_row(const uint16_t* cache, int64_t page_stride, int64
 static double attend_range(const double* qv, const uint16_t* k_cache, const uint16_t* v_cache,
                            int64_t page_stride, int64_t token_stride, const int32_t* pt_row,
                            int P, int h, int D, int j0, int j1, double sm_scale,
-                           double* s, double* o) {
+                           double* s, double* o, int dtype) {
     double m = -INFINITY;
     for (int j = j0; j < j1; ++j) {
         const uint16_t* kr = key_row(k_cache, page_stride, token_stride, pt_row, P, j, h, D);
         double acc = 0.0;
-        for (int d = 0; d < D; ++d) acc += qv[d] * bf16_to_double(kr[d]);
+        for (int d = 0; d < D; ++d) acc += qv[d] * elem_to_double(kr[d], dtype);
         s[j - j0] = acc * sm_scale;
         if (s[j - j0] > m) m = s[j - j0];
     }
@@ -224,7 +268,7 @@ static double attend_range(const double* qv, const uint16_t* k_cache, const uint
         double p = exp(s[j - j0] - m);
         l += p;
         const uint16_t* vr = key_row(v_cache, page_stride, token_stride, pt_row, P, j, h, D);
-        for (int d = 0; d < D; ++d) o[d] += p * bf16_to_double(vr[d]);
+        for (int d = 0; d < D; ++d) o[d] += p * elem_to_double(vr[d], dtype);
     }
     for (int d = 0; d < D; ++d) o[d] /= l;
     return m + log(l);
@@ -249,7 +293,7 @@ void oracle_decode_attn(const double* q_rot, const uint16_t* k_cache, const uint
                         const int32_t* seq_lens, const int32_t* active,
                         double* out, double* lse_out, double sm_scale,
                         const int32_t* rows, int n_rows,
-                        int B, int Hq, int Hkv, int D, int P) {
+                        int B, int Hq, int Hkv, int D, int P, int dtype) {
     if (sm_scale <= 0.0) sm_scale = 1.0 / sqrt((double)D);
     int G = Hq / Hkv;
     int nr = rows ? n_rows : B;
@@ -273,7 +317,7 @@ void oracle_decode_attn(const double* q_rot, const uint16_t* k_cache, const uint
             const int32_t* pt_row = page_table + (size_t)b * max_pages_per_seq;
             double lse = attend_range(q_rot + ((size_t)b * Hq + g) * D, k_cache, v_cache,
                                       page_stride, token_stride, pt_row, P, g / G, D, 0, L,
-                                      sm_scale, s, o);
+                                      sm_scale, s, o, dtype);
             if (lse_out) lse_out[(size_t)b * Hq + g] = lse;
         }
         free(s);
@@ -313,7 +357,7 @@ void oracle_decode_attn_split(const double* q_rot, const uint16_t* k_cache, cons
                               const int32_t* page_table, int max_pages_per_seq,
                               const int32_t* seq_lens, const int32_t* active,
                               double* out, double sm_scale, int n_splits,
-                              int B, int Hq, int Hkv, int D, int P) {
+                              int B, int Hq, int Hkv, int D, int P, int dtype) {
     if (sm_scale <= 0.0) sm_scale = 1.0 / sqrt((double)D);
     int G = Hq / Hkv;
     for (int b = 0; b < B; ++b) {
@@ -338,7 +382,7 @@ void oracle_decode_attn_split(const double* q_rot, const uint16_t* k_cache, cons
                 }
                 lp[k] = attend_range(q_rot + ((size_t)b * Hq + g) * D, k_cache, v_cache, page_stride,
                                      token_stride, pt_row, P, g / G, D, j0, j1, sm_scale, s,
-                                     op + (size_t)k * D);
+                                     op + (size_t)k * D, dtype);
             }
             oracle_lse_combine(op, lp, S, D, o);
             free(op);

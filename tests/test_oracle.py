@@ -479,3 +479,157 @@ def test_rms_norm_step_matches_brute_force():
     kp = r["k_pre"][0, 1]
     ref = torch.nn.functional.rms_norm(inp.k_new[0, 1].double().view(1, -1), (8,), weight=kw.double(), eps=1e-5)
     assert torch.allclose(kp, ref.view(-1), atol=1e-14)
+
+
+# ---------------------------------------------------------------- fp16 element type
+
+@pytest.mark.parametrize("x,bits", [
+    (1.0, 0x3C00),
+    (-2.0, 0xC000),
+    (1.0 + 2 ** -11, 0x3C00),              # midpoint between 0x3C00 (even) and 0x3C01: down
+    (1.0 + 3 * 2 ** -11, 0x3C02),          # midpoint between 0x3C01 (odd) and 0x3C02: up
+    (1.0 + 2 ** -11 + 2 ** -40, 0x3C01),   # just above the midpoint: up
+    (65504.0, 0x7BFF),                     # largest finite
+    (65519.99, 0x7BFF),                    # below the midpoint to 2^16: stays finite
+    (65520.0, 0x7C00),                     # the midpoint itself rounds to even = inf
+    (2 ** -24, 0x0001),                    # smallest subnormal
+    (2 ** -25, 0x0000),                    # half of it: tie to even (zero)
+    (3 * 2 ** -25, 0x0002),                # 1.5 quanta: tie to even (2)
+    (2 ** -14, 0x0400),                    # smallest normal
+    (2 ** -14 - 2 ** -25, 0x0400),         # midpoint below it: rounds up to the even normal
+    (0.0, 0x0000),
+    (-0.0, 0x8000),
+])
+def test_f16_rounding_fixed_points(x, bits):
+    assert oracle.f16_from_double(x) == bits
+    assert brute.f16_round_bits(x) == bits
+
+
+def test_f16_decode_every_pattern():
+    # every finite / infinite binary16 pattern against Python's own half codec
+    import struct
+    for bits in range(0x10000):
+        want = struct.unpack("<e", struct.pack("<H", bits))[0]
+        got = oracle.f16_to_double(bits)
+        if math.isnan(want):
+            assert math.isnan(got)
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), hex(bits)
+
+
+def test_f16_rounding_matches_exact_bracketing_and_numpy():
+    np = pytest.importorskip("numpy")
+    g = torch.Generator().manual_seed(17)
+    xs = (torch.randn(2000, generator=g, dtype=torch.float64) * 8).tolist()
+    xs += (torch.randn(500, generator=g, dtype=torch.float64) * 2 ** -18).tolist()   # subnormals
+    xs += (torch.randn(200, generator=g, dtype=torch.float64) * 3e4).tolist()        # near overflow
+    for bits in list(range(0x3C00, 0x3C40)) + list(range(0x0001, 0x0020)) + [0x7BFE]:
+        a, b = brute.f16_bits_to_float(bits), brute.f16_bits_to_float(bits + 1)
+        xs.append((a + b) / 2)
+    for x in xs:
+        o = oracle.f16_from_double(x)
+        assert o == brute.f16_round_bits(x), x
+        # numpy converts float64 -> float16 in one correctly rounded step
+        with np.errstate(over="ignore"):
+            want = int(np.array([x], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
+        assert o == want, x
+
+
+def _fp16_case(lens, **kw):
+    return _small_case(lens, dtype=torch.float16, **kw)
+
+
+def test_fp16_attention_matches_torch_sdpa_on_fp16_cache():
+    inp = _fp16_case([70, 3, 33], D=64, Hq=4, Hkv=4, seed=3)
+    r = _step(inp)
+    assert r["pool_after"].dtype == torch.float16
+    for b in range(inp.B):
+        L = int(inp.seq_lens[b])
+        idx = [(int(inp.page_table[b, j // inp.P]), j % inp.P) for j in range(L)]
+        K = torch.stack([_f64(r["pool_after"][p, 0, o]) for p, o in idx], dim=1)
+        V = torch.stack([_f64(r["pool_after"][p, 1, o]) for p, o in idx], dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(r["q_rot"][b].unsqueeze(1), K, V).squeeze(1)
+        assert torch.allclose(r["out"][b], ref, atol=1e-13, rtol=0)
+    # the appended key is the fp16 rounding of the rotated key (not the bf16 one)
+    b = 1
+    L = int(inp.seq_lens[b])
+    page, off = int(inp.page_table[b, (L - 1) // inp.P]), (L - 1) % inp.P
+    want = [oracle.f16_from_double(v) for v in r["k_rot"][b].flatten().tolist()]
+    assert _bits(r["pool_after"][page, 0, off]).flatten().tolist() == want
+    assert torch.equal(_bits(r["pool_after"][page, 1, off]), _bits(inp.v_new[b]))
+
+
+def test_fp16_inputs_are_read_as_fp16():
+    # the same float32 draws as bf16 and as fp16 give different q_rot (values
+    # read in the wrong format would be garbage, not a small difference)
+    a = _small_case([20], D=16, seed=5)
+    b = _fp16_case([20], D=16, seed=5)
+    ra, rb = _step(a), _step(b)
+    assert torch.allclose(ra["q_rot"], rb["q_rot"], atol=0.05)
+    assert not torch.equal(ra["q_rot"], rb["q_rot"])
+    assert torch.equal(rb["q_rot"][0], oracle.rope_kv_append(
+        b.q, b.k_new, b.v_new, b.pool, b.page_table, b.seq_lens, b.active, P=b.P,
+        theta=b.theta)[0][0])
+
+
+# ---------------------------------------------------------------- interleaved RoPE
+
+def test_interleaved_rope_is_complex_rotation():
+    # GPT-J pairing: (x_2i + i x_2i+1) * exp(i pos theta^(-2i/D)), in complex128
+    g = torch.Generator().manual_seed(31)
+    D, theta = 64, 10000.0
+    for dtype in (torch.bfloat16, torch.float16):
+        q = torch.randn((2, 3, D), generator=g).to(dtype)
+        k = torch.randn((2, 1, D), generator=g).to(dtype)
+        pool = torch.zeros((4, 2, 16, 1, D), dtype=dtype)
+        pos = torch.tensor([0, 4097])
+        q_rot, _, bad, k_rot = oracle.rope_kv_append(
+            q, k, k, pool, torch.tensor([[1], [2]]), torch.tensor([1, 1]), torch.tensor([1, 1]), P=16,
+            theta=theta, positions=pos, return_k_rot=True, interleaved=True)
+        assert bad == 0
+        freq = theta ** (-2.0 * torch.arange(D // 2, dtype=torch.float64) / D)
+        for x, got in ((q, q_rot), (k, k_rot)):
+            z = torch.view_as_complex(x.to(torch.float64).reshape(2, x.shape[1], D // 2, 2).contiguous())
+            rot = torch.polar(torch.ones_like(freq), pos.to(torch.float64).view(2, 1, 1) * freq)
+            want = torch.view_as_real(z * rot).reshape(2, x.shape[1], D)
+            assert torch.allclose(got, want, atol=1e-12, rtol=0)
+
+
+def test_interleaved_is_rotate_half_on_deinterleaved_vectors():
+    # permuting (2i, 2i+1) -> (i, i + D/2) turns one pairing into the other
+    inp = _small_case([40, 7], D=32, Hq=4, Hkv=2, seed=9)
+    D = inp.D
+    perm = torch.cat([torch.arange(0, D, 2), torch.arange(1, D, 2)])   # new[j] = old[perm[j]]
+    r_int = oracle.reference_step(inp, interleaved=True)
+    de = inp.clone()
+    de.q = inp.q[..., perm].contiguous()
+    de.k_new = inp.k_new[..., perm].contiguous()
+    de.v_new = inp.v_new[..., perm].contiguous()
+    de.pool = inp.pool[..., perm].contiguous()
+    r_half = oracle.reference_step(de)
+    inv = torch.argsort(perm)
+    assert torch.equal(r_half["q_rot"][..., inv], r_int["q_rot"])
+    assert torch.equal(_bits(r_half["pool_after"][..., inv]), _bits(r_int["pool_after"]))
+    assert torch.allclose(r_half["out"][..., inv], r_int["out"], atol=1e-14, rtol=0)
+    # and the two pairings do differ on the same vectors
+    assert not torch.allclose(oracle.reference_step(inp)["q_rot"], r_int["q_rot"])
+
+
+@pytest.mark.parametrize("dtype,interleaved,norm", [
+    ("fp16", False, False), ("fp16", True, False), ("bf16", True, False), ("fp16", True, True)])
+def test_fp16_and_interleaved_step_matches_brute_force(dtype, interleaved, norm):
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    inp = _small_case([17, 5, 33], Hq=4, Hkv=2, D=8, P=16, seed=23, dtype=tdt)
+    qw = kw = None
+    if norm:
+        qw, kw = _norm_weights(inp.D, 1), _norm_weights(inp.D, 2)
+    r = oracle.reference_step(inp, interleaved=interleaved, q_norm_w=qw, k_norm_w=kw)
+    pool = _nested(inp.pool)
+    q_rot, out = brute.step(_nested(inp.q), _nested(inp.k_new), _nested(inp.v_new), pool,
+                            inp.page_table.tolist(), inp.seq_lens.tolist(), inp.active.tolist(),
+                            inp.P, inp.theta, dtype=dtype, interleaved=interleaved,
+                            q_norm_w=None if qw is None else qw.tolist(),
+                            k_norm_w=None if kw is None else kw.tolist())
+    assert torch.allclose(r["q_rot"], torch.tensor(q_rot, dtype=torch.float64), atol=1e-12, rtol=0)
+    assert torch.allclose(r["out"], torch.tensor(out, dtype=torch.float64), atol=1e-12, rtol=0)
+    assert _nested(r["pool_after"]) == pool

@@ -19,8 +19,8 @@ The five workloads are the serving shapes of the Talker decode step:
 
 Layout of one layer's pool (the paged KV layout of the vox-serve "Adding a
 Model" page, section "1. The model code", with the layer axis dropped because
-every layer here owns its own pool):  bf16 [num_pages, 2, page_size,
-num_kv_heads, head_dim], K at [:, 0] and V at [:, 1].
+every layer here owns its own pool):  bf16 (or fp16) [num_pages, 2,
+page_size, num_kv_heads, head_dim], K at [:, 0] and V at [:, 1].
 
 Recipe (seed = 20260000 + 100 * workload_index + layer, torch.Generator):
   1. seq_lens: integers uniform in [lo, hi], or floor(exp(U(ln lo, ln hi)))
@@ -31,12 +31,13 @@ Recipe (seed = 20260000 + 100 * workload_index + layer, torch.Generator):
   3. pages: page 0 is the reserved dummy page and the last page is a guard
      page.  Live pages are a seeded permutation of 1 .. num_pages - 2,
      handed out to the active rows in row order and logical page order.
-  4. pool values: randn * sigma rounded to bf16; every slot that holds no
+  4. pool values: randn * sigma rounded to the element type; every slot that holds no
      cached token (page 0, the guard page, unused pages, the tail of each
      row's last page and the slot the new token will be appended to) is
      filled with a quiet-NaN bit pattern, so a read of a stale slot shows up
      in the output.
-  5. q ~ N(0, 1); k_new, v_new ~ N(0, sigma); all bf16.
+  5. q ~ N(0, 1); k_new, v_new ~ N(0, sigma); all bf16, or all fp16 when
+     fp16 is asked for (the same float32 draws, rounded to fp16 instead).
 
 The generator runs on any torch device; large pools are drawn on the GPU and
 copied to the host where the oracle needs them.
@@ -48,7 +49,9 @@ from dataclasses import dataclass, field
 
 import torch
 
-NAN_BF16 = 0x7FC0  # quiet NaN as a bf16 bit pattern
+# 0x7FC0 is a quiet NaN both as bf16 (exponent all ones, mantissa 0x40) and
+# as fp16 (exponent 0x1F, mantissa 0x3C0), so one pattern poisons either type.
+NAN_BITS = 0x7FC0
 SEED_BASE = 20260000
 
 
@@ -97,7 +100,8 @@ WORKLOADS = {
 
 @dataclass
 class DecodeInputs:
-    """One layer's inputs.  Tensors live on `device`; bf16 tensors are torch.bfloat16."""
+    """One layer's inputs.  Tensors live on `device`; q, k_new, v_new and pool
+    are all torch.bfloat16 or all torch.float16."""
     B: int
     Hq: int
     Hkv: int
@@ -106,10 +110,10 @@ class DecodeInputs:
     max_pages_per_seq: int
     num_pages: int
     theta: float
-    q: torch.Tensor            # [B, Hq, D] bf16
-    k_new: torch.Tensor        # [B, Hkv, D] bf16
-    v_new: torch.Tensor        # [B, Hkv, D] bf16
-    pool: torch.Tensor         # [NP, 2, P, Hkv, D] bf16 (K at [:,0], V at [:,1])
+    q: torch.Tensor            # [B, Hq, D] bf16 / fp16
+    k_new: torch.Tensor        # [B, Hkv, D]
+    v_new: torch.Tensor        # [B, Hkv, D]
+    pool: torch.Tensor         # [NP, 2, P, Hkv, D] (K at [:,0], V at [:,1])
     page_table: torch.Tensor   # [B, MPS] int32
     seq_lens: torch.Tensor     # [B] int32
     active: torch.Tensor       # [B] int32
@@ -160,14 +164,17 @@ def draw_lengths(w: Workload, gen: torch.Generator, n: int) -> torch.Tensor:
 def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=None,
               max_pages_per_seq: int | None = None, sigma: float = 1.0, seed: int = 0,
               device="cpu", pool_pages: int = 0, theta: float = 10000.0,
-              poison: bool = True, page_order: str = "random") -> DecodeInputs:
+              poison: bool = True, page_order: str = "random",
+              dtype: torch.dtype = torch.bfloat16) -> DecodeInputs:
     """Draw one layer of inputs for explicit shapes and lengths.
 
     `seq_lens` and `active` are Python sequences (or int64 tensors) of length B.
     Padding rows (active == 0) get seq_len 1 and an all-zero page-table row
     unless the caller passes other lengths for them on purpose.
     `page_order` is "random" (seeded permutation) or "linear" (pages 1, 2, ...).
+    `dtype` (torch.bfloat16 or torch.float16) is the type of q, k, v and the pool.
     """
+    assert dtype in (torch.bfloat16, torch.float16)
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     lens = torch.as_tensor(seq_lens, dtype=torch.int64).clone()
@@ -193,10 +200,10 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     dev = torch.device(device)
     dgen = torch.Generator(device=dev)
     dgen.manual_seed(int(torch.randint(0, 2**62, (1,), generator=gen)))
-    pool = (torch.randn((NP, 2, P, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(torch.bfloat16)
-    q = torch.randn((B, Hq, D), generator=dgen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    k_new = (torch.randn((B, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(torch.bfloat16)
-    v_new = (torch.randn((B, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(torch.bfloat16)
+    pool = (torch.randn((NP, 2, P, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(dtype)
+    q = torch.randn((B, Hq, D), generator=dgen, device=dev, dtype=torch.float32).to(dtype)
+    k_new = (torch.randn((B, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(dtype)
+    v_new = (torch.randn((B, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(dtype)
 
     if poison:
         live = torch.zeros((NP, P), dtype=torch.bool)
@@ -208,7 +215,7 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
             live[page_table[b, j // P], j % P] = True
         bits = pool.view(torch.int16)
         dead = (~live).to(dev)
-        bits.masked_fill_(dead.view(NP, 1, P, 1, 1).expand_as(bits), NAN_BF16)
+        bits.masked_fill_(dead.view(NP, 1, P, 1, 1).expand_as(bits), NAN_BITS)
 
     return DecodeInputs(
         B=B, Hq=Hq, Hkv=Hkv, D=D, P=P, max_pages_per_seq=mps, num_pages=NP, theta=theta,
@@ -219,7 +226,7 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     )
 
 
-def make_inputs(name: str, layer: int = 0, device="cpu") -> DecodeInputs:
+def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = torch.bfloat16) -> DecodeInputs:
     """Inputs of one layer of a named workload (see the module docstring)."""
     w = WORKLOADS[name]
     seed = SEED_BASE + 100 * w.index + layer
@@ -236,13 +243,13 @@ def make_inputs(name: str, layer: int = 0, device="cpu") -> DecodeInputs:
     sub_seed = int(torch.randint(0, 2**31 - 1, (1,), generator=gen))
     inp = make_case(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, P=w.P, seq_lens=lens, active=act,
                     max_pages_per_seq=w.max_pages_per_seq, sigma=w.sigma, seed=sub_seed,
-                    device=device, pool_pages=w.pool_pages, theta=w.theta)
+                    device=device, pool_pages=w.pool_pages, theta=w.theta, dtype=dtype)
     inp.meta.update({"workload": name, "layer": layer, "workload_seed": seed})
     return inp
 
 
 def kv_bytes(inp: DecodeInputs) -> int:
-    """K+V bytes one decode call must read: sum over active rows of L*Hkv*D*2*2."""
+    """K+V bytes one decode call must read: sum over active rows of L*Hkv*D*2*(element size)."""
     lens = inp.seq_lens.cpu().to(torch.int64)
     act = inp.active.cpu().to(torch.int64)
-    return int((lens * act).sum()) * inp.Hkv * inp.D * 2 * 2
+    return int((lens * act).sum()) * inp.Hkv * inp.D * 2 * inp.pool.element_size()
