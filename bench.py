@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
+                    help="16-bit element type of q, k, v, the cache and the output")
+    ap.add_argument("--interleaved", action="store_true",
+                    help="interleaved (2i, 2i+1) RoPE pairing instead of rotate-half")
     ap.add_argument("--qk-norm", action="store_true",
                     help="per-head RMSNorm of q and the new key before RoPE (unit weights, eps 1e-6)")
     ap.add_argument("--layers", type=int, default=None,
@@ -191,17 +195,18 @@ class Setup:
     layers in order."""
 
     def __init__(self, name: str, rank: int, dev, replicas: int | None = None, layers: int | None = None,
-                 qk_norm: bool = False):
+                 qk_norm: bool = False, dtype: str = "bf16", interleaved: bool = False):
         import paged_len_decode_gb300 as vh
         self.vh = vh
         self.L = layers or workloads.WORKLOADS[name].layers
+        et = torch.float16 if dtype == "fp16" else torch.bfloat16
         if self.L > 1:
-            self.layer_inputs = [workloads.make_inputs(name, layer=rank * self.L + l, device=dev)
+            self.layer_inputs = [workloads.make_inputs(name, layer=rank * self.L + l, device=dev, dtype=et)
                                  for l in range(self.L)]
             inp = self.layer_inputs[0]
         else:
             self.layer_inputs = None
-            inp = workloads.make_inputs(name, layer=rank, device=dev)
+            inp = workloads.make_inputs(name, layer=rank, device=dev, dtype=et)
         self.inp = inp
         self.B, self.Hq, self.Hkv, self.D, self.P = inp.B, inp.Hq, inp.Hkv, inp.D, inp.P
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -215,14 +220,14 @@ class Setup:
         self.cos_sin = torch.empty((inp.max_pages_per_seq * self.P, self.D), dtype=torch.float32, device=dev)
         vh.vh_rope_table(self.cos_sin, inp.theta)
         self.q_rot = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=dev)
-        self.out = torch.empty((self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((self.B, self.Hq, self.D), dtype=et, device=dev)
         self.ws3 = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.wsf = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.n_ctas = vh.vh_decode_num_ctas(self.B, self.Hq, self.Hkv, self.D, self.P)
-        self.norm = {}
+        self.norm = {"interleaved": interleaved}
         if qk_norm:
             w = torch.ones(self.D, dtype=torch.float32, device=dev)
-            self.norm = {"q_norm_w": w, "k_norm_w": w, "norm_eps": 1e-6}
+            self.norm.update({"q_norm_w": w, "k_norm_w": w, "norm_eps": 1e-6})
 
     def inputs(self, r):
         return self.layer_inputs[r] if self.layer_inputs else self.inp
@@ -248,7 +253,7 @@ def run_ncu_case(args):
     """A few eager launches on one pool: 3 fused, 3 three-call steps."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    s = Setup(args.workload, 0, dev, replicas=1, layers=1)
+    s = Setup(args.workload, 0, dev, replicas=1, layers=1, dtype=args.dtype, interleaved=args.interleaved)
     for _ in range(3):
         s.fused(0, pdl=False)
     for _ in range(3):
@@ -278,7 +283,7 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
         views[k] = d_arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
     d_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
         "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool")}, **views})
-    h_out = torch.empty((s.B, s.Hq, s.D), dtype=torch.bfloat16).pin_memory()
+    h_out = torch.empty((s.B, s.Hq, s.D), dtype=s.out.dtype).pin_memory()
     h2d = total
     d2h = h_out.numel() * h_out.element_size()
     K_e2e = min(args.steps, 2000)
@@ -331,7 +336,8 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
-    s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm)
+    s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm, dtype=args.dtype,
+              interleaved=args.interleaved)
     inp, R, L = s.inp, s.R, s.L
     by = s.step_bytes()
 
@@ -400,7 +406,8 @@ def run_ours(args, rank, world):
     res = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if args.dtype == "fp16" else "bf16",
         "accum_dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{args.workload}: B={s.B} (active {by['active']}), Hq={s.Hq}, Hkv={s.Hkv}, "
                                f"D={s.D}, P={s.P}, lengths {w.dist} [{w.len_lo},{w.len_hi}]",
@@ -408,16 +415,19 @@ def run_ours(args, rank, world):
                    "step": (f"{L} layer calls, " if L > 1 else "") +
                            "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
                            "PDL between launches",
-                   "layers": L, "qk_norm": bool(args.qk_norm),
+                   "layers": L, "qk_norm": bool(args.qk_norm), "rope": "interleaved" if args.interleaved
+                   else "rotate-half", "elements": args.dtype,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": (f"{L} KV pools, one per layer ({L * s.pool_bytes / 1e9:.1f} GB)" if L > 1 else
                           f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB")
                          + f" >= 4x L2 {s.l2 / 1e6:.0f} MB): inputs larger than L2",
                    "ctas": s.n_ctas},
         "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": f"decode_attn_kernel<{s.D},{s.Hq // s.Hkv},1> (fused step)",
+        "roofline": {"bound": "hbm", "kernel": f"decode_attn_kernel<{s.D},{s.Hq // s.Hkv},1,"
+                               f"{'ElemF16' if args.dtype == 'fp16' else 'ElemBf16'}> (fused step)",
                      "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(step_gbs / peak, 4), "traffic": recorded_traffic(args.workload),
+                     "frac": round(step_gbs / peak, 4), "traffic": (recorded_traffic(args.workload)
+                                                    if args.dtype == "bf16" and not args.interleaved else None),
                      "peak_kind": peak_kind, "ms_per_launch": round(ms_step / L, 6),
                      "algorithmic_bytes_per_launch": by["step"] // L},
         "three_call": {"ms_per_step": round(ms_three, 6),

@@ -32,7 +32,10 @@
  *   - All pointers are DEVICE pointers owned by the caller; the library
  *     allocates nothing, frees nothing and keeps no state between calls
  *     other than per-device launch settings it caches on first use.
- *   - bf16 values are passed as uint16_t bit patterns (vh_bf16).
+ *   - 16-bit values are passed as uint16_t bit patterns: vh_bf16 is always
+ *     bf16; vh_e16 is bf16, or IEEE fp16 when the call's flags hold
+ *     VH_FLAG_FP16 (the Fish kernel of the first source below takes either
+ *     type).  One call uses one type for all of its 16-bit arrays.
  *   - Strides are in ELEMENTS.  One layer's cache is reached through
  *     k_cache / v_cache plus page_stride (elements between pages) and
  *     token_stride (elements between token slots of a page); within a slot
@@ -69,7 +72,8 @@
 extern "C" {
 #endif
 
-typedef uint16_t vh_bf16;
+typedef uint16_t vh_bf16;  /* a bf16 bit pattern */
+typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16 */
 
 /* return codes */
 #define VH_OK 0
@@ -86,8 +90,10 @@ typedef uint16_t vh_bf16;
 #define VH_ERR_POS 4        /* position outside [0, max_pos): the row is skipped by the append */
 #define VH_ERR_TIMEOUT 8    /* an internal pipeline wait ran out of time: the CTA gave up */
 
-/* launch flags of vh_decode_fused */
-#define VH_FLAG_PDL 1u      /* programmatic dependent launch, see vh_decode_fused */
+/* flags (the `flags` argument of the calls that take one) */
+#define VH_FLAG_PDL 1u      /* programmatic dependent launch, see vh_decode_fused (that call only) */
+#define VH_FLAG_FP16 2u     /* 16-bit elements (q, k_new, v_new, cache, out) are IEEE fp16, not bf16 */
+#define VH_FLAG_ROPE_INTERLEAVED 4u /* RoPE pairs elements (2i, 2i+1) instead of (i, i + D/2) */
 
 /* Fill the RoPE table used by vh_rope_kv_append.
  * cos_sin: float [max_pos][D]; row p holds cos(p * f_i) in columns 0..D/2-1
@@ -99,9 +105,9 @@ typedef uint16_t vh_bf16;
 int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void* stream);
 
 /* RoPE + KV append, one CTA per row.
- * q      bf16 [B][Hq][D]   new queries (contiguous)
- * k_new  bf16 [B][Hkv][D]  new keys, rotated here before they are stored
- * v_new  bf16 [B][Hkv][D]  new values, stored bit for bit
+ * q      e16 [B][Hq][D]   new queries (contiguous)
+ * k_new  e16 [B][Hkv][D]  new keys, rotated here before they are stored
+ * v_new  e16 [B][Hkv][D]  new values, stored bit for bit
  * cos_sin float [max_pos][D] from vh_rope_table
  * positions int32 [B] or NULL; NULL means position = seq_lens[b] - 1
  * q_norm_w, k_norm_w float [D] or NULL: per-head RMSNorm applied to every q
@@ -114,22 +120,25 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
  * q_rot  float [B][Hq][D] out: rotated q in fp32 (rows with active == 0
  *        are not written)
  * err_flag int32* or NULL
+ * flags  0 or VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED
  * For every active row: q_rot = rope(q); the cache slot of token
- * seq_len-1 receives bf16_rne(rope(k_new)) and v_new.  Rotation is computed
- * in fp32 ("rotate half": element i pairs with i + D/2).  Rows with
+ * seq_len-1 receives rne(rope(k_new)) (rounded to nearest even in the
+ * element type) and v_new.  Rotation is computed in fp32; pair i, at angle
+ * pos * theta^(-2i/D), is (i, i + D/2) ("rotate half"), or (2i, 2i + 1)
+ * with VH_FLAG_ROPE_INTERLEAVED (the GPT-J pairing).  Rows with
  * active == 0 write nothing.  Precondition (not checked): live rows own
  * disjoint append slots.
  * Errors: VH_EINVAL (NULL pointer other than positions/err_flag, bad shape,
- * max_pos < 1, num_pages < 1, max_pages_per_seq < 1), VH_EALIGN (a pointer
- * or a stride not 16-byte aligned), VH_ECUDA. */
-int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+ * max_pos < 1, num_pages < 1, max_pages_per_seq < 1, unknown flags),
+ * VH_EALIGN (a pointer or a stride not 16-byte aligned), VH_ECUDA. */
+int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                       const float* cos_sin, int max_pos, const int32_t* positions,
                       const float* q_norm_w, const float* k_norm_w, float norm_eps,
-                      vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride,
+                      vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride,
                       int64_t token_stride, int num_pages,
                       const int32_t* page_table, int max_pages_per_seq,
                       const int32_t* seq_lens, const int32_t* active,
-                      float* q_rot, int32_t* err_flag,
+                      float* q_rot, int32_t* err_flag, unsigned flags,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
 /* Number of CTAs per kv-head group that vh_paged_decode_attn launches on the
@@ -144,7 +153,7 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
 
 /* Paged GQA decode attention.
  * q_rot float [B][Hq][D] (from vh_rope_kv_append); cache as above.
- * out bf16 [B][Hq][D]: rows whose keys one CTA covered entirely are written
+ * out e16 [B][Hq][D]: rows whose keys one CTA covered entirely are written
  *     here directly; rows with active == 0 (or flagged VH_ERR_SEQLEN) are
  *     written as zeros; rows split across CTAs are finished by
  *     vh_decode_combine.
@@ -158,25 +167,29 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
  *     per-row split plan and the fp32 partial results.  No initialisation
  *     is needed.  Calls that overlap on the device must use distinct
  *     workspaces.
+ * flags: 0 or VH_FLAG_FP16 (cache and out are fp16).
  * Softmax in fp32 with a running max, exp2 with log2(e) folded into the
- * scale; keys beyond seq_len (tail of the last page) are never used.
- * Errors: VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
-int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
+ * scale; keys beyond seq_len (tail of the last page) are never used.  With
+ * fp16, q_rot is split into an fp16 high part and residual for the tensor
+ * cores, so its elements must lie within the fp16 range (|x| <= 65504).
+ * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
+int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16* v_cache,
                          int64_t page_stride, int64_t token_stride, int num_pages,
                          const int32_t* page_table, int max_pages_per_seq,
                          const int32_t* seq_lens, const int32_t* active,
-                         vh_bf16* out, float sm_scale, int num_ctas,
-                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                         vh_e16* out, float sm_scale, int num_ctas,
+                         void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                          int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
-/* Merge the partial results of split rows into out (bf16 [B][Hq][D]):
+/* Merge the partial results of split rows into out (e16 [B][Hq][D]; flags 0 or
+ * VH_FLAG_FP16, as given to vh_paged_decode_attn):
  * M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s (lse in
  * base 2).  Rows that were not split are left as vh_paged_decode_attn wrote
  * them.  Must run after vh_paged_decode_attn on the same stream with the same
  * workspace and the same shape / num_ctas arguments.
- * Errors: VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
-int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
-                      int B, int Hq, int Hkv, int D, int page_size, void* stream);
+ * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
+int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out, int num_ctas,
+                      unsigned flags, int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
 /* The whole decode step of one layer in ONE launch: optional per-head RMSNorm
  * and RoPE of q and of the new key, append of the new key/value into the
@@ -193,8 +206,9 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
  *   - the new token's key is rotated and used by the CTA that owns the row's
  *     last tile, which also writes it (and v) to the cache slot; no other CTA
  *     reads that slot, so there is no ordering hazard inside the launch;
- *   - flags: 0, or VH_FLAG_PDL to launch as a programmatic dependent of the
- *     previous kernel on the stream, so that this launch's start-up (reading
+ *   - flags: VH_FLAG_FP16 and VH_FLAG_ROPE_INTERLEAVED as for
+ *     vh_rope_kv_append, and VH_FLAG_PDL to launch as a programmatic
+ *     dependent of the previous kernel on the stream, so that this launch's start-up (reading
  *     seq_lens, active, positions and page_table, planning the split)
  *     overlaps the end of that kernel.  Only valid when the kernel launched
  *     immediately before on the same stream does not write seq_lens, active,
@@ -203,13 +217,13 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
  *     kernel itself always lets a following dependent launch start early.
  * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,
  * VH_ENODEV, VH_ECUDA. */
-int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     const float* cos_sin, int max_pos, const int32_t* positions,
                     const float* q_norm_w, const float* k_norm_w, float norm_eps,
-                    vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride, int64_t token_stride,
+                    vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride, int64_t token_stride,
                     int num_pages, const int32_t* page_table, int max_pages_per_seq,
                     const int32_t* seq_lens, const int32_t* active,
-                    vh_bf16* out, float sm_scale, int num_ctas,
+                    vh_e16* out, float sm_scale, int num_ctas,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                     int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
@@ -219,7 +233,8 @@ int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new
  * hands out preallocated arenas, a plug-in inside a host process that owns
  * the CUDA context, a measurement that must not change the memory footprint).
  * Same arguments and result as vh_paged_decode_attn followed by
- * vh_decode_combine, except that there is no workspace: the split-K partial
+ * vh_decode_combine with flags 0 (bf16 cache and output), except that there
+ * is no workspace: the split-K partial
  * results go into one fixed array of VH_STATIC_SCRATCH_BYTES (8 MiB) compiled
  * into the library, which every GPU that loads the library keeps until the
  * process exits.  The call itself allocates and frees nothing.

@@ -6,6 +6,10 @@ dtypes, contiguity and devices, reads shapes and strides, and passes raw
 pointers plus the current torch stream.  There is no fallback: if the
 library is missing or a call fails, an exception is raised.
 
+The 16-bit element type (bf16 or fp16) is the cache's dtype; q, k_new,
+v_new and out must have the same dtype, and VH_FLAG_FP16 is passed for fp16.
+`interleaved=True` selects the (2i, 2i+1) RoPE pairing.
+
 Functions mirror the C entry points by name:
     vh_rope_table, vh_rope_kv_append, vh_decode_num_ctas,
     vh_decode_workspace_bytes, vh_paged_decode_attn, vh_decode_combine,
@@ -27,7 +31,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
 VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3, -4, -5
 VH_ESCRATCH = -6
 VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
-VH_FLAG_PDL = 1
+VH_FLAG_PDL, VH_FLAG_FP16, VH_FLAG_ROPE_INTERLEAVED = 1, 2, 4
+ELEM_DTYPES = (torch.bfloat16, torch.float16)
 
 
 class VHError(RuntimeError):
@@ -46,17 +51,18 @@ def _load() -> ctypes.CDLL:
     lib.vh_status_string.restype = ctypes.c_char_p
     lib.vh_rope_table.argtypes = [P, I, I, D, P]
     lib.vh_rope_table.restype = I
-    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I, P, I, P, P, P, P,
+    U = ctypes.c_uint
+    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I, P, I, P, P, P, P, U,
                                       I, I, I, I, I, P]
     lib.vh_rope_kv_append.restype = I
     lib.vh_decode_num_ctas.argtypes = [I, I, I, I, I]
     lib.vh_decode_num_ctas.restype = I
     lib.vh_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.vh_decode_workspace_bytes.restype = SZ
-    lib.vh_paged_decode_attn.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P,
+    lib.vh_paged_decode_attn.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P, U,
                                          I, I, I, I, I, P]
     lib.vh_paged_decode_attn.restype = I
-    lib.vh_decode_combine.argtypes = [P, SZ, P, I, I, I, I, I, I, P]
+    lib.vh_decode_combine.argtypes = [P, SZ, P, I, U, I, I, I, I, I, P]
     lib.vh_decode_combine.restype = I
     lib.vh_paged_decode_attn_noalloc.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P,
                                                  I, I, I, I, I, P]
@@ -107,15 +113,21 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _cache_view(k_cache: torch.Tensor, v_cache: torch.Tensor):
+def _cache_view(k_cache: torch.Tensor, v_cache: torch.Tensor, bf16_only: bool = False):
     """Pointers and element strides of a [NP, P, Hkv, D] paged cache view."""
     if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
         raise ValueError("k_cache / v_cache must be [NP, P, Hkv, D] views with equal strides")
     if k_cache.stride(3) != 1 or k_cache.stride(2) != k_cache.shape[3]:
         raise ValueError("the heads of one token slot must be contiguous ([.., Hkv, D] dense)")
+    if k_cache.dtype not in (ELEM_DTYPES[:1] if bf16_only else ELEM_DTYPES):
+        raise TypeError(f"k_cache must be bfloat16{'' if bf16_only else ' or float16'}, got {k_cache.dtype}")
     NP, P, Hkv, D = k_cache.shape
-    return (_ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+    return (_ptr(k_cache, k_cache.dtype, "k_cache"), _ptr(v_cache, k_cache.dtype, "v_cache"),
             k_cache.stride(0), k_cache.stride(1), NP, P, Hkv, D)
+
+
+def _elem_flags(k_cache: torch.Tensor, interleaved: bool = False) -> int:
+    return (VH_FLAG_FP16 if k_cache.dtype == torch.float16 else 0) | (VH_FLAG_ROPE_INTERLEAVED if interleaved else 0)
 
 
 def vh_rope_table(cos_sin: torch.Tensor, theta: float = 10000.0, stream=None) -> torch.Tensor:
@@ -136,21 +148,22 @@ def _norm_w(t, D, name):
 
 def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
                       q_rot, positions=None, err_flag=None, q_norm_w=None, k_norm_w=None,
-                      norm_eps: float = 1e-6, stream=None) -> None:
+                      norm_eps: float = 1e-6, interleaved: bool = False, stream=None) -> None:
     B, Hq, D = q.shape
     kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    et = k_cache.dtype
     if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or q_rot.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q, k_new, v_new, q_rot and the cache")
     _check(lib.vh_rope_kv_append(
-        _contig(q, torch.bfloat16, "q"), _contig(k_new, torch.bfloat16, "k_new"),
-        _contig(v_new, torch.bfloat16, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
+        _contig(q, et, "q"), _contig(k_new, et, "k_new"),
+        _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
         kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(q_rot, torch.float32, "q_rot"),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        B, Hq, Hkv, D, P, _stream(stream)), "vh_rope_kv_append")
+        _elem_flags(k_cache, interleaved), B, Hq, Hkv, D, P, _stream(stream)), "vh_rope_kv_append")
 
 
 def vh_decode_num_ctas(B: int, Hq: int, Hkv: int, D: int, page_size: int) -> int:
@@ -177,18 +190,21 @@ def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, 
         _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, NP,
         _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
-        _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
+        _contig(out, k_cache.dtype, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn")
+        _elem_flags(k_cache), B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn")
 
 
 def vh_decode_combine(workspace, out, Hkv: int, page_size: int, num_ctas: int = 0, stream=None) -> None:
+    """Merge split rows into out (bf16 or fp16: the type vh_paged_decode_attn wrote)."""
     B, Hq, D = out.shape
+    if out.dtype not in ELEM_DTYPES:
+        raise TypeError(f"out must be bfloat16 or float16, got {out.dtype}")
     _check(lib.vh_decode_combine(
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
-        _contig(out, torch.bfloat16, "out"), int(num_ctas), B, Hq, Hkv, D, page_size,
-        _stream(stream)), "vh_decode_combine")
+        _contig(out, out.dtype, "out"), int(num_ctas), VH_FLAG_FP16 if out.dtype == torch.float16 else 0,
+        B, Hq, Hkv, D, page_size, _stream(stream)), "vh_decode_combine")
 
 
 def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, active, out,
@@ -197,7 +213,7 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
     """Attention plus combine into `out` with the library's fixed scratch array,
     for callers that cannot allocate a workspace (see include/vh.h)."""
     B, Hq, D = q_rot.shape
-    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache, bf16_only=True)
     if Dc != D or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q_rot, out and the cache")
     _check(lib.vh_paged_decode_attn_noalloc(
@@ -212,25 +228,27 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
 def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, out,
                     workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
                     pdl: bool = False, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
-                    stream=None) -> torch.Tensor:
+                    interleaved: bool = False, stream=None) -> torch.Tensor:
     """One whole decode step in one launch (RoPE, append, attention, merge).
     `workspace` must be zero-filled before its first use (alloc_workspace does that).
     pdl=True sets VH_FLAG_PDL (see include/vh.h for when that is allowed)."""
     B, Hq, D = q.shape
     kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    et = k_cache.dtype
     if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q, k_new, v_new, out and the cache")
     _check(lib.vh_decode_fused(
-        _contig(q, torch.bfloat16, "q"), _contig(k_new, torch.bfloat16, "k_new"),
-        _contig(v_new, torch.bfloat16, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
+        _contig(q, et, "q"), _contig(k_new, et, "k_new"),
+        _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
         kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
-        _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
+        _contig(out, et, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        VH_FLAG_PDL if pdl else 0, B, Hq, Hkv, D, P, _stream(stream)), "vh_decode_fused")
+        (VH_FLAG_PDL if pdl else 0) | _elem_flags(k_cache, interleaved), B, Hq, Hkv, D, P,
+        _stream(stream)), "vh_decode_fused")
     return out
 
 
@@ -244,11 +262,11 @@ def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas:
 def decode_step(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, q_rot,
                 out, workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0,
                 err_flag=None, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
-                stream=None) -> torch.Tensor:
+                interleaved: bool = False, stream=None) -> torch.Tensor:
     """One decode step of one layer: (RMSNorm +) RoPE + append, attention, combine."""
     vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
                       q_rot, positions=positions, err_flag=err_flag, q_norm_w=q_norm_w,
-                      k_norm_w=k_norm_w, norm_eps=norm_eps, stream=stream)
+                      k_norm_w=k_norm_w, norm_eps=norm_eps, interleaved=interleaved, stream=stream)
     vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
                          sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, stream=stream)
     vh_decode_combine(workspace, out, k_cache.shape[2], k_cache.shape[1], num_ctas=num_ctas,

@@ -30,11 +30,12 @@
 //    tile and the G q heads of the kv head padded to 8, the scores are one
 //    m16n8 tile: S^T (keys x heads) = K (keys x D) . q^T, and the output is
 //    O^T (D x heads) += V^T (D x keys) . P^T (keys x heads), both as
-//    mma.sync m16n8k16 with bf16 operands and fp32 accumulation.  q and p are
-//    fp32 values: each is split into a bf16 high part and a bf16 residual
-//    (x = hi + lo to 2^-16 relative) and both parts are multiplied, so the
-//    products keep about 16 significant bits while K and V (bf16 already)
-//    enter exactly.  P goes from the score-fragment layout to the operand
+//    mma.sync m16n8k16 with operands of the cache's element type (bf16 or
+//    fp16) and fp32 accumulation.  q and p are fp32 values: each is split
+//    into a high part and a residual of that type (x = hi + lo to 2^-16
+//    relative for bf16, 2^-22 for fp16) and both parts are multiplied, so
+//    the products keep at least 16 significant bits while K and V enter
+//    exactly.  P goes from the score-fragment layout to the operand
 //    layout with movmatrix transposes.  K and V rows get a 16-byte pad so
 //    ldmatrix reads are free of bank conflicts.
 //  * Stale slots (tail of the last page, slots never copied) never reach the
@@ -101,7 +102,7 @@ enum { kMiscWarpTot = 0, kMiscAbort = 32, kMiscNVerdict = 33, kMiscVerdict = 34,
 // with M the running max, so each batch of U pieces costs one round trip: its
 // lse and o loads are all issued before any is used (they bypass L1: other
 // CTAs wrote them during this launch).
-template <int D, int G>
+template <int D, int G, typename E>
 __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse, const float* __restrict__ part_o,
                                              long long slot_base /* (gy * N) * 2 */, int HG, int wg /* w * G */,
                                              int cf, int np, int first_slot, uint16_t* __restrict__ out_row,
@@ -168,14 +169,14 @@ __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse,
     uint16_t* dst = out_row + static_cast<long long>(n) * D + lane * PER;
     if constexpr (PER == 4) {
       *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16x2(o[n][0] * iw, o[n][1] * iw), pack_bf16x2(o[n][2] * iw, o[n][3] * iw));
+          make_uint2(E::pack2(o[n][0] * iw, o[n][1] * iw), E::pack2(o[n][2] * iw, o[n][3] * iw));
     } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[n][0] * iw, o[n][1] * iw);
+      *reinterpret_cast<uint32_t*>(dst) = E::pack2(o[n][0] * iw, o[n][1] * iw);
     }
   }
 }
 
-template <int D, int G, bool FUSED>
+template <int D, int G, bool FUSED, typename E>
 __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnParams p) {
   constexpr int KSTEPS = D / 16;  // k-steps of the score product = m-tiles of the value product
   extern __shared__ __align__(128) unsigned char smem[];
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         page = 0;
       }
       if (new_seg) {
-        // q rows of this segment's row (fused: bf16 q and the RoPE row of its
+        // q rows of this segment's row (fused: 16-bit q and the RoPE row of its
         // position) into the staging buffer, once the consumers have taken
         // the previous segment's q into registers.
         if (nseg > 0 && !mbar_wait(qempty, (nseg - 1) & 1)) {
@@ -471,23 +472,34 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
   float wq[4] = {1.f, 1.f, 1.f, 1.f}, wk[2 * KPAIRS];
 #pragma unroll
   for (int j = 0; j < 2 * KPAIRS; ++j) wk[j] = 1.f;
+  // weights in the order (x0, x1, y0, y1) of the rotation pairs (x, y): pair i is
+  // (i, i + D/2), or (2i, 2i + 1) with interleaved RoPE
+  const bool ilv = p.rope_interleaved != 0;
   if constexpr (FUSED) {
     const int iq = 2 * (lane % NQU);
     if (p.q_norm_w) {
-      const float2 a = *reinterpret_cast<const float2*>(p.q_norm_w + iq);
-      const float2 c2 = *reinterpret_cast<const float2*>(p.q_norm_w + D / 2 + iq);
-      wq[0] = a.x;
-      wq[1] = a.y;
-      wq[2] = c2.x;
-      wq[3] = c2.y;
+      if (ilv) {
+        const float4 a = *reinterpret_cast<const float4*>(p.q_norm_w + 2 * iq);
+        wq[0] = a.x;
+        wq[1] = a.z;
+        wq[2] = a.y;
+        wq[3] = a.w;
+      } else {
+        const float2 a = *reinterpret_cast<const float2*>(p.q_norm_w + iq);
+        const float2 c2 = *reinterpret_cast<const float2*>(p.q_norm_w + D / 2 + iq);
+        wq[0] = a.x;
+        wq[1] = a.y;
+        wq[2] = c2.x;
+        wq[3] = c2.y;
+      }
     }
     if (p.k_norm_w) {
 #pragma unroll
       for (int j = 0; j < KPAIRS; ++j) {
         const int i = lane + 32 * j;
         if (i < D / 2) {
-          wk[2 * j] = p.k_norm_w[i];
-          wk[2 * j + 1] = p.k_norm_w[i + D / 2];
+          wk[2 * j] = p.k_norm_w[ilv ? 2 * i : i];
+          wk[2 * j + 1] = p.k_norm_w[ilv ? 2 * i + 1 : i + D / 2];
         }
       }
     }
@@ -525,9 +537,10 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       }
       const unsigned char* qb = smem + p.q_off;
       const float* cs = reinterpret_cast<const float*>(qb + HG * p.q_row_bytes);  // fused: RoPE row
-      // fused: (1) all 32 lanes rotate this warp's G q rows (rotate-half RoPE in
-      // fp32, pairs (i, i + D/2)) into padded per-warp fp32 rows (D*4 + 32 bytes)
-      // so that (2) every lane reads its operand pairs without bank conflicts.
+      // fused: (1) all 32 lanes rotate this warp's G q rows (RoPE in fp32, pairs
+      // (i, i + D/2), or (2i, 2i + 1) interleaved) into padded per-warp fp32 rows
+      // (D*4 + 32 bytes) so that (2) every lane reads its operand pairs without
+      // bank conflicts.
       // Three-call path: the staged rows are fp32 already and are read directly.
       constexpr int QS_ROW = D * 4 + 32;
       const unsigned char* qsrc;
@@ -541,10 +554,18 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
           const int n = valid ? e / NQU : 0;
           const int i = (e % NQU) * 2;  // i, i+1 in [0, D/2)
           const unsigned char* row = qb + (w * G + n) * p.q_row_bytes;
+          // xv: first elements of pairs i and i + 1, yv: their partners
           float2 xv = make_float2(0.f, 0.f), yv = make_float2(0.f, 0.f);
           if (valid) {
-            xv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * i));
-            yv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * (i + D / 2)));
+            if (ilv) {
+              const uint2 w2 = *reinterpret_cast<const uint2*>(row + 4 * i);  // elements 2i .. 2i+3
+              const float2 a = E::to_float2(w2.x), c2 = E::to_float2(w2.y);
+              xv = make_float2(a.x, c2.x);
+              yv = make_float2(a.y, c2.y);
+            } else {
+              xv = E::to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * i));
+              yv = E::to_float2(*reinterpret_cast<const uint32_t*>(row + 2 * (i + D / 2)));
+            }
           }
           if (p.q_norm_w) {
             // RMSNorm in fp32: the NQU lanes of a head hold its D elements
@@ -559,9 +580,14 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
             const float2 cv = *reinterpret_cast<const float2*>(cs + i);
             const float2 sv = *reinterpret_cast<const float2*>(cs + D / 2 + i);
             float* dst = reinterpret_cast<float*>(qs + n * QS_ROW);
-            *reinterpret_cast<float2*>(dst + i) = make_float2(xv.x * cv.x - yv.x * sv.x, xv.y * cv.y - yv.y * sv.y);
-            *reinterpret_cast<float2*>(dst + i + D / 2) =
-                make_float2(yv.x * cv.x + xv.x * sv.x, yv.y * cv.y + xv.y * sv.y);
+            const float2 rx = make_float2(xv.x * cv.x - yv.x * sv.x, xv.y * cv.y - yv.y * sv.y);
+            const float2 ry = make_float2(yv.x * cv.x + xv.x * sv.x, yv.y * cv.y + xv.y * sv.y);
+            if (ilv) {
+              *reinterpret_cast<float4*>(dst + 2 * i) = make_float4(rx.x, ry.x, rx.y, ry.y);
+            } else {
+              *reinterpret_cast<float2*>(dst + i) = rx;
+              *reinterpret_cast<float2*>(dst + i + D / 2) = ry;
+            }
           }
         }
         __syncwarp();
@@ -581,8 +607,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
           a = *reinterpret_cast<const float2*>(qrow + 16 * k + 2 * t4);
           c2 = *reinterpret_cast<const float2*>(qrow + 16 * k + 2 * t4 + 8);
         }
-        split_bf16x2(a.x, a.y, qh[k][0], ql[k][0]);
-        split_bf16x2(c2.x, c2.y, qh[k][1], ql[k][1]);
+        split2<E>(a.x, a.y, qh[k][0], ql[k][0]);
+        split2<E>(c2.x, c2.y, qh[k][1], ql[k][1]);
       }
       if constexpr (FUSED) {
 #pragma unroll
@@ -622,8 +648,17 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
 #pragma unroll
         for (int j = 0; j < KPAIRS; ++j) {
           const int i = lane + 32 * j;
-          kx[j] = i < D / 2 ? __uint_as_float(static_cast<uint32_t>(kr[i]) << 16) : 0.f;
-          ky[j] = i < D / 2 ? __uint_as_float(static_cast<uint32_t>(kr[i + D / 2]) << 16) : 0.f;
+          kx[j] = ky[j] = 0.f;
+          if (i < D / 2) {
+            if (ilv) {
+              const float2 xy = E::to_float2(*reinterpret_cast<const uint32_t*>(kr + 2 * i));
+              kx[j] = xy.x;
+              ky[j] = xy.y;
+            } else {
+              kx[j] = E::to_float(kr[i]);
+              ky[j] = E::to_float(kr[i + D / 2]);
+            }
+          }
           ss += kx[j] * kx[j] + ky[j] * ky[j];
         }
         if (p.k_norm_w) {
@@ -643,13 +678,20 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
           const int i = lane + 32 * j;
           if (i < D / 2) {
             const float x = kx[j], y = ky[j];
-            const uint16_t xr = static_cast<uint16_t>(float_to_bf16_bits(x * rc[j] - y * rs[j]));
-            const uint16_t yr = static_cast<uint16_t>(float_to_bf16_bits(y * rc[j] + x * rs[j]));
-            kr[i] = xr;
-            kr[i + D / 2] = yr;
-            if (dst >= 0) {
-              p.k_cache_w[dst + static_cast<long long>(w) * D + i] = xr;
-              p.k_cache_w[dst + static_cast<long long>(w) * D + i + D / 2] = yr;
+            const float xr = x * rc[j] - y * rs[j], yr = y * rc[j] + x * rs[j];
+            uint16_t* cache_row = p.k_cache_w + dst + static_cast<long long>(w) * D;
+            if (ilv) {
+              const uint32_t xy = E::pack2(xr, yr);
+              *reinterpret_cast<uint32_t*>(kr + 2 * i) = xy;
+              if (dst >= 0) *reinterpret_cast<uint32_t*>(cache_row + 2 * i) = xy;
+            } else {
+              const uint16_t xb = E::bits(xr), yb = E::bits(yr);
+              kr[i] = xb;
+              kr[i + D / 2] = yb;
+              if (dst >= 0) {
+                cache_row[i] = xb;
+                cache_row[i + D / 2] = yb;
+              }
             }
           }
         }
@@ -677,8 +719,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       for (int k = 0; k < KSTEPS; ++k) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(ka + 32 * k, a0, a1, a2, a3);
-        mma_bf16(sh, a0, a1, a2, a3, qh[k][0], qh[k][1]);
-        mma_bf16(sl, a0, a1, a2, a3, ql[k][0], ql[k][1]);
+        E::mma(sh, a0, a1, a2, a3, qh[k][0], qh[k][1]);
+        E::mma(sl, a0, a1, a2, a3, ql[k][0], ql[k][1]);
       }
     }
     // lane holds keys g4 (s[0], s[1]) and g4 + 8 (s[2], s[3]), heads 2 t4 and 2 t4 + 1
@@ -704,8 +746,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
     m0 = mn0;
     m1 = mn1;
     uint32_t ph01, pl01, ph23, pl23;
-    split_bf16x2(p0, p1, ph01, pl01);
-    split_bf16x2(p2, p3, ph23, pl23);
+    split2<E>(p0, p1, ph01, pl01);
+    split2<E>(p2, p3, ph23, pl23);
     const uint32_t bh0 = movm_t(ph01), bh1 = movm_t(ph23);
     const uint32_t bl0 = movm_t(pl01), bl1 = movm_t(pl23);
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
@@ -725,8 +767,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       for (int mt = 0; mt < KSTEPS; ++mt) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(vaddr + 32 * mt, a0, a1, a2, a3);
-        mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
-        mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+        E::mma(acc[mt], a0, a1, a2, a3, bh0, bh1);
+        E::mma(acc[mt], a0, a1, a2, a3, bl0, bl1);
       }
     }
     if (touched) fence_proxy_async_smem();  // generic writes before the next bulk copy into this stage
@@ -755,12 +797,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         for (int mt = 0; mt < KSTEPS; ++mt) {
           const int d = mt * 16 + g4;
           if (n0 < G) {
-            o0[d] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][0] * il0));
-            o0[d + 8] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][2] * il0));
+            o0[d] = E::bits(acc[mt][0] * il0);
+            o0[d + 8] = E::bits(acc[mt][2] * il0);
           }
           if (n1 < G) {
-            o1[d] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][1] * il1));
-            o1[d + 8] = static_cast<uint16_t>(float_to_bf16_bits(acc[mt][3] * il1));
+            o1[d] = E::bits(acc[mt][1] * il1);
+            o1[d + 8] = E::bits(acc[mt][3] * il1);
           }
         }
       } else {
@@ -803,7 +845,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       for (int k = 0; k < nv; ++k) {
         const int* v = misc + kMiscVerdict + 5 * k;
         if (!v[0]) continue;
-        merge_pieces<D, G>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, v[2],
+        merge_pieces<D, G, E>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, v[2],
                            v[3] - v[2] + 1, v[4],
                            p.out + (static_cast<long long>(v[1]) * p.Hq + static_cast<long long>(h) * G) * D, lane);
       }
@@ -814,7 +856,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
 // Three-call path: one CTA per (row, kv-head group), one warp per kv head of
 // the group (its G q heads).  Rows that one CTA finished, and padding rows,
 // return at once.
-template <int D, int G>
+template <int D, int G, typename E>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineParams p) {
   pdl_wait();  // launched as a dependent of the attention kernel
   const int b = blockIdx.x, gy = blockIdx.y;
@@ -822,57 +864,63 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineParams
   if (pl.x < 0 || pl.x == pl.y) return;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int HG = p.Hc * G;
-  merge_pieces<D, G>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, pl.x, pl.y - pl.x + 1,
+  merge_pieces<D, G, E>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, pl.x, pl.y - pl.x + 1,
                      pl.z, p.out + (static_cast<long long>(b) * p.Hq + static_cast<long long>(gy) * HG + w * G) * D,
                      lane);
 }
 
-template <int D, int G>
+template <int D, int G, typename E>
 const void* attn_kernel_ptr(bool fused) {
-  return fused ? reinterpret_cast<const void*>(&decode_attn_kernel<D, G, true>)
-               : reinterpret_cast<const void*>(&decode_attn_kernel<D, G, false>);
+  return fused ? reinterpret_cast<const void*>(&decode_attn_kernel<D, G, true, E>)
+               : reinterpret_cast<const void*>(&decode_attn_kernel<D, G, false, E>);
 }
 
-const void* select_attn_kernel(int D, int G, bool fused) {
+template <typename E>
+const void* select_attn_kernel_t(int D, int G, bool fused) {
   if (D == 128) {
     switch (G) {
-      case 1: return attn_kernel_ptr<128, 1>(fused);
-      case 2: return attn_kernel_ptr<128, 2>(fused);
-      case 4: return attn_kernel_ptr<128, 4>(fused);
-      case 8: return attn_kernel_ptr<128, 8>(fused);
+      case 1: return attn_kernel_ptr<128, 1, E>(fused);
+      case 2: return attn_kernel_ptr<128, 2, E>(fused);
+      case 4: return attn_kernel_ptr<128, 4, E>(fused);
+      case 8: return attn_kernel_ptr<128, 8, E>(fused);
     }
   } else if (D == 64) {
     switch (G) {
-      case 1: return attn_kernel_ptr<64, 1>(fused);
-      case 2: return attn_kernel_ptr<64, 2>(fused);
-      case 4: return attn_kernel_ptr<64, 4>(fused);
-      case 8: return attn_kernel_ptr<64, 8>(fused);
+      case 1: return attn_kernel_ptr<64, 1, E>(fused);
+      case 2: return attn_kernel_ptr<64, 2, E>(fused);
+      case 4: return attn_kernel_ptr<64, 4, E>(fused);
+      case 8: return attn_kernel_ptr<64, 8, E>(fused);
     }
   }
   return nullptr;
 }
 
+const void* select_attn_kernel(int D, int G, bool fused, bool f16) {
+  return f16 ? select_attn_kernel_t<ElemF16>(D, G, fused) : select_attn_kernel_t<ElemBf16>(D, G, fused);
+}
+
 }  // namespace
 
 cudaError_t prepare_decode_attn(int D, int G, int max_smem) {
-  for (bool fused : {false, true}) {
-    const void* k = select_attn_kernel(D, G, fused);
-    if (!k) return cudaErrorInvalidValue;
-    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) return e;
-  }
+  for (bool f16 : {false, true})
+    for (bool fused : {false, true}) {
+      const void* k = select_attn_kernel(D, G, fused, f16);
+      if (!k) return cudaErrorInvalidValue;
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
 cudaError_t decode_attn_occupancy(const AttnParams& p, int* blocks_per_sm) {
-  const void* k = select_attn_kernel(p.D, p.G, p.fused != 0);
+  const void* k = select_attn_kernel(p.D, p.G, p.fused != 0, p.f16 != 0);
   if (!k) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, 32 * (p.Hc + (p.fused ? 2 : 1)),
                                                        p.smem_bytes);
 }
 
 cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pdl) {
-  const void* k = select_attn_kernel(p.D, p.G, p.fused != 0);
+  const void* k = select_attn_kernel(p.D, p.G, p.fused != 0, p.f16 != 0);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.N, p.groups);
@@ -899,8 +947,10 @@ cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-#define VH_COMBINE_CASE(DD, GG) \
-  if (p.D == DD && p.G == GG) return cudaLaunchKernelEx(&cfg, decode_combine_kernel<DD, GG>, p);
+#define VH_COMBINE_CASE(DD, GG)                                                                             \
+  if (p.D == DD && p.G == GG)                                                                               \
+    return p.f16 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<DD, GG, ElemF16>, p)                      \
+                 : cudaLaunchKernelEx(&cfg, decode_combine_kernel<DD, GG, ElemBf16>, p);
   VH_COMBINE_CASE(128, 1)
   VH_COMBINE_CASE(128, 2)
   VH_COMBINE_CASE(128, 4)

@@ -204,17 +204,17 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
              : VH_ECUDA;
 }
 
-int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                       const float* cos_sin, int max_pos, const int32_t* positions,
                       const float* q_norm_w, const float* k_norm_w, float norm_eps,
-                      vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride,
+                      vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride,
                       int64_t token_stride, int num_pages,
                       const int32_t* page_table, int max_pages_per_seq,
                       const int32_t* seq_lens, const int32_t* active,
-                      float* q_rot, int32_t* err_flag,
+                      float* q_rot, int32_t* err_flag, unsigned flags,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream) {
   if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !page_table || !seq_lens || !active ||
-      !q_rot)
+      !q_rot || (flags & ~(VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0)
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
       page_stride < 1 || token_stride < 1 || too_many_tiles(B, max_pages_per_seq, page_size))
@@ -229,6 +229,8 @@ int vh_rope_kv_append(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_n
   p.q_norm_w = q_norm_w;
   p.k_norm_w = k_norm_w;
   p.norm_eps = norm_eps;
+  p.rope_interleaved = (flags & VH_FLAG_ROPE_INTERLEAVED) != 0;
+  p.f16 = (flags & VH_FLAG_FP16) != 0;
   p.q = q;
   p.k_new = k_new;
   p.v_new = v_new;
@@ -289,14 +291,16 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
   return ws_layout(B, Hq, Hkv, D, N).total;
 }
 
-int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf16* v_cache,
+int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16* v_cache,
                          int64_t page_stride, int64_t token_stride, int num_pages,
                          const int32_t* page_table, int max_pages_per_seq,
                          const int32_t* seq_lens, const int32_t* active,
-                         vh_bf16* out, float sm_scale, int num_ctas,
-                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                         vh_e16* out, float sm_scale, int num_ctas,
+                         void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                          int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out) return VH_EINVAL;
+  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out ||
+      (flags & ~static_cast<unsigned>(VH_FLAG_FP16)) != 0)
+    return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
       token_stride < 1 || num_ctas < 0 || num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) ||
       !(sm_scale == sm_scale))
@@ -321,6 +325,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
   p.active = active;
   p.out = out;
   p.err_flag = err_flag;
+  p.f16 = (flags & VH_FLAG_FP16) != 0;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -339,9 +344,11 @@ int vh_paged_decode_attn(const float* q_rot, const vh_bf16* k_cache, const vh_bf
   return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? VH_OK : VH_ECUDA;
 }
 
-int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* out, int num_ctas,
-                      int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!out || !valid_shape(B, Hq, Hkv, D, page_size) || num_ctas < 0 || num_ctas > 65535) return VH_EINVAL;
+int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out, int num_ctas,
+                      unsigned flags, int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!out || !valid_shape(B, Hq, Hkv, D, page_size) || num_ctas < 0 || num_ctas > 65535 ||
+      (flags & ~static_cast<unsigned>(VH_FLAG_FP16)) != 0)
+    return VH_EINVAL;
   if (!aligned16(out)) return VH_EALIGN;
   if (!workspace) return VH_EWORKSPACE;
   if (!aligned16(workspace)) return VH_EALIGN;
@@ -369,21 +376,22 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_bf16* ou
   p.Hc = a.Hc;
   p.G = a.G;
   p.N = N;
+  p.f16 = (flags & VH_FLAG_FP16) != 0;
   return vh::launch_decode_combine(p, a.groups, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK
                                                                                                  : VH_ECUDA;
 }
 
-int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new,
+int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     const float* cos_sin, int max_pos, const int32_t* positions,
                     const float* q_norm_w, const float* k_norm_w, float norm_eps,
-                    vh_bf16* k_cache, vh_bf16* v_cache, int64_t page_stride, int64_t token_stride,
+                    vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride, int64_t token_stride,
                     int num_pages, const int32_t* page_table, int max_pages_per_seq,
                     const int32_t* seq_lens, const int32_t* active,
-                    vh_bf16* out, float sm_scale, int num_ctas,
+                    vh_e16* out, float sm_scale, int num_ctas,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                     int B, int Hq, int Hkv, int D, int page_size, void* stream) {
   if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !page_table || !seq_lens || !active ||
-      !out || (flags & ~static_cast<unsigned>(VH_FLAG_PDL)) != 0)
+      !out || (flags & ~(VH_FLAG_PDL | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0)
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
       page_stride < 1 || token_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
@@ -402,6 +410,8 @@ int vh_decode_fused(const vh_bf16* q, const vh_bf16* k_new, const vh_bf16* v_new
   p.q_norm_w = q_norm_w;
   p.k_norm_w = k_norm_w;
   p.norm_eps = norm_eps;
+  p.rope_interleaved = (flags & VH_FLAG_ROPE_INTERLEAVED) != 0;
+  p.f16 = (flags & VH_FLAG_FP16) != 0;
   p.q = q;
   p.k_new = k_new;
   p.v_new = v_new;

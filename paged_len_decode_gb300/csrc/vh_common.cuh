@@ -2,8 +2,9 @@
 //
 // Inline PTX for the Blackwell data movers used here: mbarrier phase waits
 // with a time limit, and the bulk (TMA, non-tensor) global->shared copy that
-// completes on an mbarrier transaction count.  Plus bf16 unpacking and the
-// packed two-lane fp32 FMA of sm_100-class GPUs.
+// completes on an mbarrier transaction count.  Plus bf16 / fp16 unpacking,
+// rounding and tensor-core products, and the packed two-lane fp32 FMA of
+// sm_100-class GPUs.
 #pragma once
 
 #include <cstdint>
@@ -157,6 +158,76 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   hi = pack_bf16x2(x0, x1);
   const float2 h = bf16x2_to_float2(hi);
   lo = pack_bf16x2(x0 - h.x, x1 - h.y);
+}
+
+// fp16 counterparts of the conversions above (IEEE binary16, round to nearest even).
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
+  float a, b;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(w));
+  return make_float2(a, b);
+}
+
+__device__ __forceinline__ uint32_t float_to_f16_bits(float f) {
+  unsigned short h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// c += a (16x16, row) * b (16x8, col), fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Element type of q, k, v, the cache and the output: bf16 or fp16, both
+// 16-bit patterns in memory.  The kernels are written once against this
+// interface: unpacking, rounding (RNE), the hi + residual split of an fp32
+// operand, and the tensor-core product of that type.
+struct ElemBf16 {
+  static constexpr bool kF16 = false;
+  static __device__ __forceinline__ float2 to_float2(uint32_t w) { return bf16x2_to_float2(w); }
+  static __device__ __forceinline__ float to_float(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+  static __device__ __forceinline__ uint16_t bits(float f) { return static_cast<uint16_t>(float_to_bf16_bits(f)); }
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  static __device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    mma_bf16(c, a0, a1, a2, a3, b0, b1);
+  }
+};
+
+struct ElemF16 {
+  static constexpr bool kF16 = true;
+  static __device__ __forceinline__ float2 to_float2(uint32_t w) { return f16x2_to_float2(w); }
+  static __device__ __forceinline__ float to_float(uint16_t h) { return f16x2_to_float2(h).x; }
+  static __device__ __forceinline__ uint16_t bits(float f) { return static_cast<uint16_t>(float_to_f16_bits(f)); }
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_f16x2(lo, hi); }
+  static __device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    mma_f16(c, a0, a1, a2, a3, b0, b1);
+  }
+};
+
+// Split two fp32 values into a high part and a residual of element type E,
+// x = hi + lo, both rounded to nearest even: bf16 keeps |x - hi - lo| <= 2^-16 |x|;
+// fp16 keeps 2^-22 |x| for normal residuals, and an absolute 2^-25 once the
+// residual is subnormal (the fp16 exponent range ends at 2^-14).
+template <typename E>
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = E::pack2(x0, x1);
+  const float2 h = E::to_float2(hi);
+  lo = E::pack2(x0 - h.x, x1 - h.y);
 }
 
 // Programmatic dependent launch: let the next kernel on the stream start its

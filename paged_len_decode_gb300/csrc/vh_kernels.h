@@ -28,6 +28,8 @@ struct RopeAppendParams {
   const float* q_norm_w;       // [D] RMSNorm weights of q heads, or null
   const float* k_norm_w;       // [D] RMSNorm weights of the new k heads, or null
   float norm_eps;
+  int rope_interleaved;        // RoPE pairs (2i, 2i+1) instead of (i, i + D/2)
+  int f16;                     // 16-bit elements are fp16 (else bf16)
   int B, Hq, Hkv, D, P;
 };
 
@@ -53,7 +55,7 @@ struct AttnParams {
   float* part_lse;             // [groups][N][2][Hc*G]   (base-2 log-sum-exp)
   int32_t* err_flag;
   // fused step only: RoPE of q and k, append of the new token, in-kernel combine
-  const uint16_t* q;           // [B][Hq][D] bf16 new queries
+  const uint16_t* q;           // [B][Hq][D] new queries (bf16 / fp16)
   const uint16_t* k_new;       // [B][Hkv][D]
   const uint16_t* v_new;       // [B][Hkv][D]
   const float* cos_sin;        // [max_pos][D]
@@ -64,6 +66,9 @@ struct AttnParams {
   const float* q_norm_w;       // [D] per-head RMSNorm weights before RoPE, or null
   const float* k_norm_w;
   float norm_eps;
+  int rope_interleaved;        // RoPE pairs (2i, 2i+1) instead of (i, i + D/2)
+  // element type of q, k_new, v_new, the cache and out: fp16 if set, else bf16
+  int f16;
   // shapes and plan
   int B, Hq, Hkv, D, G, P;
   int Hc;                      // kv heads per CTA = consumer warps
@@ -90,11 +95,12 @@ struct CombineParams {
   const float* part_lse;
   uint16_t* out;
   int B, Hq, D, Hc, G, N;
+  int f16;
 };
 
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, cudaStream_t stream);
 cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream);
-cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device, both variants
+cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device, every variant
 cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream_t stream);
 cudaError_t decode_attn_occupancy(const AttnParams& p, int* blocks_per_sm);

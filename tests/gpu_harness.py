@@ -1,11 +1,12 @@
 """Helpers for the GPU tests: run the CUDA path through the C interface and
 compare it with the float64 oracle on the same seeded inputs.
 
-Tolerance for float outputs (the attention output, bf16): elementwise
+Tolerance for float outputs (the attention output, bf16 or fp16): elementwise
 |gpu - ref| <= 2e-3 + 1e-2 * |ref|.  The rotated q (fp32) must agree to
 1e-5 + 1e-5 * |ref| (fp32 RoPE with fp32 cos/sin against float64).  The KV
 append must be bit-exact, except rotated-key elements whose float64 value
-lies within the fp32 rotation's error bound of a bf16 rounding midpoint,
+lies within the fp32 rotation's error bound of a rounding midpoint of the
+element type (bf16 or fp16),
 where fp32 and float64 rotation may round to different neighbours.  For
 x' = x_i cos - x_{i+D/2} sin computed in fp32 (cos/sin rounded to fp32, two
 products, one subtraction) the error is below 3 * 2^-24 * (|x_i| + |x_{i+D/2}|);
@@ -32,7 +33,7 @@ PATHS = ("three", "fused")
 
 
 def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, graph=False,
-             repeat=1, pdl=False, norm=None):
+             repeat=1, pdl=False, norm=None, interleaved=False):
     """Run one decode step on `inp` (CPU or CUDA DecodeInputs) through the C interface.
 
     path "three": vh_rope_kv_append + vh_paged_decode_attn + vh_decode_combine;
@@ -47,7 +48,7 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
     cos_sin = torch.empty((max_pos, D), dtype=torch.float32, device=dev)
     v.vh_rope_table(cos_sin, g.theta)
     q_rot = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=dev)
-    out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    out = torch.full((B, Hq, D), float("nan"), dtype=g.pool.dtype, device=dev)
     ws = v.alloc_workspace(B, Hq, Hkv, D, P, num_ctas, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     pos = positions.to(dev, torch.int32) if positions is not None else None
@@ -64,11 +65,12 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
             if path == "fused":
                 v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
                                   g.active, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
-                                  err_flag=err, pdl=pdl, q_norm_w=nq, k_norm_w=nk, norm_eps=eps)
+                                  err_flag=err, pdl=pdl, q_norm_w=nq, k_norm_w=nk, norm_eps=eps,
+                                  interleaved=interleaved)
             else:
                 v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
                               g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
-                              err_flag=err, q_norm_w=nq, k_norm_w=nk, norm_eps=eps)
+                              err_flag=err, q_norm_w=nq, k_norm_w=nk, norm_eps=eps, interleaved=interleaved)
 
     if graph:
         # first call outside capture (sets per-device launch attributes)
@@ -93,23 +95,34 @@ def bits16(t):
     return t.contiguous().view(torch.int16).to(torch.int32) & 0xFFFF
 
 
-def midpoint_mask(x: torch.Tensor, k_in: torch.Tensor, rel: float = MIDPOINT_REL) -> torch.Tensor:
+# significand bits and smallest quantum (subnormal step) of the 16-bit types
+_GRID = {torch.bfloat16: (8, -133), torch.float16: (11, -24)}
+
+
+def midpoint_mask(x: torch.Tensor, k_in: torch.Tensor, rel: float = MIDPOINT_REL,
+                  dtype=torch.bfloat16, interleaved: bool = False) -> torch.Tensor:
     """Elements of the rotated keys x (float64 [..., D]) that lie within the fp32
-    rotation error bound of a bf16 rounding midpoint; k_in are the keys fed to
-    the rotation, whose pair magnitudes set the bound."""
+    rotation error bound of a rounding midpoint of `dtype`; k_in are the keys
+    fed to the rotation, whose pair magnitudes set the bound (pairs (i, i+D/2),
+    or (2i, 2i+1) when interleaved)."""
+    bits, qmin = _GRID[dtype]
     ax = x.abs()
     nz = ax > 0
     e = torch.frexp(torch.where(nz, ax, torch.ones_like(ax))).exponent
-    ulp = torch.ldexp(torch.ones_like(ax), (e - 8).clamp(min=-133))
+    ulp = torch.ldexp(torch.ones_like(ax), (e - bits).clamp(min=qmin))
     frac = torch.remainder(ax / ulp, 1.0)
     k = k_in.double().abs()
-    h = k.shape[-1] // 2
-    pair = k[..., :h] + k[..., h:]
-    scale = torch.cat([pair, pair], dim=-1)
+    if interleaved:
+        pair = k[..., 0::2] + k[..., 1::2]
+        scale = torch.stack([pair, pair], dim=-1).flatten(-2)
+    else:
+        h = k.shape[-1] // 2
+        pair = k[..., :h] + k[..., h:]
+        scale = torch.cat([pair, pair], dim=-1)
     return nz & ((frac - 0.5).abs() * ulp <= rel * scale)
 
 
-def check_append(inp, ref, gpu_pool, rel=MIDPOINT_REL):
+def check_append(inp, ref, gpu_pool, rel=MIDPOINT_REL, interleaved=False):
     """Bit-exact placement: pool after the GPU append == pool after the oracle append,
     except midpoint-exempt rotated-key elements.  Returns (number of exempt
     elements, number that actually differ)."""
@@ -122,7 +135,7 @@ def check_append(inp, ref, gpu_pool, rel=MIDPOINT_REL):
     act = inp.active.cpu().bool()
     lens = inp.seq_lens.cpu()
     pt = inp.page_table.cpu()
-    mid = midpoint_mask(ref["k_rot"], ref["k_pre"], rel)
+    mid = midpoint_mask(ref["k_rot"], ref["k_pre"], rel, dtype=gpu_pool.dtype, interleaved=interleaved)
     n = 0
     for bb in torch.nonzero(act).flatten().tolist():
         L = int(lens[bb])
@@ -132,7 +145,7 @@ def check_append(inp, ref, gpu_pool, rel=MIDPOINT_REL):
     bad = diff & ~allowed
     assert not bad.any(), f"{int(bad.sum())} pool elements differ outside the midpoint exemption, " \
                           f"first at {torch.nonzero(bad)[0].tolist()}"
-    # and the differing exempt elements are one bf16 step apart
+    # and the differing exempt elements are one step of the element type apart
     d = (a[diff] - b[diff]).abs()
     assert (d == 1).all()
     return n, int(diff.sum())
@@ -170,16 +183,19 @@ def check_q_rot(inp, ref_q_rot, gpu_q_rot):
 
 
 def full_check(inp, *, path="three", num_ctas=0, rows=None, positions=None, sm_scale=0.0, graph=False,
-               max_pos=None, repeat=1, pdl=False, norm=None):
+               max_pos=None, repeat=1, pdl=False, norm=None, interleaved=False):
     """Run the GPU path and the oracle on `inp`; check q_rot (three-call path),
-    the append bits and the output.  norm: dict(q, k, eps) of RMSNorm weights."""
+    the append bits and the output.  norm: dict(q, k, eps) of RMSNorm weights.
+    The element type (bf16 / fp16) is the one of inp's tensors."""
     cpu = inp.to("cpu")
     nk = {} if norm is None else {"q_norm_w": norm["q"], "k_norm_w": norm["k"], "norm_eps": norm["eps"]}
-    ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale, **nk)
+    ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale, interleaved=interleaved,
+                                **nk)
     got = run_step(inp, path=path, num_ctas=num_ctas, positions=positions, sm_scale=sm_scale, graph=graph,
-                   max_pos=max_pos, repeat=repeat, pdl=pdl, norm=norm)
+                   max_pos=max_pos, repeat=repeat, pdl=pdl, norm=norm, interleaved=interleaved)
     assert got["err"] == 0, f"device error flag {got['err']}"
-    exempt, n_diff = check_append(cpu, ref, got["pool_after"], MIDPOINT_REL if norm is None else MIDPOINT_REL_NORM)
+    exempt, n_diff = check_append(cpu, ref, got["pool_after"], MIDPOINT_REL if norm is None else MIDPOINT_REL_NORM,
+                                  interleaved=interleaved)
     qerr = check_q_rot(cpu, ref["q_rot"], got["q_rot"]) if path == "three" else 0.0
     oerr = check_out(cpu, ref["out"], got["out"], rows=rows)
     return {"exempt": exempt, "n_diff": n_diff, "q_rot_err": qerr, "out_err": oerr, "got": got, "ref": ref}

@@ -39,12 +39,13 @@ def test_status_strings():
 
 def attn(**over):
     a = dict(q_rot=FAKE, k=FAKE, vv=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10,
-             sl=FAKE, act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None,
+             sl=FAKE, act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None, flags=0,
              B=4, Hq=16, Hkv=8, D=128, P=16)
     a.update(over)
     return v.lib.vh_paged_decode_attn(a["q_rot"], a["k"], a["vv"], a["ps"], a["ts"], a["npages"], a["pt"],
                                       a["mps"], a["sl"], a["act"], a["out"], a["scale"], a["nctas"], a["ws"],
-                                      a["wsb"], a["err"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
+                                      a["wsb"], a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
+                                      None)
 
 
 @pytest.mark.parametrize("over,code", [
@@ -67,6 +68,10 @@ def attn(**over):
     (dict(ts=8 * 128 + 4), v.VH_EALIGN),      # stride not a multiple of 16 bytes
     (dict(ws=None), v.VH_EWORKSPACE),
     (dict(ws=ODD), v.VH_EALIGN),
+    (dict(flags=v.VH_FLAG_PDL), v.VH_EINVAL),                 # not a flag of this call
+    (dict(flags=v.VH_FLAG_ROPE_INTERLEAVED), v.VH_EINVAL),    # nor this one (no RoPE here)
+    (dict(flags=8), v.VH_EINVAL),
+    (dict(flags=v.VH_FLAG_FP16, q_rot=ODD), v.VH_EALIGN),     # fp16 passes the flag check
 ])
 def test_attention_argument_checks(over, code):
     assert attn(**over) == code
@@ -86,11 +91,11 @@ def test_rope_append_argument_checks():
     def call(**over):
         a = dict(q=FAKE, k=FAKE, vv=FAKE, cs=FAKE, max_pos=4096, pos=None, qw=None, kw=None, eps=1e-6,
                  kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10, sl=FAKE,
-                 act=FAKE, q_rot=FAKE, err=None, B=4, Hq=16, Hkv=8, D=128, P=16)
+                 act=FAKE, q_rot=FAKE, err=None, flags=0, B=4, Hq=16, Hkv=8, D=128, P=16)
         a.update(over)
         return f(a["q"], a["k"], a["vv"], a["cs"], a["max_pos"], a["pos"], a["qw"], a["kw"], a["eps"], a["kc"],
                  a["vc"], a["ps"], a["ts"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["q_rot"],
-                 a["err"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
+                 a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
 
     assert call(cs=None) == v.VH_EINVAL
     assert call(max_pos=0) == v.VH_EINVAL
@@ -101,6 +106,9 @@ def test_rope_append_argument_checks():
     assert call(q_rot=ODD) == v.VH_EALIGN
     assert call(qw=ODD) == v.VH_EALIGN
     assert call(kw=ODD) == v.VH_EALIGN
+    assert call(flags=v.VH_FLAG_PDL) == v.VH_EINVAL
+    assert call(flags=16) == v.VH_EINVAL
+    assert call(flags=v.VH_FLAG_FP16 | v.VH_FLAG_ROPE_INTERLEAVED, q=ODD) == v.VH_EALIGN
 
 
 def test_fused_argument_checks():
@@ -118,7 +126,8 @@ def test_fused_argument_checks():
                  None)
 
     assert call(q=None) == v.VH_EINVAL
-    assert call(flags=4) == v.VH_EINVAL            # unknown flag
+    assert call(flags=8) == v.VH_EINVAL            # unknown flag
+    assert call(flags=v.VH_FLAG_PDL | v.VH_FLAG_FP16 | v.VH_FLAG_ROPE_INTERLEAVED, out=ODD) == v.VH_EALIGN
     assert call(Hq=24) == v.VH_EINVAL
     assert call(eps=-0.5) == v.VH_EINVAL
     assert call(out=ODD) == v.VH_EALIGN
@@ -130,8 +139,10 @@ def test_rope_table_and_combine_argument_checks():
     assert v.lib.vh_rope_table(None, 10, 128, 10000.0, None) == v.VH_EINVAL
     assert v.lib.vh_rope_table(FAKE, 10, 128, -1.0, None) == v.VH_EINVAL
     assert v.lib.vh_rope_table(ODD, 10, 128, 10000.0, None) == v.VH_EALIGN
-    assert v.lib.vh_decode_combine(None, 0, FAKE, 0, 4, 16, 8, 128, 16, None) == v.VH_EWORKSPACE
-    assert v.lib.vh_decode_combine(FAKE, 1 << 30, ODD, 0, 4, 16, 8, 128, 16, None) == v.VH_EALIGN
-    assert v.lib.vh_decode_combine(FAKE, 1 << 30, FAKE, 0, 4, 12, 8, 128, 16, None) == v.VH_EINVAL
+    assert v.lib.vh_decode_combine(None, 0, FAKE, 0, 0, 4, 16, 8, 128, 16, None) == v.VH_EWORKSPACE
+    assert v.lib.vh_decode_combine(FAKE, 1 << 30, ODD, 0, 0, 4, 16, 8, 128, 16, None) == v.VH_EALIGN
+    assert v.lib.vh_decode_combine(FAKE, 1 << 30, FAKE, 0, 0, 4, 12, 8, 128, 16, None) == v.VH_EINVAL
+    assert v.lib.vh_decode_combine(FAKE, 1 << 30, FAKE, 0, v.VH_FLAG_PDL, 4, 16, 8, 128, 16, None) == v.VH_EINVAL
+    assert v.lib.vh_decode_combine(FAKE, 1 << 30, ODD, 0, v.VH_FLAG_FP16, 4, 16, 8, 128, 16, None) == v.VH_EALIGN
     assert v.lib.vh_decode_workspace_bytes(4, 12, 8, 128, 16, 10) == 0
     assert v.lib.vh_decode_workspace_bytes(4, 16, 8, 128, 16, 152) > 0

@@ -271,3 +271,95 @@ def test_qk_rms_norm_of_q_only(path):
     inp = case([77, 16, 5], seed=41)
     nm = _norm(inp.D, 41)
     H.full_check(inp, path=path, norm={"q": nm["q"], "k": None, "eps": 1e-6})
+
+
+# ---------------------------------------------------------------- fp16 elements and interleaved RoPE
+
+F16 = torch.float16
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("name", ["tiny", "c64", "padded", "long"])
+def test_fp16_workload_parity(name, path):
+    inp = workloads.make_inputs(name, device="cuda", dtype=F16)
+    r = H.full_check(inp, path=path)
+    assert r["got"]["out"].dtype == F16
+    print(f"{name} fp16: out max|d| {r['out_err']:.2e}, exempt {r['exempt']} (differing {r['n_diff']})")
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_fp16_high_concurrency_layer(path):
+    inp = workloads.make_inputs("high", layer=5, device="cuda", dtype=F16)
+    H.full_check(inp, path=path)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, F16])
+@pytest.mark.parametrize("name", ["tiny", "c64", "long"])
+def test_interleaved_rope_parity(name, dtype, path):
+    inp = workloads.make_inputs(name, device="cuda", dtype=dtype)
+    H.full_check(inp, path=path, interleaved=True)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("interleaved", [False, True])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp16_groups_and_dims(G, D, interleaved, path):
+    inp = case([37, 300, 129, 1, 16], Hq=G * 2, Hkv=2, D=D, seed=G * 7 + D, dtype=F16)
+    H.full_check(inp, path=path, interleaved=interleaved)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, F16])
+def test_interleaved_rope_with_qk_norm(dtype, path):
+    inp = case([200, 33, 1, 64], Hq=16, Hkv=8, seed=51, dtype=dtype)
+    H.full_check(inp, path=path, norm=_norm(inp.D, 52), interleaved=True)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_fp16_single_key_rows_return_v_new_bit_exactly(path):
+    inp = case([1, 1, 1], Hq=16, Hkv=8, dtype=F16)
+    r = H.full_check(inp, path=path, interleaved=True)
+    G = inp.Hq // inp.Hkv
+    for g in range(inp.Hq):
+        assert torch.equal(H.bits16(r["got"]["out"][:, g]), H.bits16(inp.v_new.cpu()[:, g // G]))
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("num_ctas", [1, 3, 64, 1000])
+def test_fp16_forced_cta_counts(num_ctas, path):
+    # split rows are merged into fp16 by the combine kernel / the fused merge
+    inp = case([1500, 7, 640, 33], Hq=16, Hkv=8, seed=61, dtype=F16)
+    H.full_check(inp, path=path, num_ctas=num_ctas)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_fp16_fused_programmatic_dependent_launch(graph):
+    inp = workloads.make_inputs("c64", device="cuda", dtype=F16)
+    H.full_check(inp, path="fused", pdl=True, graph=graph, interleaved=True)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_fp16_wide_value_range(path):
+    # keys scaled up (large, peaked scores) and values spread from fp16
+    # subnormals (below 2^-14) to a few thousand, all exactly representable
+    inp = case([90, 300, 17], Hq=8, Hkv=2, seed=71, dtype=F16)
+    g = torch.Generator(device="cuda").manual_seed(72)
+    scale = torch.exp2(torch.randint(-20, 12, inp.pool[:, 1].shape, generator=g, device="cuda").float())
+    nan = torch.isnan(inp.pool.float())
+    inp.pool[:, 1] = (inp.pool[:, 1].float() * scale).to(F16)
+    inp.pool[:, 0] = (inp.pool[:, 0].float() * 6.0).to(F16)
+    inp.pool[nan] = float("nan")                      # keep the stale slots poisoned
+    inp.v_new.mul_(1e-6)
+    r = H.full_check(inp, path=path)
+    assert torch.isfinite(r["got"]["out"].float()).all()
+
+
+def test_fp16_fused_and_three_call_paths_agree():
+    inp = workloads.make_inputs("c64", device="cuda", dtype=F16)
+    a = H.run_step(inp, path="three", interleaved=True)
+    b = H.run_step(inp, path="fused", interleaved=True)
+    assert torch.equal(H.bits16(a["pool_after"]), H.bits16(b["pool_after"]))
+    d = (a["out"].double() - b["out"].double()).abs()
+    assert (d <= 2e-3 + 1e-2 * a["out"].double().abs()).all()
