@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="16-bit element type of q, k, v, the cache and the output")
+    ap.add_argument("--layout", default="NHD", choices=["NHD", "HND"],
+                    help="page layout: token-major [NP,2,P,Hkv,D] or head-major [NP,2,Hkv,P,D]")
     ap.add_argument("--interleaved", action="store_true",
                     help="interleaved (2i, 2i+1) RoPE pairing instead of rotate-half")
     ap.add_argument("--qk-norm", action="store_true",
@@ -195,18 +197,18 @@ class Setup:
     layers in order."""
 
     def __init__(self, name: str, rank: int, dev, replicas: int | None = None, layers: int | None = None,
-                 qk_norm: bool = False, dtype: str = "bf16", interleaved: bool = False):
+                 qk_norm: bool = False, dtype: str = "bf16", interleaved: bool = False, layout: str = "NHD"):
         import paged_len_decode_gb300 as vh
         self.vh = vh
         self.L = layers or workloads.WORKLOADS[name].layers
         et = torch.float16 if dtype == "fp16" else torch.bfloat16
         if self.L > 1:
-            self.layer_inputs = [workloads.make_inputs(name, layer=rank * self.L + l, device=dev, dtype=et)
-                                 for l in range(self.L)]
+            self.layer_inputs = [workloads.make_inputs(name, layer=rank * self.L + l, device=dev, dtype=et,
+                                                       layout=layout) for l in range(self.L)]
             inp = self.layer_inputs[0]
         else:
             self.layer_inputs = None
-            inp = workloads.make_inputs(name, layer=rank, device=dev, dtype=et)
+            inp = workloads.make_inputs(name, layer=rank, device=dev, dtype=et, layout=layout)
         self.inp = inp
         self.B, self.Hq, self.Hkv, self.D, self.P = inp.B, inp.Hq, inp.Hkv, inp.D, inp.P
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -238,14 +240,23 @@ class Setup:
         per = [step_bytes(li) for li in self.layer_inputs]
         return {k: (sum(x[k] for x in per) if k != "active" else per[0][k]) for k in per[0]}
 
+    def kv(self, r):
+        """[NP, P, Hkv, D] K and V views of pool r (strided for head-major pages)."""
+        pool = self.pools[r]
+        if self.inp.layout == "HND":
+            return pool[:, 0].transpose(1, 2), pool[:, 1].transpose(1, 2)
+        return pool[:, 0], pool[:, 1]
+
     def fused(self, r, pdl=True, src=None):
         s = src or self.inputs(r)
-        self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
+        k, v = self.kv(r)
+        self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v,
                                 s.page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl, **self.norm)
 
     def three(self, r):
         i = self.inputs(r)
-        self.vh.decode_step(i.q, i.k_new, i.v_new, self.cos_sin, self.pools[r][:, 0], self.pools[r][:, 1],
+        k, v = self.kv(r)
+        self.vh.decode_step(i.q, i.k_new, i.v_new, self.cos_sin, k, v,
                             i.page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3, **self.norm)
 
 
@@ -253,7 +264,8 @@ def run_ncu_case(args):
     """A few eager launches on one pool: 3 fused, 3 three-call steps."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    s = Setup(args.workload, 0, dev, replicas=1, layers=1, dtype=args.dtype, interleaved=args.interleaved)
+    s = Setup(args.workload, 0, dev, replicas=1, layers=1, dtype=args.dtype, interleaved=args.interleaved,
+              layout=args.layout)
     for _ in range(3):
         s.fused(0, pdl=False)
     for _ in range(3):
@@ -282,7 +294,7 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
         h_arena[offs[k]:offs[k] + n].copy_(t.contiguous().view(torch.uint8).view(-1).cpu())
         views[k] = d_arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
     d_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
-        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool")}, **views})
+        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool", "layout")}, **views})
     h_out = torch.empty((s.B, s.Hq, s.D), dtype=s.out.dtype).pin_memory()
     h2d = total
     d2h = h_out.numel() * h_out.element_size()
@@ -337,7 +349,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
     s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm, dtype=args.dtype,
-              interleaved=args.interleaved)
+              interleaved=args.interleaved, layout=args.layout)
     inp, R, L = s.inp, s.R, s.L
     by = s.step_bytes()
 
@@ -416,7 +428,7 @@ def run_ours(args, rank, world):
                            "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
                            "PDL between launches",
                    "layers": L, "qk_norm": bool(args.qk_norm), "rope": "interleaved" if args.interleaved
-                   else "rotate-half", "elements": args.dtype,
+                   else "rotate-half", "elements": args.dtype, "pages": args.layout,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": (f"{L} KV pools, one per layer ({L * s.pool_bytes / 1e9:.1f} GB)" if L > 1 else
                           f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB")
@@ -427,7 +439,8 @@ def run_ours(args, rank, world):
                                f"{'ElemF16' if args.dtype == 'fp16' else 'ElemBf16'}> (fused step)",
                      "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(step_gbs / peak, 4), "traffic": (recorded_traffic(args.workload)
-                                                    if args.dtype == "bf16" and not args.interleaved else None),
+                                                    if args.dtype == "bf16" and not args.interleaved
+                                                    and args.layout == "NHD" else None),
                      "peak_kind": peak_kind, "ms_per_launch": round(ms_step / L, 6),
                      "algorithmic_bytes_per_launch": by["step"] // L},
         "three_call": {"ms_per_step": round(ms_three, 6),

@@ -37,11 +37,18 @@
  *     VH_FLAG_FP16 (the Fish kernel of the first source below takes either
  *     type).  One call uses one type for all of its 16-bit arrays.
  *   - Strides are in ELEMENTS.  One layer's cache is reached through
- *     k_cache / v_cache plus page_stride (elements between pages) and
- *     token_stride (elements between token slots of a page); within a slot
- *     the heads are contiguous, head h at offset h*D.  For the layout
- *     [NP, 2, P, Hkv, D]: v_cache = k_cache + P*Hkv*D, page_stride =
- *     2*P*Hkv*D, token_stride = Hkv*D.
+ *     k_cache / v_cache plus page_stride (elements between pages),
+ *     token_stride (elements between token slots of a page) and head_stride
+ *     (elements between the kv heads of a slot); element d of head h of slot
+ *     t of page n is at n*page_stride + t*token_stride + h*head_stride + d.
+ *     Token-major pages [NP, 2, P, Hkv, D] (the vox-serve layout, "NHD"):
+ *     v_cache = k_cache + P*Hkv*D, page_stride = 2*P*Hkv*D, token_stride =
+ *     Hkv*D, head_stride = D.  Head-major pages [NP, 2, Hkv, P, D] ("HND"):
+ *     v_cache = k_cache + Hkv*P*D, page_stride = 2*Hkv*P*D, token_stride = D,
+ *     head_stride = P*D.  All three strides must be multiples of 8 elements
+ *     (16 bytes); the caller guarantees that distinct (page, slot, head)
+ *     rows do not overlap.  Token-major pages move one copy per token row of
+ *     a CTA's heads, head-major pages one copy per (token, head).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
  *   - Every call checks its scalar arguments and pointer alignment on the
  *     host, launches asynchronously and never synchronises or reads device
@@ -114,7 +121,7 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
  *        head / new k head before RoPE, x <- w * x / sqrt(mean(x^2) + norm_eps),
  *        in fp32 (the pages keep "RMSNorm variance" in fp32 for alignment);
  *        NULL skips it.  16-byte aligned.  norm_eps >= 0.
- * k_cache, v_cache, page_stride, token_stride: the layer's paged cache
+ * k_cache, v_cache, page_stride, token_stride, head_stride: the layer's paged cache
  * num_pages: pages in the pool, used only to bounds-check page ids (> 0)
  * page_table int32 [B][max_pages_per_seq]; seq_lens, active int32 [B]
  * q_rot  float [B][Hq][D] out: rotated q in fp32 (rows with active == 0
@@ -135,7 +142,7 @@ int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                       const float* cos_sin, int max_pos, const int32_t* positions,
                       const float* q_norm_w, const float* k_norm_w, float norm_eps,
                       vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride,
-                      int64_t token_stride, int num_pages,
+                      int64_t token_stride, int64_t head_stride, int num_pages,
                       const int32_t* page_table, int max_pages_per_seq,
                       const int32_t* seq_lens, const int32_t* active,
                       float* q_rot, int32_t* err_flag, unsigned flags,
@@ -174,7 +181,7 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
  * cores, so its elements must lie within the fp16 range (|x| <= 65504).
  * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE, VH_ECUDA. */
 int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16* v_cache,
-                         int64_t page_stride, int64_t token_stride, int num_pages,
+                         int64_t page_stride, int64_t token_stride, int64_t head_stride, int num_pages,
                          const int32_t* page_table, int max_pages_per_seq,
                          const int32_t* seq_lens, const int32_t* active,
                          vh_e16* out, float sm_scale, int num_ctas,
@@ -221,7 +228,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     const float* cos_sin, int max_pos, const int32_t* positions,
                     const float* q_norm_w, const float* k_norm_w, float norm_eps,
                     vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride, int64_t token_stride,
-                    int num_pages, const int32_t* page_table, int max_pages_per_seq,
+                    int64_t head_stride, int num_pages, const int32_t* page_table, int max_pages_per_seq,
                     const int32_t* seq_lens, const int32_t* active,
                     vh_e16* out, float sm_scale, int num_ctas,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
@@ -233,7 +240,8 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
  * hands out preallocated arenas, a plug-in inside a host process that owns
  * the CUDA context, a measurement that must not change the memory footprint).
  * Same arguments and result as vh_paged_decode_attn followed by
- * vh_decode_combine with flags 0 (bf16 cache and output), except that there
+ * vh_decode_combine with flags 0 (bf16 cache and output) and token-major
+ * pages (head_stride = D, so it takes no head_stride), except that there
  * is no workspace: the split-K partial
  * results go into one fixed array of VH_STATIC_SCRATCH_BYTES (8 MiB) compiled
  * into the library, which every GPU that loads the library keeps until the

@@ -52,14 +52,14 @@ def _load() -> ctypes.CDLL:
     lib.vh_rope_table.argtypes = [P, I, I, D, P]
     lib.vh_rope_table.restype = I
     U = ctypes.c_uint
-    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I, P, I, P, P, P, P, U,
+    lib.vh_rope_kv_append.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I64, I, P, I, P, P, P, P, U,
                                       I, I, I, I, I, P]
     lib.vh_rope_kv_append.restype = I
     lib.vh_decode_num_ctas.argtypes = [I, I, I, I, I]
     lib.vh_decode_num_ctas.restype = I
     lib.vh_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.vh_decode_workspace_bytes.restype = SZ
-    lib.vh_paged_decode_attn.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P, U,
+    lib.vh_paged_decode_attn.argtypes = [P, P, P, I64, I64, I64, I, P, I, P, P, P, F, I, P, SZ, P, U,
                                          I, I, I, I, I, P]
     lib.vh_paged_decode_attn.restype = I
     lib.vh_decode_combine.argtypes = [P, SZ, P, I, U, I, I, I, I, I, P]
@@ -67,8 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.vh_paged_decode_attn_noalloc.argtypes = [P, P, P, I64, I64, I, P, I, P, P, P, F, I, P,
                                                  I, I, I, I, I, P]
     lib.vh_paged_decode_attn_noalloc.restype = I
-    lib.vh_decode_fused.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I, P, I, P, P, P, F, I, P, SZ,
-                                    P, ctypes.c_uint, I, I, I, I, I, P]
+    lib.vh_decode_fused.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I64, I, P, I, P, P, P, F, I, P,
+                                    SZ, P, ctypes.c_uint, I, I, I, I, I, P]
     lib.vh_decode_fused.restype = I
     return lib
 
@@ -114,16 +114,24 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _cache_view(k_cache: torch.Tensor, v_cache: torch.Tensor, bf16_only: bool = False):
-    """Pointers and element strides of a [NP, P, Hkv, D] paged cache view."""
+    """Pointers and element strides of a [NP, P, Hkv, D] paged cache view.
+
+    Returns (k, v, page_stride, token_stride, head_stride, NP, P, Hkv, D).  The
+    view may be token-major (a slice of [NP, 2, P, Hkv, D]) or head-major (a
+    slice of [NP, 2, Hkv, P, D], transposed to [NP, P, Hkv, D]); head_dim must
+    be contiguous.  With bf16_only (the entry point without a workspace) the
+    heads of a slot must also be contiguous."""
     if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
         raise ValueError("k_cache / v_cache must be [NP, P, Hkv, D] views with equal strides")
-    if k_cache.stride(3) != 1 or k_cache.stride(2) != k_cache.shape[3]:
+    if k_cache.stride(3) != 1:
+        raise ValueError("head_dim must be contiguous in the cache")
+    if bf16_only and k_cache.stride(2) != k_cache.shape[3]:
         raise ValueError("the heads of one token slot must be contiguous ([.., Hkv, D] dense)")
     if k_cache.dtype not in (ELEM_DTYPES[:1] if bf16_only else ELEM_DTYPES):
         raise TypeError(f"k_cache must be bfloat16{'' if bf16_only else ' or float16'}, got {k_cache.dtype}")
     NP, P, Hkv, D = k_cache.shape
     return (_ptr(k_cache, k_cache.dtype, "k_cache"), _ptr(v_cache, k_cache.dtype, "v_cache"),
-            k_cache.stride(0), k_cache.stride(1), NP, P, Hkv, D)
+            k_cache.stride(0), k_cache.stride(1), k_cache.stride(2), NP, P, Hkv, D)
 
 
 def _elem_flags(k_cache: torch.Tensor, interleaved: bool = False) -> int:
@@ -150,7 +158,7 @@ def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, se
                       q_rot, positions=None, err_flag=None, q_norm_w=None, k_norm_w=None,
                       norm_eps: float = 1e-6, interleaved: bool = False, stream=None) -> None:
     B, Hq, D = q.shape
-    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     et = k_cache.dtype
     if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or q_rot.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q, k_new, v_new, q_rot and the cache")
@@ -159,7 +167,7 @@ def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, se
         _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
-        kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        kp, vp, ps, ts, hs, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(q_rot, torch.float32, "q_rot"),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
@@ -183,11 +191,11 @@ def vh_decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, page_size: int,
 def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
                          sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None, stream=None) -> None:
     B, Hq, D = q_rot.shape
-    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     if Dc != D or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q_rot, out and the cache")
     _check(lib.vh_paged_decode_attn(
-        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, NP,
+        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, hs, NP,
         _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(out, k_cache.dtype, "out"), float(sm_scale), int(num_ctas),
@@ -213,7 +221,7 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
     """Attention plus combine into `out` with the library's fixed scratch array,
     for callers that cannot allocate a workspace (see include/vh.h)."""
     B, Hq, D = q_rot.shape
-    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache, bf16_only=True)
+    kp, vp, ps, ts, _hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache, bf16_only=True)
     if Dc != D or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q_rot, out and the cache")
     _check(lib.vh_paged_decode_attn_noalloc(
@@ -233,7 +241,7 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
     `workspace` must be zero-filled before its first use (alloc_workspace does that).
     pdl=True sets VH_FLAG_PDL (see include/vh.h for when that is allowed)."""
     B, Hq, D = q.shape
-    kp, vp, ps, ts, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
+    kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     et = k_cache.dtype
     if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q, k_new, v_new, out and the cache")
@@ -242,7 +250,7 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
         _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
-        kp, vp, ps, ts, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        kp, vp, ps, ts, hs, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(out, et, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),

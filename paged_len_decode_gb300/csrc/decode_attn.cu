@@ -22,9 +22,10 @@
 //    where its tiles straddle two CTAs (at most two partial segments per CTA).
 //  * Data movement.  One producer warp streams each tile into a ring of
 //    shared-memory stages with bulk asynchronous copies (one 16-byte-aligned
-//    copy per token row, K and V rows of the CTA's kv heads) completed on an
-//    mbarrier transaction count; consumers release a stage through a second
-//    mbarrier.  The q rows of the next segment are copied the same way into a
+//    copy per token row, K and V rows of the CTA's kv heads, when the heads
+//    of a slot are contiguous; one copy per token and head for head-major
+//    pages) completed on an mbarrier transaction count; consumers release a
+//    stage through a second mbarrier.  The q rows of the next segment are copied the same way into a
 //    staging buffer while the current segment is still being consumed.
 //  * Math on tensor cores.  One consumer warp per kv head.  With 16 keys per
 //    tile and the G q heads of the kv head padded to 8, the scores are one
@@ -345,8 +346,14 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
     // and the page ids come from a 32-tile window that is loaded (one
     // coalesced load per lane) a whole window ahead of its use.
     const int h0 = gy * Hc;
-    const unsigned char* kbase = reinterpret_cast<const unsigned char*>(p.k_cache + static_cast<long long>(h0) * D);
-    const unsigned char* vbase = reinterpret_cast<const unsigned char*>(p.v_cache + static_cast<long long>(h0) * D);
+    const unsigned char* kbase =
+        reinterpret_cast<const unsigned char*>(p.k_cache + static_cast<long long>(h0) * p.head_stride);
+    const unsigned char* vbase =
+        reinterpret_cast<const unsigned char*>(p.v_cache + static_cast<long long>(h0) * p.head_stride);
+    // heads of a token slot contiguous (token-major pages): one copy per token
+    // row; otherwise (head-major pages) one copy per (token, head)
+    const bool heads_contig = p.head_stride == D;
+    const long long head_bytes = 2LL * p.head_stride;
     long long wb = t0;
     int b = b0;
     long long rt0 = cum[b], rt1 = cum[b + 1];
@@ -406,10 +413,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       // source and destination of this lane's row copy, and the append slot
       const long long page_off = static_cast<long long>(page) * p.page_stride;
       const void* src;
+      bool contig = heads_contig;
       if (FUSED && last_of_row && r == nvalid - 1) {
         // the new token: raw k (rotated by the consumers) and v straight from the inputs
         const long long nrow = (static_cast<long long>(b) * p.Hkv + h0) * D;
         src = lane < 16 ? static_cast<const void*>(p.k_new + nrow) : static_cast<const void*>(p.v_new + nrow);
+        contig = true;
       } else {
         const long long off = 2LL * (page_off + static_cast<long long>(tin_page * kTile + r) * p.token_stride);
         src = (lane < 16 ? kbase : vbase) + off;
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       if constexpr (FUSED) {
         if (last_of_row && page_ok)
           meta_val = page_off + static_cast<long long>(tin_page * kTile + nvalid - 1) * p.token_stride +
-                     static_cast<long long>(h0) * D;
+                     static_cast<long long>(h0) * p.head_stride;
       }
       const uint32_t tx = static_cast<uint32_t>(nvalid) * 2u * p.row_copy_bytes;
 
@@ -440,7 +449,14 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         mbar_arrive_expect_tx(fb, tx);
       }
       __syncwarp();
-      if (r < nvalid) bulk_g2s(dst, src, p.row_copy_bytes, fb);
+      if (r < nvalid) {
+        if (contig) {
+          bulk_g2s(dst, src, p.row_copy_bytes, fb);
+        } else {
+          for (int hh = 0; hh < p.Hc; ++hh)
+            bulk_g2s(dst + hh * D * 2, static_cast<const unsigned char*>(src) + hh * head_bytes, D * 2, fb);
+        }
+      }
       if (++stage == S) {
         stage = 0;
         ++round;
@@ -679,7 +695,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
           if (i < D / 2) {
             const float x = kx[j], y = ky[j];
             const float xr = x * rc[j] - y * rs[j], yr = y * rc[j] + x * rs[j];
-            uint16_t* cache_row = p.k_cache_w + dst + static_cast<long long>(w) * D;
+            uint16_t* cache_row = p.k_cache_w + dst + static_cast<long long>(w) * p.head_stride;
             if (ilv) {
               const uint32_t xy = E::pack2(xr, yr);
               *reinterpret_cast<uint32_t*>(kr + 2 * i) = xy;
@@ -697,7 +713,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         }
         if (dst >= 0 && lane < D / 8) {
           const uint4 vv = *reinterpret_cast<const uint4*>(vst + (nvalid - 1) * p.v_row_bytes + lane * 16);
-          *reinterpret_cast<uint4*>(p.v_cache_w + dst + static_cast<long long>(w) * D + lane * 8) = vv;
+          *reinterpret_cast<uint4*>(p.v_cache_w + dst + static_cast<long long>(w) * p.head_stride + lane * 8) = vv;
         }
         touched = true;
       }

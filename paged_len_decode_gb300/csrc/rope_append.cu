@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p
         *reinterpret_cast<float4*>(dst + half + i) = make_float4(ry[0], ry[1], ry[2], ry[3]);
       }
     } else {
-      uint16_t* dst = p.k_cache + slot_off + static_cast<long long>(h - p.Hq) * D;
+      uint16_t* dst = p.k_cache + slot_off + static_cast<long long>(h - p.Hq) * p.head_stride;
       if (ilv) {
         *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(E::pack2(rx[0], ry[0]), E::pack2(rx[1], ry[1]),
                                                             E::pack2(rx[2], ry[2]), E::pack2(rx[3], ry[3]));
@@ -158,12 +158,13 @@ __global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p
     }
   }
   if (!page_ok) return;
-  // V: Hkv*D 16-bit elements contiguous in v_new and in the slot; 8 per thread.
+  // V: Hkv*D 16-bit elements contiguous in v_new, head h at h*head_stride in
+  // the slot; 8 per thread.
   const int nvec = p.Hkv * D / 8;
   const uint4* vsrc = reinterpret_cast<const uint4*>(p.v_new + static_cast<long long>(b) * p.Hkv * D);
   for (int u = threadIdx.x; u < nvec; u += blockDim.x) {
     const int h = (u * 8) / D, d = (u * 8) % D;
-    *reinterpret_cast<uint4*>(p.v_cache + slot_off + static_cast<long long>(h) * D + d) = vsrc[u];
+    *reinterpret_cast<uint4*>(p.v_cache + slot_off + static_cast<long long>(h) * p.head_stride + d) = vsrc[u];
   }
 }
 

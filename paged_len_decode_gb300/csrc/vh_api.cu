@@ -208,7 +208,7 @@ int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                       const float* cos_sin, int max_pos, const int32_t* positions,
                       const float* q_norm_w, const float* k_norm_w, float norm_eps,
                       vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride,
-                      int64_t token_stride, int num_pages,
+                      int64_t token_stride, int64_t head_stride, int num_pages,
                       const int32_t* page_table, int max_pages_per_seq,
                       const int32_t* seq_lens, const int32_t* active,
                       float* q_rot, int32_t* err_flag, unsigned flags,
@@ -217,12 +217,12 @@ int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
       !q_rot || (flags & ~(VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0)
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
-      page_stride < 1 || token_stride < 1 || too_many_tiles(B, max_pages_per_seq, page_size))
+      page_stride < 1 || token_stride < 1 || head_stride < 1 || too_many_tiles(B, max_pages_per_seq, page_size))
     return VH_EINVAL;
   if (!(norm_eps >= 0.f) || !(norm_eps < 1e30f)) return VH_EINVAL;
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(q_rot) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0 ||
-      !aligned16(q_norm_w) || !aligned16(k_norm_w))
+      (head_stride * 2) % 16 != 0 || !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return VH_EALIGN;
   if (!device_info()) return VH_ENODEV;
   vh::RopeAppendParams p{};
@@ -241,6 +241,7 @@ int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   p.v_cache = v_cache;
   p.page_stride = page_stride;
   p.token_stride = token_stride;
+  p.head_stride = head_stride;
   p.num_pages = num_pages;
   p.page_table = page_table;
   p.max_pages_per_seq = max_pages_per_seq;
@@ -292,7 +293,7 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
 }
 
 int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16* v_cache,
-                         int64_t page_stride, int64_t token_stride, int num_pages,
+                         int64_t page_stride, int64_t token_stride, int64_t head_stride, int num_pages,
                          const int32_t* page_table, int max_pages_per_seq,
                          const int32_t* seq_lens, const int32_t* active,
                          vh_e16* out, float sm_scale, int num_ctas,
@@ -302,11 +303,11 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
       (flags & ~static_cast<unsigned>(VH_FLAG_FP16)) != 0)
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
-      token_stride < 1 || num_ctas < 0 || num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) ||
-      !(sm_scale == sm_scale))
+      token_stride < 1 || head_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
+      too_many_tiles(B, max_pages_per_seq, page_size) || !(sm_scale == sm_scale))
     return VH_EINVAL;
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0)
+      (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0 || (head_stride * 2) % 16 != 0)
     return VH_EALIGN;
   if (!workspace) return VH_EWORKSPACE;
   if (!aligned16(workspace)) return VH_EALIGN;
@@ -318,6 +319,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
   p.v_cache = v_cache;
   p.page_stride = page_stride;
   p.token_stride = token_stride;
+  p.head_stride = head_stride;
   p.num_pages = num_pages;
   p.page_table = page_table;
   p.max_pages_per_seq = max_pages_per_seq;
@@ -385,7 +387,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     const float* cos_sin, int max_pos, const int32_t* positions,
                     const float* q_norm_w, const float* k_norm_w, float norm_eps,
                     vh_e16* k_cache, vh_e16* v_cache, int64_t page_stride, int64_t token_stride,
-                    int num_pages, const int32_t* page_table, int max_pages_per_seq,
+                    int64_t head_stride, int num_pages, const int32_t* page_table, int max_pages_per_seq,
                     const int32_t* seq_lens, const int32_t* active,
                     vh_e16* out, float sm_scale, int num_ctas,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
@@ -394,13 +396,13 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
       !out || (flags & ~(VH_FLAG_PDL | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0)
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
-      page_stride < 1 || token_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
+      page_stride < 1 || token_stride < 1 || head_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
       too_many_tiles(B, max_pages_per_seq, page_size) || !(sm_scale == sm_scale))
     return VH_EINVAL;
   if (!(norm_eps >= 0.f) || !(norm_eps < 1e30f)) return VH_EINVAL;
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(out) || (page_stride * 2) % 16 != 0 || (token_stride * 2) % 16 != 0 ||
-      !aligned16(q_norm_w) || !aligned16(k_norm_w))
+      (head_stride * 2) % 16 != 0 || !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return VH_EALIGN;
   if (!workspace) return VH_EWORKSPACE;
   if (!aligned16(workspace)) return VH_EALIGN;
@@ -424,6 +426,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   p.v_cache_w = v_cache;
   p.page_stride = page_stride;
   p.token_stride = token_stride;
+  p.head_stride = head_stride;
   p.num_pages = num_pages;
   p.page_table = page_table;
   p.max_pages_per_seq = max_pages_per_seq;
@@ -521,6 +524,7 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
   p.v_cache = v_cache;
   p.page_stride = page_stride;
   p.token_stride = token_stride;
+  p.head_stride = D;  // token-major pages: the heads of a slot are contiguous
   p.num_pages = num_pages;
   p.page_table = page_table;
   p.max_pages_per_seq = max_pages_per_seq;

@@ -18,6 +18,7 @@ struct RopeAppendParams {
   uint16_t* v_cache;
   long long page_stride;
   long long token_stride;
+  long long head_stride;       // elements between the kv heads of one token slot
   int num_pages;
   const int32_t* page_table;
   int max_pages_per_seq;
@@ -42,6 +43,7 @@ struct AttnParams {
   const uint16_t* v_cache;
   long long page_stride;
   long long token_stride;
+  long long head_stride;       // elements between the kv heads of one token slot (D: heads contiguous)
   int num_pages;
   const int32_t* page_table;
   int max_pages_per_seq;

@@ -38,7 +38,8 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
 
     path "three": vh_rope_kv_append + vh_paged_decode_attn + vh_decode_combine;
     path "fused": vh_decode_fused (one launch; q_rot is not produced).
-    Returns dict(q_rot, out, pool_after, err) on the CPU; `inp` is not modified.
+    Returns dict(q_rot, out, pool_after, err) on the CPU (pool_after token-major);
+    `inp` is not modified.
     """
     v = vh()
     dev = torch.device("cuda")
@@ -52,7 +53,7 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
     ws = v.alloc_workspace(B, Hq, Hkv, D, P, num_ctas, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     pos = positions.to(dev, torch.int32) if positions is not None else None
-    k_cache, v_cache = g.pool[:, 0], g.pool[:, 1]
+    k_cache, v_cache = g.k_cache(), g.v_cache()   # [NP, P, Hkv, D] views of either page layout
     nq = nk = None
     eps = 1e-6
     if norm is not None:
@@ -88,7 +89,9 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
     else:
         step()
     torch.cuda.synchronize()
-    return {"q_rot": q_rot.cpu(), "out": out.cpu(), "pool_after": g.pool.cpu(), "err": int(err.item())}
+    # pool_after in token-major order whatever the layout, for comparison with the oracle
+    return {"q_rot": q_rot.cpu(), "out": out.cpu(), "pool_after": g.nhd_pool().contiguous().cpu(),
+            "err": int(err.item())}
 
 
 def bits16(t):
@@ -186,8 +189,9 @@ def full_check(inp, *, path="three", num_ctas=0, rows=None, positions=None, sm_s
                max_pos=None, repeat=1, pdl=False, norm=None, interleaved=False):
     """Run the GPU path and the oracle on `inp`; check q_rot (three-call path),
     the append bits and the output.  norm: dict(q, k, eps) of RMSNorm weights.
-    The element type (bf16 / fp16) is the one of inp's tensors."""
-    cpu = inp.to("cpu")
+    The element type (bf16 / fp16) and page layout are those of inp; the oracle
+    always sees the token-major copy of the same pool."""
+    cpu = inp.to("cpu").as_nhd()
     nk = {} if norm is None else {"q_norm_w": norm["q"], "k_norm_w": norm["k"], "norm_eps": norm["eps"]}
     ref = oracle.reference_step(cpu, positions=positions, rows=rows, sm_scale=sm_scale, interleaved=interleaved,
                                 **nk)

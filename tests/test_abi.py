@@ -38,11 +38,11 @@ def test_status_strings():
 
 
 def attn(**over):
-    a = dict(q_rot=FAKE, k=FAKE, vv=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10,
+    a = dict(q_rot=FAKE, k=FAKE, vv=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, hs=128, npages=100, pt=FAKE, mps=10,
              sl=FAKE, act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None, flags=0,
              B=4, Hq=16, Hkv=8, D=128, P=16)
     a.update(over)
-    return v.lib.vh_paged_decode_attn(a["q_rot"], a["k"], a["vv"], a["ps"], a["ts"], a["npages"], a["pt"],
+    return v.lib.vh_paged_decode_attn(a["q_rot"], a["k"], a["vv"], a["ps"], a["ts"], a["hs"], a["npages"], a["pt"],
                                       a["mps"], a["sl"], a["act"], a["out"], a["scale"], a["nctas"], a["ws"],
                                       a["wsb"], a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
                                       None)
@@ -66,6 +66,8 @@ def attn(**over):
     (dict(q_rot=ODD), v.VH_EALIGN),
     (dict(k=ODD), v.VH_EALIGN),
     (dict(ts=8 * 128 + 4), v.VH_EALIGN),      # stride not a multiple of 16 bytes
+    (dict(hs=0), v.VH_EINVAL),
+    (dict(hs=68), v.VH_EALIGN),               # head stride not a multiple of 16 bytes
     (dict(ws=None), v.VH_EWORKSPACE),
     (dict(ws=ODD), v.VH_EALIGN),
     (dict(flags=v.VH_FLAG_PDL), v.VH_EINVAL),                 # not a flag of this call
@@ -90,11 +92,11 @@ def test_rope_append_argument_checks():
 
     def call(**over):
         a = dict(q=FAKE, k=FAKE, vv=FAKE, cs=FAKE, max_pos=4096, pos=None, qw=None, kw=None, eps=1e-6,
-                 kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10, sl=FAKE,
-                 act=FAKE, q_rot=FAKE, err=None, flags=0, B=4, Hq=16, Hkv=8, D=128, P=16)
+                 kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=128, hs=16 * 128, npages=100, pt=FAKE, mps=10,
+                 sl=FAKE, act=FAKE, q_rot=FAKE, err=None, flags=0, B=4, Hq=16, Hkv=8, D=128, P=16)
         a.update(over)
         return f(a["q"], a["k"], a["vv"], a["cs"], a["max_pos"], a["pos"], a["qw"], a["kw"], a["eps"], a["kc"],
-                 a["vc"], a["ps"], a["ts"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["q_rot"],
+                 a["vc"], a["ps"], a["ts"], a["hs"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["q_rot"],
                  a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
 
     assert call(cs=None) == v.VH_EINVAL
@@ -109,6 +111,8 @@ def test_rope_append_argument_checks():
     assert call(flags=v.VH_FLAG_PDL) == v.VH_EINVAL
     assert call(flags=16) == v.VH_EINVAL
     assert call(flags=v.VH_FLAG_FP16 | v.VH_FLAG_ROPE_INTERLEAVED, q=ODD) == v.VH_EALIGN
+    assert call(hs=-8) == v.VH_EINVAL
+    assert call(hs=16 * 128 + 2) == v.VH_EALIGN
 
 
 def test_fused_argument_checks():
@@ -116,12 +120,12 @@ def test_fused_argument_checks():
 
     def call(**over):
         a = dict(q=FAKE, k=FAKE, vv=FAKE, cs=FAKE, max_pos=4096, pos=None, qw=None, kw=None, eps=1e-6,
-                 kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10, sl=FAKE,
-                 act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None, flags=0,
+                 kc=FAKE, vc=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, hs=128, npages=100, pt=FAKE, mps=10,
+                 sl=FAKE, act=FAKE, out=FAKE, scale=0.0, nctas=0, ws=FAKE, wsb=1 << 30, err=None, flags=0,
                  B=4, Hq=16, Hkv=8, D=128, P=16)
         a.update(over)
         return f(a["q"], a["k"], a["vv"], a["cs"], a["max_pos"], a["pos"], a["qw"], a["kw"], a["eps"], a["kc"],
-                 a["vc"], a["ps"], a["ts"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["out"], a["scale"],
+                 a["vc"], a["ps"], a["ts"], a["hs"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"], a["out"], a["scale"],
                  a["nctas"], a["ws"], a["wsb"], a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
                  None)
 
@@ -133,6 +137,8 @@ def test_fused_argument_checks():
     assert call(out=ODD) == v.VH_EALIGN
     assert call(kw=ODD) == v.VH_EALIGN
     assert call(ws=None) == v.VH_EWORKSPACE
+    assert call(hs=0) == v.VH_EINVAL
+    assert call(hs=100) == v.VH_EALIGN
 
 
 def test_rope_table_and_combine_argument_checks():

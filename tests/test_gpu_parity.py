@@ -363,3 +363,54 @@ def test_fp16_fused_and_three_call_paths_agree():
     assert torch.equal(H.bits16(a["pool_after"]), H.bits16(b["pool_after"]))
     d = (a["out"].double() - b["out"].double()).abs()
     assert (d <= 2e-3 + 1e-2 * a["out"].double().abs()).all()
+
+
+# ---------------------------------------------------------------- head-major (HND) pages
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("name", ["tiny", "c64", "padded", "long"])
+def test_head_major_pages_workload_parity(name, path):
+    inp = workloads.make_inputs(name, device="cuda", layout="HND")
+    assert inp.pool.shape[2] == inp.Hkv and inp.head_stride == inp.P * inp.D
+    H.full_check(inp, path=path)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_head_major_pages_high_concurrency_layer(path):
+    inp = workloads.make_inputs("high", layer=9, device="cuda", layout="HND")
+    H.full_check(inp, path=path)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_head_major_pages_groups_and_dims(G, D, path):
+    inp = case([37, 300, 129, 1, 16], Hq=G * 2, Hkv=2, D=D, seed=G * 5 + D + 3, layout="HND")
+    H.full_check(inp, path=path)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("P", [16, 64, 256])
+def test_head_major_pages_sizes_fp16_interleaved_norm(P, path):
+    inp = case([P * 3 + 5, 17, 1, 2 * P], Hq=16, Hkv=8, P=P, seed=P + 80, layout="HND", dtype=torch.float16)
+    H.full_check(inp, path=path, interleaved=True, norm=_norm(inp.D, P))
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_head_major_and_token_major_pages_agree_bit_for_bit(path):
+    a = workloads.make_inputs("c64", device="cuda")
+    b = workloads.make_inputs("c64", device="cuda", layout="HND")
+    assert torch.equal(H.bits16(b.nhd_pool().cpu()), H.bits16(a.pool.cpu()))
+    ra = H.run_step(a, path=path)
+    rb = H.run_step(b, path=path)
+    # the same copies land in the same shared-memory rows: identical results
+    assert torch.equal(H.bits16(ra["out"]), H.bits16(rb["out"]))
+    assert torch.equal(H.bits16(ra["pool_after"]), H.bits16(rb["pool_after"]))
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_head_major_padding_rows_leave_page_zero_alone(path):
+    inp = workloads.make_inputs("padded", device="cuda", layout="HND")
+    before = H.bits16(inp.nhd_pool().cpu())
+    got = H.run_step(inp, path=path)
+    assert torch.equal(H.bits16(got["pool_after"][0]), before[0]), "dummy page 0 was written"

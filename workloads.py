@@ -20,7 +20,9 @@ The five workloads are the serving shapes of the Talker decode step:
 Layout of one layer's pool (the paged KV layout of the vox-serve "Adding a
 Model" page, section "1. The model code", with the layer axis dropped because
 every layer here owns its own pool):  bf16 (or fp16) [num_pages, 2,
-page_size, num_kv_heads, head_dim], K at [:, 0] and V at [:, 1].
+page_size, num_kv_heads, head_dim], K at [:, 0] and V at [:, 1]; on request
+the same values are stored head-major, [num_pages, 2, num_kv_heads,
+page_size, head_dim] (the other layout generic paged attention offers).
 
 Recipe (seed = 20260000 + 100 * workload_index + layer, torch.Generator):
   1. seq_lens: integers uniform in [lo, hi], or floor(exp(U(ln lo, ln hi)))
@@ -113,11 +115,12 @@ class DecodeInputs:
     q: torch.Tensor            # [B, Hq, D] bf16 / fp16
     k_new: torch.Tensor        # [B, Hkv, D]
     v_new: torch.Tensor        # [B, Hkv, D]
-    pool: torch.Tensor         # [NP, 2, P, Hkv, D] (K at [:,0], V at [:,1])
+    pool: torch.Tensor         # NHD: [NP, 2, P, Hkv, D]; HND: [NP, 2, Hkv, P, D] (K at [:,0], V at [:,1])
     page_table: torch.Tensor   # [B, MPS] int32
     seq_lens: torch.Tensor     # [B] int32
     active: torch.Tensor       # [B] int32
     meta: dict = field(default_factory=dict)
+    layout: str = "NHD"        # "NHD": token-major pages; "HND": head-major pages
 
     # element strides of the pool, as the C interface takes them
     @property
@@ -126,27 +129,42 @@ class DecodeInputs:
 
     @property
     def token_stride(self) -> int:
-        return self.Hkv * self.D
+        return self.Hkv * self.D if self.layout == "NHD" else self.D
+
+    @property
+    def head_stride(self) -> int:
+        return self.D if self.layout == "NHD" else self.P * self.D
 
     def k_cache(self) -> torch.Tensor:
-        return self.pool[:, 0]
+        """K as a [NP, P, Hkv, D] view (strided for head-major pages)."""
+        return self.pool[:, 0] if self.layout == "NHD" else self.pool[:, 0].transpose(1, 2)
 
     def v_cache(self) -> torch.Tensor:
-        return self.pool[:, 1]
+        return self.pool[:, 1] if self.layout == "NHD" else self.pool[:, 1].transpose(1, 2)
+
+    def nhd_pool(self) -> torch.Tensor:
+        """The pool in token-major order [NP, 2, P, Hkv, D] (a view, or the pool itself)."""
+        return self.pool if self.layout == "NHD" else self.pool.transpose(2, 3)
+
+    def _fields(self, fn) -> "DecodeInputs":
+        kw = {k: getattr(self, k) for k in ("B", "Hq", "Hkv", "D", "P", "max_pages_per_seq",
+                                            "num_pages", "theta", "layout")}
+        for k in ("q", "k_new", "v_new", "pool", "page_table", "seq_lens", "active"):
+            kw[k] = fn(getattr(self, k))
+        return DecodeInputs(meta=dict(self.meta), **kw)
 
     def to(self, device) -> "DecodeInputs":
-        kw = {k: getattr(self, k) for k in ("B", "Hq", "Hkv", "D", "P", "max_pages_per_seq",
-                                            "num_pages", "theta")}
-        for k in ("q", "k_new", "v_new", "pool", "page_table", "seq_lens", "active"):
-            kw[k] = getattr(self, k).to(device)
-        return DecodeInputs(meta=dict(self.meta), **kw)
+        return self._fields(lambda t: t.to(device))
 
     def clone(self) -> "DecodeInputs":
-        kw = {k: getattr(self, k) for k in ("B", "Hq", "Hkv", "D", "P", "max_pages_per_seq",
-                                            "num_pages", "theta")}
-        for k in ("q", "k_new", "v_new", "pool", "page_table", "seq_lens", "active"):
-            kw[k] = getattr(self, k).clone()
-        return DecodeInputs(meta=dict(self.meta), **kw)
+        return self._fields(lambda t: t.clone())
+
+    def as_nhd(self) -> "DecodeInputs":
+        """The same inputs with a token-major (contiguous) copy of the pool."""
+        d = self._fields(lambda t: t)
+        d.pool = self.nhd_pool().contiguous()
+        d.layout = "NHD"
+        return d
 
 
 def draw_lengths(w: Workload, gen: torch.Generator, n: int) -> torch.Tensor:
@@ -165,7 +183,7 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
               max_pages_per_seq: int | None = None, sigma: float = 1.0, seed: int = 0,
               device="cpu", pool_pages: int = 0, theta: float = 10000.0,
               poison: bool = True, page_order: str = "random",
-              dtype: torch.dtype = torch.bfloat16) -> DecodeInputs:
+              dtype: torch.dtype = torch.bfloat16, layout: str = "NHD") -> DecodeInputs:
     """Draw one layer of inputs for explicit shapes and lengths.
 
     `seq_lens` and `active` are Python sequences (or int64 tensors) of length B.
@@ -173,8 +191,10 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     unless the caller passes other lengths for them on purpose.
     `page_order` is "random" (seeded permutation) or "linear" (pages 1, 2, ...).
     `dtype` (torch.bfloat16 or torch.float16) is the type of q, k, v and the pool.
+    `layout` "HND" stores the same pool values head-major ([NP, 2, Hkv, P, D]).
     """
     assert dtype in (torch.bfloat16, torch.float16)
+    assert layout in ("NHD", "HND")
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     lens = torch.as_tensor(seq_lens, dtype=torch.int64).clone()
@@ -217,8 +237,10 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
         dead = (~live).to(dev)
         bits.masked_fill_(dead.view(NP, 1, P, 1, 1).expand_as(bits), NAN_BITS)
 
+    if layout == "HND":
+        pool = pool.transpose(2, 3).contiguous()
     return DecodeInputs(
-        B=B, Hq=Hq, Hkv=Hkv, D=D, P=P, max_pages_per_seq=mps, num_pages=NP, theta=theta,
+        B=B, Hq=Hq, Hkv=Hkv, D=D, P=P, max_pages_per_seq=mps, num_pages=NP, theta=theta, layout=layout,
         q=q, k_new=k_new, v_new=v_new, pool=pool,
         page_table=page_table.to(torch.int32).to(dev),
         seq_lens=lens.to(torch.int32).to(dev), active=act.to(torch.int32).to(dev),
@@ -226,7 +248,8 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     )
 
 
-def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = torch.bfloat16) -> DecodeInputs:
+def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = torch.bfloat16,
+                layout: str = "NHD") -> DecodeInputs:
     """Inputs of one layer of a named workload (see the module docstring)."""
     w = WORKLOADS[name]
     seed = SEED_BASE + 100 * w.index + layer
@@ -243,7 +266,7 @@ def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = to
     sub_seed = int(torch.randint(0, 2**31 - 1, (1,), generator=gen))
     inp = make_case(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, P=w.P, seq_lens=lens, active=act,
                     max_pages_per_seq=w.max_pages_per_seq, sigma=w.sigma, seed=sub_seed,
-                    device=device, pool_pages=w.pool_pages, theta=w.theta, dtype=dtype)
+                    device=device, pool_pages=w.pool_pages, theta=w.theta, dtype=dtype, layout=layout)
     inp.meta.update({"workload": name, "layer": layer, "workload_seed": seed})
     return inp
 
