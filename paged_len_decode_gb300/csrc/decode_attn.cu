@@ -11,7 +11,10 @@
 // The fused variant also applies RoPE to q and to the new key and appends
 // the new key/value to the cache ("Adding a Model", vox-serve, section 1:
 // write K/V into the paged cache, then attend), and merges split rows
-// itself, so one launch is one whole decode step of a layer.
+// itself, so one launch is one whole decode step of a layer: the CTA that
+// owns a row's last tile reads the raw new k / v from the inputs, writes the
+// rotated key and the value into that tile's last row in shared memory and
+// into the cache slot.
 //
 // Design for GB300 (HBM-bound: 2-4 flops per byte of K/V):
 //  * Work list.  Every active row contributes ceil(L/16) tiles of 16 tokens;
@@ -21,12 +24,18 @@
 //    balanced to within one tile whatever the length mix; a row is split
 //    where its tiles straddle two CTAs (at most two partial segments per CTA).
 //  * Data movement.  One producer warp streams each tile into a ring of
-//    shared-memory stages with bulk asynchronous copies (one 16-byte-aligned
-//    copy per token row, K and V rows of the CTA's kv heads, when the heads
-//    of a slot are contiguous; one copy per token and head for head-major
-//    pages) completed on an mbarrier transaction count; consumers release a
-//    stage through a second mbarrier.  The q rows of the next segment are copied the same way into a
-//    staging buffer while the current segment is still being consumed.
+//    shared-memory stages with tiled tensor copies (TMA, cp.async.bulk.tensor)
+//    completed on an mbarrier transaction count; consumers release a stage
+//    through a second mbarrier.  The cache is described to the copy engine as
+//    a 4-D tensor (head_dim, token, kv head, page) whose strides come from the
+//    caller, so token-major and head-major pages take the same path: per
+//    64-element column block and per 8-token group, one box holds all of the
+//    CTA's kv heads (8 copies per 16-token tile at head_dim 128), and the
+//    second group is skipped when a row's last tile has at most 8 tokens.
+//    Boxes land with the 128-byte swizzle, so ldmatrix reads of 8 rows at the
+//    same column hit 8 different bank groups without padding.  The q rows of
+//    the next segment are copied (plain bulk copy) into a staging buffer
+//    while the current segment is still being consumed.
 //  * Math on tensor cores.  One consumer warp per kv head.  With 16 keys per
 //    tile and the G q heads of the kv head padded to 8, the scores are one
 //    m16n8 tile: S^T (keys x heads) = K (keys x D) . q^T, and the output is
@@ -37,8 +46,7 @@
 //    relative for bf16, 2^-22 for fp16) and both parts are multiplied, so
 //    the products keep at least 16 significant bits while K and V enter
 //    exactly.  P goes from the score-fragment layout to the operand
-//    layout with movmatrix transposes.  K and V rows get a 16-byte pad so
-//    ldmatrix reads are free of bank conflicts.
+//    layout with movmatrix transposes.
 //  * Stale slots (tail of the last page, slots never copied) never reach the
 //    output: their scores are replaced by -inf before the max and their V rows
 //    are zeroed in shared memory before the value product.
@@ -178,9 +186,13 @@ __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse,
 }
 
 template <int D, int G, bool FUSED, typename E>
-__global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __grid_constant__ AttnParams p) {
   constexpr int KSTEPS = D / 16;  // k-steps of the score product = m-tiles of the value product
-  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int HALVES = D / 64;  // 64-element (128-byte) column blocks of a K or V row
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // the swizzled tensor copies want 1024-byte aligned boxes: every offset of
+  // the plan is taken from the first 1024-byte boundary (the plan reserves it)
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hc = p.Hc, S = p.stages;
   const int c = blockIdx.x, gy = blockIdx.y;
@@ -267,6 +279,10 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
   if (warp == Hc && c < n_eff) {
     win = tile_page(t0_pre + lane);
     nxt = tile_page(t0_pre + 32 + lane);
+    // the tensor-map descriptors live in the launch parameters, not in memory
+    // the previous kernel writes: fetch them before the wait as well
+    if (lane == 0) prefetch_tensormap(&p.tmap_k);
+    if (lane == 1) prefetch_tensormap(&p.tmap_v);
   }
   pdl_wait();
 
@@ -346,14 +362,32 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
     // and the page ids come from a 32-tile window that is loaded (one
     // coalesced load per lane) a whole window ahead of its use.
     const int h0 = gy * Hc;
-    const unsigned char* kbase =
-        reinterpret_cast<const unsigned char*>(p.k_cache + static_cast<long long>(h0) * p.head_stride);
-    const unsigned char* vbase =
-        reinterpret_cast<const unsigned char*>(p.v_cache + static_cast<long long>(h0) * p.head_stride);
-    // heads of a token slot contiguous (token-major pages): one copy per token
-    // row; otherwise (head-major pages) one copy per (token, head)
-    const bool heads_contig = p.head_stride == D;
-    const long long head_bytes = 2LL * p.head_stride;
+    // The tile's copies are boxes of box_heads heads x 8 tokens x 128 bytes:
+    // for K and for V, per 64-element column block hf, per 8-token group g
+    // and per group of box_heads heads.  Box j lands at [hf][g][head][token]
+    // in the K or V half of the stage; lane l issues boxes l and l + 32.  The
+    // same boxes serve token-major and head-major pages (the tensor map holds
+    // the strides).  Group g = 1 is skipped when the tile has <= 8 tokens.
+    const int HG_BOX = Hc / p.box_heads;  // head groups per (column block, token group)
+    const int NB = HALVES * 2 * HG_BOX;   // boxes of K (and of V) per tile
+    int bx_g[2], bx_hf[2], bx_head[2];
+    const void* bx_map[2];
+    uint32_t bx_off[2];
+    bool bx_on[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = lane + 32 * u;
+      bx_on[u] = j < 2 * NB;
+      const int kv = j >= NB ? 1 : 0, rem = j - kv * NB;
+      const int hf = rem / (2 * HG_BOX), rem2 = rem - hf * 2 * HG_BOX;
+      const int g = rem2 / HG_BOX, hq = rem2 - g * HG_BOX;
+      bx_g[u] = g;
+      bx_hf[u] = hf;
+      bx_head[u] = h0 + hq * p.box_heads;
+      bx_map[u] = kv ? static_cast<const void*>(&p.tmap_v) : static_cast<const void*>(&p.tmap_k);
+      bx_off[u] = static_cast<uint32_t>(kv * (p.stage_bytes / 2) + hf * Hc * 2048 + g * Hc * 1024 +
+                                        hq * p.box_heads * 1024);
+    }
     long long wb = t0;
     int b = b0;
     long long rt0 = cum[b], rt1 = cum[b + 1];
@@ -361,7 +395,6 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
     int stage = 0, round = 0, nseg = 0;
     long long issued = 0;
     bool aborted = false;
-    const int r = lane & 15;
     for (long long t = t0; t < t1; ++t, ++issued) {
       bool new_seg = (t == t0);
       if (t > t0 && ++tin_page == tpp) tin_page = 0;
@@ -410,28 +443,21 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         }
         ++nseg;
       }
-      // source and destination of this lane's row copy, and the append slot
+      // the box coordinates of this tile and the append slot (the new token's
+      // row arrives as whatever the cache slot holds; the consumers overwrite
+      // it with the rotated key and v_new)
       const long long page_off = static_cast<long long>(page) * p.page_stride;
-      const void* src;
-      bool contig = heads_contig;
-      if (FUSED && last_of_row && r == nvalid - 1) {
-        // the new token: raw k (rotated by the consumers) and v straight from the inputs
-        const long long nrow = (static_cast<long long>(b) * p.Hkv + h0) * D;
-        src = lane < 16 ? static_cast<const void*>(p.k_new + nrow) : static_cast<const void*>(p.v_new + nrow);
-        contig = true;
-      } else {
-        const long long off = 2LL * (page_off + static_cast<long long>(tin_page * kTile + r) * p.token_stride);
-        src = (lane < 16 ? kbase : vbase) + off;
-      }
+      const int tokc = tin_page * kTile;
+      const bool two_groups = nvalid > 8;
       const uint32_t st = smem_addr(smem) + static_cast<uint32_t>(stage) * p.stage_bytes;
-      const uint32_t dst = lane < 16 ? st + r * p.k_row_bytes : st + kTile * p.k_row_bytes + r * p.v_row_bytes;
       long long meta_val = -1;
       if constexpr (FUSED) {
         if (last_of_row && page_ok)
           meta_val = page_off + static_cast<long long>(tin_page * kTile + nvalid - 1) * p.token_stride +
                      static_cast<long long>(h0) * p.head_stride;
       }
-      const uint32_t tx = static_cast<uint32_t>(nvalid) * 2u * p.row_copy_bytes;
+      // bytes of the boxes issued: both token groups, or the first only
+      const uint32_t tx = static_cast<uint32_t>(two_groups ? p.stage_bytes : p.stage_bytes / 2);
 
       if (issued >= S && !mbar_wait(empty0 + 8 * stage, (round - 1) & 1)) {
         if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
@@ -449,12 +475,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
         mbar_arrive_expect_tx(fb, tx);
       }
       __syncwarp();
-      if (r < nvalid) {
-        if (contig) {
-          bulk_g2s(dst, src, p.row_copy_bytes, fb);
-        } else {
-          for (int hh = 0; hh < p.Hc; ++hh)
-            bulk_g2s(dst + hh * D * 2, static_cast<const unsigned char*>(src) + hh * head_bytes, D * 2, fb);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (bx_on[u] && (two_groups || bx_g[u] == 0)) {
+          const int tk = tokc + 8 * bx_g[u];
+          const int c1 = p.tm_tok_dim == 1 ? tk : bx_head[u], c2 = p.tm_tok_dim == 1 ? bx_head[u] : tk;
+          tma_load_4d(st + bx_off[u], bx_map[u], bx_hf[u] * 64, c1, c2, page, fb);
         }
       }
       if (++stage == S) {
@@ -477,9 +503,22 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
   const int h = gy * Hc + w;     // kv head
   const int g4 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
   const float NEG_INF = __int_as_float(0xff800000);
-  // ldmatrix row/column of this lane: K tile (keys x dims) and V tile (transposed)
-  const int ka_row = (lane & 7) + 8 * ((lane >> 3) & 1), ka_col = 8 * (lane >> 4);
-  const int va_row = (lane & 7) + 8 * (lane >> 4), va_col = 8 * ((lane >> 3) & 1);
+  // ldmatrix row (key) and 16-byte column chunk of this lane: K tile (keys x
+  // dims; k-step k reads chunk 2k + (lane >> 4)) and V tile (read transposed;
+  // m-tile mt reads chunk 2 mt + ((lane >> 3) & 1)).  In the swizzled boxes,
+  // chunk c of row r sits at chunk c ^ (r & 7); as 2k is even, the physical
+  // chunk is (2k mod 8) ^ ksw with ksw = (lane >> 4) ^ (r & 7).
+  const int ka_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int va_row = (lane & 7) + 8 * (lane >> 4);
+  const int ksw = (lane >> 4) ^ (ka_row & 7), vsw = ((lane >> 3) & 1) ^ (va_row & 7);
+  // Stage layout of K (and then V): [64-column block][8-token group][head][8 tokens][128 B];
+  // row r of head w of a column block is at row_off(r) + w * 1024.
+  const uint32_t half_bytes = static_cast<uint32_t>(Hc) * 2048u;  // one 64-column block of all heads
+  auto row_off = [&](int r) -> uint32_t {
+    return static_cast<uint32_t>((r >> 3) * Hc * 1024 + w * 1024 + (r & 7) * 128);
+  };
+  const uint32_t k_lane = row_off(ka_row);
+  const uint32_t v_lane = static_cast<uint32_t>(p.stage_bytes / 2) + row_off(va_row);
 
   // fused: per-lane RMSNorm weights (q: the lane's fixed elements in step (1) of
   // the fragment build; k: the lane's pairs in the append patch)
@@ -527,8 +566,17 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
   float acc[KSTEPS][4];                   // O^T fragments: dims mt*16 + g4 (+8), heads 2 t4 (+1)
   float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
   float rc[(D / 2 + 31) / 32], rs[(D / 2 + 31) / 32];  // fused: RoPE row for the new key
+  // fused: the new token's raw key (pair j of this lane: first element in the
+  // low half, partner in the high half) and this lane's 16 bytes of v_new,
+  // loaded when a segment that holds the row's last tile starts
+  uint32_t knew[KPAIRS];
+  uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < KPAIRS; ++j) knew[j] = 0u;
   (void)rc;
   (void)rs;
+  (void)knew;
+  (void)vnew;
 
   int b = b0;
   long long rt0 = cum[b], rt1 = cum[b + 1];
@@ -633,6 +681,19 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
           rc[j] = i < D / 2 ? cs[i] : 0.f;
           rs[j] = i < D / 2 ? cs[D / 2 + i] : 0.f;
         }
+        if (se == rt1) {
+          // this segment ends the row: fetch the new key and value now, used at its last tile
+          const uint16_t* kn = p.k_new + (static_cast<long long>(b) * p.Hkv + h) * D;
+#pragma unroll
+          for (int j = 0; j < KPAIRS; ++j) {
+            const int i = lane + 32 * j;
+            if (i < D / 2)
+              knew[j] = ilv ? *reinterpret_cast<const uint32_t*>(kn + 2 * i)
+                            : static_cast<uint32_t>(kn[i]) | (static_cast<uint32_t>(kn[i + D / 2]) << 16);
+          }
+          if (lane < D / 8)
+            vnew = *reinterpret_cast<const uint4*>(p.v_new + (static_cast<long long>(b) * p.Hkv + h) * D + lane * 8);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty);
@@ -650,31 +711,31 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
       *abort_flag = 1;
       return;
     }
-    unsigned char* kst = smem + static_cast<long long>(stage) * p.stage_bytes + w * D * 2;
-    unsigned char* vst = smem + static_cast<long long>(stage) * p.stage_bytes + kTile * p.k_row_bytes + w * D * 2;
+    // this stage: K boxes [D/64][2][Hc][8][128 B], then V boxes, all swizzled
+    unsigned char* stg = smem + static_cast<long long>(stage) * p.stage_bytes;
+    unsigned char* vst = stg + p.stage_bytes / 2;
     bool touched = false;
 
     if constexpr (FUSED) {
       if (t == rt1 - 1) {
-        // the new token (row nvalid-1): rotate its key in place, then append k and v to the cache
-        uint16_t* kr = reinterpret_cast<uint16_t*>(kst + (nvalid - 1) * p.k_row_bytes);
+        // the new token (row nvalid-1 of the tile, which the box copy filled
+        // with whatever the cache slot held): (RMSNorm and) rotate its key,
+        // write key and value into the tile row and append them to the cache
+        const int rr = nvalid - 1;
+        unsigned char* krow = stg + row_off(rr);   // + column block * half_bytes
+        unsigned char* vrow = vst + row_off(rr);
+        // byte offset of element e of row rr within this head's boxes
+        auto elem_off = [&](int e) -> uint32_t {
+          return static_cast<uint32_t>(e >> 6) * half_bytes + (((((e >> 3) & 7) ^ (rr & 7))) << 4) + (e & 7) * 2;
+        };
         const long long dst = meta[stage];
         float kx[KPAIRS], ky[KPAIRS];
         float ss = 0.f;
 #pragma unroll
         for (int j = 0; j < KPAIRS; ++j) {
-          const int i = lane + 32 * j;
-          kx[j] = ky[j] = 0.f;
-          if (i < D / 2) {
-            if (ilv) {
-              const float2 xy = E::to_float2(*reinterpret_cast<const uint32_t*>(kr + 2 * i));
-              kx[j] = xy.x;
-              ky[j] = xy.y;
-            } else {
-              kx[j] = E::to_float(kr[i]);
-              ky[j] = E::to_float(kr[i + D / 2]);
-            }
-          }
+          const float2 xy = E::to_float2(knew[j]);  // zero for lanes without a pair
+          kx[j] = xy.x;
+          ky[j] = xy.y;
           ss += kx[j] * kx[j] + ky[j] * ky[j];
         }
         if (p.k_norm_w) {
@@ -688,7 +749,6 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
             ky[j] = wk[2 * j + 1] * (ky[j] * r);
           }
         }
-        __syncwarp();
 #pragma unroll
         for (int j = 0; j < KPAIRS; ++j) {
           const int i = lane + 32 * j;
@@ -698,12 +758,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
             uint16_t* cache_row = p.k_cache_w + dst + static_cast<long long>(w) * p.head_stride;
             if (ilv) {
               const uint32_t xy = E::pack2(xr, yr);
-              *reinterpret_cast<uint32_t*>(kr + 2 * i) = xy;
+              *reinterpret_cast<uint32_t*>(krow + elem_off(2 * i)) = xy;
               if (dst >= 0) *reinterpret_cast<uint32_t*>(cache_row + 2 * i) = xy;
             } else {
               const uint16_t xb = E::bits(xr), yb = E::bits(yr);
-              kr[i] = xb;
-              kr[i + D / 2] = yb;
+              *reinterpret_cast<uint16_t*>(krow + elem_off(i)) = xb;
+              *reinterpret_cast<uint16_t*>(krow + elem_off(i + D / 2)) = yb;
               if (dst >= 0) {
                 cache_row[i] = xb;
                 cache_row[i + D / 2] = yb;
@@ -711,18 +771,23 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
             }
           }
         }
-        if (dst >= 0 && lane < D / 8) {
-          const uint4 vv = *reinterpret_cast<const uint4*>(vst + (nvalid - 1) * p.v_row_bytes + lane * 16);
-          *reinterpret_cast<uint4*>(p.v_cache_w + dst + static_cast<long long>(w) * p.head_stride + lane * 8) = vv;
+        if (lane < D / 8) {
+          *reinterpret_cast<uint4*>(vrow + elem_off(lane * 8)) = vnew;
+          if (dst >= 0)
+            *reinterpret_cast<uint4*>(p.v_cache_w + dst + static_cast<long long>(w) * p.head_stride + lane * 8) = vnew;
         }
         touched = true;
       }
     }
     if (nvalid < kTile) {
       // stale V rows would meet p = 0 in the product; make them exact zeros
-      constexpr int CH = D / 8;
-      for (int r = nvalid + lane / CH; r < kTile; r += 32 / CH)
-        *reinterpret_cast<uint4*>(vst + r * p.v_row_bytes + (lane % CH) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      // (whole rows, so the swizzle does not matter)
+      constexpr int CH = D / 8;  // 16-byte chunks per row, over the column blocks
+      for (int r = nvalid + lane / CH; r < kTile; r += 32 / CH) {
+        const int ch = lane % CH;
+        *reinterpret_cast<uint4*>(vst + (ch >> 3) * half_bytes + row_off(r) + (ch & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
       touched = true;
     }
     if (touched) __syncwarp();
@@ -730,11 +795,11 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
     // ---- scores S^T = K q^T on tensor cores ----------------------------------
     float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
     {
-      const uint32_t ka = smem_addr(kst + ka_row * p.k_row_bytes + ka_col * 2);
+      const uint32_t ka = smem_addr(stg) + k_lane;
 #pragma unroll
       for (int k = 0; k < KSTEPS; ++k) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(ka + 32 * k, a0, a1, a2, a3);
+        ldsm_x4(ka + (k >> 2) * half_bytes + ((((2 * k) & 7) ^ ksw) << 4), a0, a1, a2, a3);
         E::mma(sh, a0, a1, a2, a3, qh[k][0], qh[k][1]);
         E::mma(sl, a0, a1, a2, a3, ql[k][0], ql[k][1]);
       }
@@ -778,11 +843,11 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const AttnP
 
     // ---- values O^T += V^T P^T on tensor cores ---------------------------------
     {
-      const uint32_t vaddr = smem_addr(vst + va_row * p.v_row_bytes + va_col * 2);
+      const uint32_t vaddr = smem_addr(stg) + v_lane;
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vaddr + 32 * mt, a0, a1, a2, a3);
+        ldsm_x4_t(vaddr + (mt >> 2) * half_bytes + ((((2 * mt) & 7) ^ vsw) << 4), a0, a1, a2, a3);
         E::mma(acc[mt], a0, a1, a2, a3, bh0, bh1);
         E::mma(acc[mt], a0, a1, a2, a3, bl0, bl1);
       }

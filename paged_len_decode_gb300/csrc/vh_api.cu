@@ -10,6 +10,8 @@
 #include <cstdlib>
 #include <mutex>
 
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include "../../include/vh.h"
 #include "vh_kernels.h"
 
@@ -102,10 +104,10 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   int stages = 0;
   for (;;) {
     p.Hc = hc;
-    p.row_copy_bytes = hc * p.D * 2;
-    p.k_row_bytes = p.row_copy_bytes + 16;  // 16-byte pad: conflict-free ldmatrix rows
-    p.v_row_bytes = p.row_copy_bytes + 16;
-    p.stage_bytes = static_cast<int>(align_up(16 * static_cast<size_t>(p.k_row_bytes + p.v_row_bytes), 128));
+    // K and V of a 16-token tile, as swizzled 16 x 128-byte boxes (no padding
+    // needed for conflict-free ldmatrix): 2 * 16 * Hc * D * 2 bytes, a
+    // multiple of 2048 so every box stays 1024-byte aligned
+    p.stage_bytes = 2 * 16 * hc * p.D * 2;
     const size_t hg = static_cast<size_t>(hc) * p.G;
     // staged q rows, contiguous: one bulk copy per segment
     p.q_row_bytes = fused ? p.D * 2 : p.D * 4;
@@ -113,7 +115,8 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
     p.q_bytes = static_cast<int>(hg * p.q_row_bytes + (fused ? p.D * 4 : 0));
     const size_t qs_bytes = fused ? static_cast<size_t>(hc) * p.G * (p.D * 4 + 32) : 0;
     fixed = align_up(p.q_bytes, 128) + align_up(qs_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
-            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256;
+            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256 +
+            1024 /* alignment of the base */;
     stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
     if (stages >= 3 || hc == 1) break;
     int next = hc - 1;
@@ -140,7 +143,8 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   off += 8 * static_cast<size_t>(stages);
   p.bar_off = static_cast<int>(align_up(off, 16));
   off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 4) + 48 * 4;
-  p.smem_bytes = static_cast<int>(align_up(off, 128));
+  // + up to 1024 bytes that the kernel skips to align its base for the boxes
+  p.smem_bytes = static_cast<int>(align_up(off, 128) + 1024);
   p.min_tiles = kMinTilesPerCta;
   return static_cast<size_t>(p.smem_bytes) <= budget;
 }
@@ -171,6 +175,68 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int D, int N) {
   w.o = w.lse + align_up(static_cast<size_t>(N) * 2 * Hq * 4, 256);
   w.total = w.o + static_cast<size_t>(N) * 2 * Hq * D * 4;
   return w;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor maps of the K and V caches for the attention kernel's tile copies:
+// 4-D tensors of 16-bit elements (dimension 0 = head_dim, 3 = page) with the
+// 128-byte swizzle, boxes of 64 elements x 8 tokens x box_heads heads, which
+// land in shared memory as [head][token][128 bytes].  Preferred: dimension
+// 1 = token, 2 = head and box_heads = Hc, so a tile is two boxes (token
+// groups) per 64-column block of K and of V.  If the encoder rejects that order (the strides of
+// token-major pages decrease from dimension 1 to 2), dimensions 1 and 2 are
+// token and head in increasing stride order and each box holds one head.
+// Sets p.tm_tok_dim and p.box_heads.  Returns false if no encoding is accepted.
+bool encode_cache_maps(AttnParams& p) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  // L2 fill granularity of the tile reads (VH_TMA_L2 = 0, 64, 128 or 256 bytes, for tuning)
+  CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  switch (env_int("VH_TMA_L2", 256)) {
+    case 0: promo = CU_TENSOR_MAP_L2_PROMOTION_NONE; break;
+    case 64: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_64B; break;
+    case 128: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B; break;
+    default: break;
+  }
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  auto encode = [&](bool tok_first, cuuint32_t heads) -> bool {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.D), static_cast<cuuint64_t>(tok_first ? p.P : p.Hkv),
+                                static_cast<cuuint64_t>(tok_first ? p.Hkv : p.P),
+                                static_cast<cuuint64_t>(p.num_pages)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(2 * (tok_first ? p.token_stride : p.head_stride)),
+                                   static_cast<cuuint64_t>(2 * (tok_first ? p.head_stride : p.token_stride)),
+                                   static_cast<cuuint64_t>(2 * p.page_stride)};
+    const cuuint32_t box[4] = {64, tok_first ? 8u : 1u, tok_first ? heads : 8u, 1};
+    for (int kv = 0; kv < 2; ++kv) {
+      CUtensorMap* m = kv ? &p.tmap_v : &p.tmap_k;
+      void* base = const_cast<uint16_t*>(kv ? p.v_cache : p.k_cache);
+      if (enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    }
+    p.tm_tok_dim = tok_first ? 1 : 2;
+    p.box_heads = static_cast<int>(heads);
+    return true;
+  };
+  if (env_int("VH_TMA_BOX_HEADS", 0) != 1 && encode(true, static_cast<cuuint32_t>(p.Hc))) return true;
+  return encode(p.token_stride <= p.head_stride, 1);
 }
 
 bool too_many_tiles(int B, int max_pages_per_seq, int P) {
@@ -334,6 +400,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
   p.D = D;
   p.P = page_size;
   if (!plan_attn(p, *dev, false)) return VH_EINVAL;
+  if (!encode_cache_maps(p)) return VH_EINVAL;
   p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
   const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
@@ -440,6 +507,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   p.D = D;
   p.P = page_size;
   if (!plan_attn(p, *dev, true)) return VH_EINVAL;
+  if (!encode_cache_maps(p)) return VH_EINVAL;
   p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
   const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
@@ -538,6 +606,7 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
   p.D = D;
   p.P = page_size;
   if (!plan_attn(p, *dev, false)) return VH_EINVAL;
+  if (!encode_cache_maps(p)) return VH_EINVAL;
   p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
   const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (w.total > static_cast<size_t>(VH_STATIC_SCRATCH_BYTES)) return VH_ESCRATCH;

@@ -78,6 +78,31 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Tiled tensor copy of one 4-D box from global memory, described by a tensor
+// map (in kernel-parameter space), into this CTA's shared memory; completion
+// is signalled as a transaction count on mbarrier `bar`.  c0 is the innermost
+// coordinate (in elements; c0 * element size must be a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a box stored with the
+// 128-byte swizzle (rows of 128 bytes, box base 1024-byte aligned): the chunk
+// index is XORed with the row index modulo 8, so the 8 rows an ldmatrix reads
+// at the same logical chunk fall in 8 different bank groups.
+__device__ __forceinline__ uint32_t swz128(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
 // Two bf16 packed in a 32-bit word -> two exact fp32 values (low half first).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap (the type only: the library does not link the driver library)
 #include <cuda_runtime.h>
 
 namespace vh {
@@ -35,8 +36,14 @@ struct RopeAppendParams {
 };
 
 // Shared-memory plan of the attention kernel (byte offsets from the dynamic
-// shared-memory base) and the split plan parameters.
+// shared-memory base, rounded up to 1024 bytes) and the split plan parameters.
 struct AttnParams {
+  // K and V caches as 4-D tensors (head_dim, then token and head in stride
+  // order, then page) with 64-element x 16-token boxes and the 128-byte swizzle
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  int tm_tok_dim;              // tensor-map dimension of the token index (1 or 2; the head index is the other)
+  int box_heads;               // kv heads per box: Hc (one box per 64-column block) or 1
   // attention over the cache (both kernels)
   const float* q_rot;          // [B][Hq][D] fp32 rotated q (three-call path)
   const uint16_t* k_cache;
@@ -78,10 +85,7 @@ struct AttnParams {
   int N;                       // CTAs per group (gridDim.x)
   int stages;
   int min_tiles;               // lower bound on tiles per CTA when the work list is short
-  int k_row_bytes;             // padded shared-memory stride of a K row (token)
-  int v_row_bytes;             // padded shared-memory stride of a V row
-  int row_copy_bytes;          // bytes copied per token row (Hc * D * 2)
-  int stage_bytes;
+  int stage_bytes;             // K then V of one tile: [D/64][Hc][16 tokens][128 B swizzled] each
   int q_bytes;                 // bytes reserved for the q staging buffer
   int q_row_bytes;             // padded shared-memory stride of a staged q row
   int q_tx_bytes;              // bytes the q copies deliver
