@@ -59,8 +59,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="16-bit element type of q, k, v, the cache and the output")
-    ap.add_argument("--layout", default="NHD", choices=["NHD", "HND"],
-                    help="page layout: token-major [NP,2,P,Hkv,D] or head-major [NP,2,Hkv,P,D]")
+    ap.add_argument("--layout", default=None, choices=["NHD", "HND", "CONTIG"],
+                    help="cache layout: token-major pages [NP,2,P,Hkv,D], head-major pages "
+                         "[NP,2,Hkv,P,D] or one contiguous cache per row [2,B,Hkv,P,D] "
+                         "(default: the workload's)")
     ap.add_argument("--interleaved", action="store_true",
                     help="interleaved (2i, 2i+1) RoPE pairing instead of rotate-half")
     ap.add_argument("--qk-norm", action="store_true",
@@ -214,8 +216,12 @@ class Setup:
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.pool_bytes = inp.pool.numel() * 2
         if self.layer_inputs:
+            # one pool per layer; small layer sets are repeated (fresh copies)
+            # until they exceed 4x L2, and a step cycles through them
+            reps = replicas or max(1, math.ceil(4 * self.l2 / (self.L * self.pool_bytes)))
             self.pools = [li.pool for li in self.layer_inputs]
-            self.R = self.L
+            self.pools += [li.pool.clone() for _ in range(reps - 1) for li in self.layer_inputs]
+            self.R = self.L * reps
         else:
             self.R = replicas or max(2, math.ceil(4 * self.l2 / self.pool_bytes))
             self.pools = [inp.pool] + [inp.pool.clone() for _ in range(self.R - 1)]
@@ -232,7 +238,7 @@ class Setup:
             self.norm.update({"q_norm_w": w, "k_norm_w": w, "norm_eps": 1e-6})
 
     def inputs(self, r):
-        return self.layer_inputs[r] if self.layer_inputs else self.inp
+        return self.layer_inputs[r % self.L] if self.layer_inputs else self.inp
 
     def step_bytes(self) -> dict:
         if not self.layer_inputs:
@@ -241,8 +247,10 @@ class Setup:
         return {k: (sum(x[k] for x in per) if k != "active" else per[0][k]) for k in per[0]}
 
     def kv(self, r):
-        """[NP, P, Hkv, D] K and V views of pool r (strided for head-major pages)."""
+        """[NP, P, Hkv, D] K and V views of pool r (strided unless token-major)."""
         pool = self.pools[r]
+        if self.inp.layout == "CONTIG":
+            return pool[0].transpose(1, 2), pool[1].transpose(1, 2)
         if self.inp.layout == "HND":
             return pool[:, 0].transpose(1, 2), pool[:, 1].transpose(1, 2)
         return pool[:, 0], pool[:, 1]
@@ -251,13 +259,13 @@ class Setup:
         s = src or self.inputs(r)
         k, v = self.kv(r)
         self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v,
-                                s.page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl, **self.norm)
+                                s.api_page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl, **self.norm)
 
     def three(self, r):
         i = self.inputs(r)
         k, v = self.kv(r)
         self.vh.decode_step(i.q, i.k_new, i.v_new, self.cos_sin, k, v,
-                            i.page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3, **self.norm)
+                            i.api_page_table, i.seq_lens, i.active, self.q_rot, self.out, self.ws3, **self.norm)
 
 
 def run_ncu_case(args):
@@ -428,9 +436,10 @@ def run_ours(args, rank, world):
                            "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
                            "PDL between launches",
                    "layers": L, "qk_norm": bool(args.qk_norm), "rope": "interleaved" if args.interleaved
-                   else "rotate-half", "elements": args.dtype, "pages": args.layout,
+                   else "rotate-half", "elements": args.dtype, "pages": s.inp.layout,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": (f"{L} KV pools, one per layer ({L * s.pool_bytes / 1e9:.1f} GB)" if L > 1 else
+                   "l2": (f"{R} KV pools, one per layer call ({R // L} sets of {L} layers, "
+                          f"{R * s.pool_bytes / 1e6:.0f} MB" if L > 1 else
                           f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB")
                          + f" >= 4x L2 {s.l2 / 1e6:.0f} MB): inputs larger than L2",
                    "ctas": s.n_ctas},
@@ -440,7 +449,7 @@ def run_ours(args, rank, world):
                      "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(step_gbs / peak, 4), "traffic": (recorded_traffic(args.workload)
                                                     if args.dtype == "bf16" and not args.interleaved
-                                                    and args.layout == "NHD" else None),
+                                                    and s.inp.layout == "NHD" else None),
                      "peak_kind": peak_kind, "ms_per_launch": round(ms_step / L, 6),
                      "algorithmic_bytes_per_launch": by["step"] // L},
         "three_call": {"ms_per_step": round(ms_three, 6),

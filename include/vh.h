@@ -63,11 +63,22 @@
  *     *err_flag when err_flag is not NULL.  The caller reads it later.
  *
  * Shapes: B rows, Hq q heads, Hkv kv heads (Hq % Hkv == 0, G = Hq / Hkv
- * in {1, 2, 4, 8}), head dim D in {64, 128}, page size P a multiple of 16
- * (16 <= P <= 1024), 1 <= B <= 65535.  seq_len counts the token being
- * appended: row b attends over logical slots 0 .. seq_lens[b]-1, and the new
- * token is slot seq_lens[b]-1, i.e. page page_table[b][(L-1)/P], offset
- * (L-1) % P.  page_table is int32 [B][max_pages_per_seq], row-major.
+ * in {1, 2, 4, 8}), head dim D in {64, 128}, page size 1 <= P <= 1024, a
+ * multiple of 16 when max_pages_per_seq > 1, 1 <= B <= 65535.  seq_len
+ * counts the token being appended: row b attends over logical slots
+ * 0 .. seq_lens[b]-1, and the new token is slot seq_lens[b]-1, i.e. page
+ * page_table[b][(L-1)/P], offset (L-1) % P.  page_table is int32
+ * [B][max_pages_per_seq], row-major.
+ *
+ * Contiguous caches: page_table may be NULL (all calls but the one without a
+ * workspace); row b's logical page j is then physical page
+ * b * max_pages_per_seq + j (B * max_pages_per_seq <= num_pages).  With
+ * max_pages_per_seq = 1 and P = the cache length, this is a per-request
+ * contiguous cache such as the Fast AR cache of the vLLM-Omni blog's Fish
+ * Speech section ("Fast AR buffer reuse": K/V preallocated per layer as
+ * [batch][kv head][position][head_dim], one new token written and read in
+ * place per step): page_stride = Hkv*P*D, token_stride = D, head_stride =
+ * P*D, k_cache and v_cache the layer's two tensors.
  */
 #ifndef VH_H
 #define VH_H
@@ -123,7 +134,8 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
  *        NULL skips it.  16-byte aligned.  norm_eps >= 0.
  * k_cache, v_cache, page_stride, token_stride, head_stride: the layer's paged cache
  * num_pages: pages in the pool, used only to bounds-check page ids (> 0)
- * page_table int32 [B][max_pages_per_seq]; seq_lens, active int32 [B]
+ * page_table int32 [B][max_pages_per_seq], or NULL (contiguous cache, see above);
+ *        seq_lens, active int32 [B]
  * q_rot  float [B][Hq][D] out: rotated q in fp32 (rows with active == 0
  *        are not written)
  * err_flag int32* or NULL
@@ -135,7 +147,7 @@ int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void*
  * with VH_FLAG_ROPE_INTERLEAVED (the GPT-J pairing).  Rows with
  * active == 0 write nothing.  Precondition (not checked): live rows own
  * disjoint append slots.
- * Errors: VH_EINVAL (NULL pointer other than positions/err_flag, bad shape,
+ * Errors: VH_EINVAL (NULL pointer other than positions/err_flag/page_table/norm weights, bad shape,
  * max_pos < 1, num_pages < 1, max_pages_per_seq < 1, unknown flags),
  * VH_EALIGN (a pointer or a stride not 16-byte aligned), VH_ECUDA. */
 int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,

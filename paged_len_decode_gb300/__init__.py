@@ -8,7 +8,8 @@ library is missing or a call fails, an exception is raised.
 
 The 16-bit element type (bf16 or fp16) is the cache's dtype; q, k_new,
 v_new and out must have the same dtype, and VH_FLAG_FP16 is passed for fp16.
-`interleaved=True` selects the (2i, 2i+1) RoPE pairing.
+`interleaved=True` selects the (2i, 2i+1) RoPE pairing.  page_table=None
+selects a contiguous cache (row b owns pages b*m .. b*m+m-1, m = pages / B).
 
 Functions mirror the C entry points by name:
     vh_rope_table, vh_rope_kv_append, vh_decode_num_ctas,
@@ -134,6 +135,16 @@ def _cache_view(k_cache: torch.Tensor, v_cache: torch.Tensor, bf16_only: bool = 
             k_cache.stride(0), k_cache.stride(1), k_cache.stride(2), NP, P, Hkv, D)
 
 
+def _table(page_table, B: int, NP: int):
+    """(pointer, max_pages_per_seq) of the page table; None means a contiguous
+    cache whose row b owns pages b * m .. b * m + m - 1, m = NP // B."""
+    if page_table is None:
+        if NP % B != 0:
+            raise ValueError("without a page table the cache must hold a whole number of pages per row")
+        return None, NP // B
+    return _contig(page_table, torch.int32, "page_table"), page_table.shape[1]
+
+
 def _elem_flags(k_cache: torch.Tensor, interleaved: bool = False) -> int:
     return (VH_FLAG_FP16 if k_cache.dtype == torch.float16 else 0) | (VH_FLAG_ROPE_INTERLEAVED if interleaved else 0)
 
@@ -167,7 +178,7 @@ def vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, se
         _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
-        kp, vp, ps, ts, hs, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        kp, vp, ps, ts, hs, NP, *_table(page_table, B, NP),
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(q_rot, torch.float32, "q_rot"),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
@@ -195,8 +206,7 @@ def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, 
     if Dc != D or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q_rot, out and the cache")
     _check(lib.vh_paged_decode_attn(
-        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, hs, NP,
-        _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, hs, NP, *_table(page_table, B, NP),
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(out, k_cache.dtype, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
@@ -250,7 +260,7 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
         _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
         cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
-        kp, vp, ps, ts, hs, NP, _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        kp, vp, ps, ts, hs, NP, *_table(page_table, B, NP),
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(out, et, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),

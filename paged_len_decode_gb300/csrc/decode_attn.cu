@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     b0_pre = lo;
   }
   // The producer's first page ids are read before the wait as well.
-  const int tpp = p.P / kTile;  // tiles per page
+  // tiles per page (P is a multiple of 16, or a row has one page of any size)
+  const int tpp = (p.P + kTile - 1) / kTile;
   auto tile_page = [&](long long tt) -> int {
     if (tt >= t1_pre) return 0;
     int lo = b0_pre, hi = p.B - 1;  // row of tile tt: first row with cum[row + 1] > tt
@@ -273,7 +274,9 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       if (cum[mid + 1] > tt) hi = mid; else lo = mid + 1;
     }
     const int tk = static_cast<int>(tt - cum[lo]);
-    return p.page_table[static_cast<long long>(lo) * p.max_pages_per_seq + tk / tpp];
+    const long long lp = static_cast<long long>(lo) * p.max_pages_per_seq + tk / tpp;
+    // no page table: a contiguous cache, row b's pages are b * max_pages_per_seq + j
+    return p.page_table ? p.page_table[lp] : static_cast<int>(lp);
   };
   int win = 0, nxt = 0;
   if (warp == Hc && c < n_eff) {

@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p
     return;
   }
   const int slot = L - 1;
-  const int page = p.page_table[static_cast<long long>(b) * p.max_pages_per_seq + slot / p.P];
+  const long long lp = static_cast<long long>(b) * p.max_pages_per_seq + slot / p.P;
+  const int page = p.page_table ? p.page_table[lp] : static_cast<int>(lp);  // no table: contiguous cache
   const bool page_ok = page >= 0 && page < p.num_pages;
   if (!page_ok && threadIdx.x == 0) flag_error(p.err_flag, VH_ERR_PAGE);
   const long long slot_off = static_cast<long long>(page) * p.page_stride +

@@ -69,8 +69,18 @@ bool valid_gqa(int Hq, int Hkv) {
 }
 
 bool valid_shape(int B, int Hq, int Hkv, int D, int P) {
-  return B >= 1 && B <= 65535 && valid_gqa(Hq, Hkv) && (D == 64 || D == 128) && P >= 16 &&
-         P <= 1024 && P % 16 == 0 && Hkv <= 1024;
+  return B >= 1 && B <= 65535 && valid_gqa(Hq, Hkv) && (D == 64 || D == 128) && P >= 1 && P <= 1024 &&
+         Hkv <= 1024;
+}
+
+// Pages of a row hold whole 16-token tiles, unless a row has a single page.
+bool valid_paging(int P, int max_pages_per_seq) {
+  return max_pages_per_seq >= 1 && (P % 16 == 0 || max_pages_per_seq == 1);
+}
+
+// Without a page table, row b's pages are b * max_pages_per_seq + j: they must exist.
+bool valid_table(const int32_t* page_table, int B, int max_pages_per_seq, int num_pages) {
+  return page_table != nullptr || static_cast<long long>(B) * max_pages_per_seq <= num_pages;
 }
 
 int env_int(const char* name, int dflt) {
@@ -279,8 +289,9 @@ int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                       const int32_t* seq_lens, const int32_t* active,
                       float* q_rot, int32_t* err_flag, unsigned flags,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !page_table || !seq_lens || !active ||
-      !q_rot || (flags & ~(VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0)
+  if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !seq_lens || !active || !q_rot ||
+      (flags & ~(VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0 || !valid_paging(page_size, max_pages_per_seq) ||
+      !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
       page_stride < 1 || token_stride < 1 || head_stride < 1 || too_many_tiles(B, max_pages_per_seq, page_size))
@@ -365,8 +376,9 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
                          vh_e16* out, float sm_scale, int num_ctas,
                          void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                          int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out ||
-      (flags & ~static_cast<unsigned>(VH_FLAG_FP16)) != 0)
+  if (!q_rot || !k_cache || !v_cache || !seq_lens || !active || !out ||
+      (flags & ~static_cast<unsigned>(VH_FLAG_FP16)) != 0 || !valid_paging(page_size, max_pages_per_seq) ||
+      !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
       token_stride < 1 || head_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
@@ -459,8 +471,9 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     vh_e16* out, float sm_scale, int num_ctas,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                     int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !page_table || !seq_lens || !active ||
-      !out || (flags & ~(VH_FLAG_PDL | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0)
+  if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !seq_lens || !active || !out ||
+      (flags & ~(VH_FLAG_PDL | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0 ||
+      !valid_paging(page_size, max_pages_per_seq) || !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
       page_stride < 1 || token_stride < 1 || head_stride < 1 || num_ctas < 0 || num_ctas > 65535 ||
@@ -576,7 +589,9 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
                                             const int32_t* seq_lens, const int32_t* active,
                                             vh_bf16* out, float sm_scale, int num_ctas, int32_t* err_flag,
                                             int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out) return VH_EINVAL;
+  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out ||
+      !valid_paging(page_size, max_pages_per_seq))
+    return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
       token_stride < 1 || num_ctas < 0 || num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) ||
       !(sm_scale == sm_scale))

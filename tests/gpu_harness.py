@@ -64,12 +64,12 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
     def step():
         for _ in range(repeat):
             if path == "fused":
-                v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
+                v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.api_page_table, g.seq_lens,
                                   g.active, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
                                   err_flag=err, pdl=pdl, q_norm_w=nq, k_norm_w=nk, norm_eps=eps,
                                   interleaved=interleaved)
             else:
-                v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.page_table, g.seq_lens,
+                v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.api_page_table, g.seq_lens,
                               g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
                               err_flag=err, q_norm_w=nq, k_norm_w=nk, norm_eps=eps, interleaved=interleaved)
 
@@ -148,9 +148,32 @@ def check_append(inp, ref, gpu_pool, rel=MIDPOINT_REL, interleaved=False):
     bad = diff & ~allowed
     assert not bad.any(), f"{int(bad.sum())} pool elements differ outside the midpoint exemption, " \
                           f"first at {torch.nonzero(bad)[0].tolist()}"
-    # and the differing exempt elements are one step of the element type apart
-    d = (a[diff] - b[diff]).abs()
-    assert (d == 1).all()
+    # and every differing element is the rounding of a value within the fp32
+    # error window of the exact rotated key: |gpu - exact| <= window + one step
+    # of the element type (near zero, after cancellation, that may be several
+    # bit patterns away, or the other sign)
+    bits_, qmin = _GRID[gpu_pool.dtype]
+    k = ref["k_pre"].double().abs()
+    if interleaved:
+        pair = k[..., 0::2] + k[..., 1::2]
+        scale = torch.stack([pair, pair], dim=-1).flatten(-2)
+    else:
+        h = k.shape[-1] // 2
+        pair = k[..., :h] + k[..., h:]
+        scale = torch.cat([pair, pair], dim=-1)
+    for bb in torch.nonzero(act).flatten().tolist():
+        L = int(lens[bb])
+        page, off = int(pt[bb, (L - 1) // inp.P]), (L - 1) % inp.P
+        dd = diff[page, 0, off]
+        if not dd.any():
+            continue
+        got = gpu_pool[page, 0, off].double()[dd]
+        exact = ref["k_rot"][bb][dd]
+        mag = torch.maximum(got.abs(), exact.abs())
+        e = torch.frexp(torch.where(mag > 0, mag, torch.ones_like(mag))).exponent
+        step = torch.ldexp(torch.ones_like(mag), (e - bits_).clamp(min=qmin))
+        assert ((got - exact).abs() <= rel * scale[bb][dd] + step).all(), \
+            f"row {bb}: an exempt element is further than the window from the exact key"
     return n, int(diff.sum())
 
 

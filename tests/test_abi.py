@@ -152,3 +152,21 @@ def test_rope_table_and_combine_argument_checks():
     assert v.lib.vh_decode_combine(FAKE, 1 << 30, ODD, 0, v.VH_FLAG_FP16, 4, 16, 8, 128, 16, None) == v.VH_EALIGN
     assert v.lib.vh_decode_workspace_bytes(4, 12, 8, 128, 16, 10) == 0
     assert v.lib.vh_decode_workspace_bytes(4, 16, 8, 128, 16, 152) > 0
+
+
+def test_contiguous_cache_arguments():
+    # no page table: the rows' pages b * max_pages_per_seq + j must exist
+    assert attn(pt=None, npages=3, mps=1) == v.VH_EINVAL          # B = 4 rows, 3 pages
+    assert attn(pt=None, npages=8, mps=2, P=11) == v.VH_EINVAL    # pages of 11 tokens need one page per row
+    assert attn(P=11, mps=2) == v.VH_EINVAL
+    assert attn(P=0) == v.VH_EINVAL
+    assert attn(P=1025) == v.VH_EINVAL
+
+
+def test_contiguous_cache_arguments_pass_host_checks_without_device():
+    # valid without a table: on a GPU-less machine the device query is the
+    # first check that fails (the fake pointers are never used)
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert attn(pt=None, npages=4, mps=1, P=11) == v.VH_ENODEV

@@ -66,10 +66,25 @@ def test_fp32_rotation_differs_from_float64_only_inside_the_window(dtype, interl
     c, s = _table_row(pos, D, inp.theta)
     k = inp.k_new.double()
     n_diff = 0
+    kp = k_pre.abs()
+    if interleaved:
+        pair = kp[..., 0::2] + kp[..., 1::2]
+        scale = torch.stack([pair, pair], dim=-1).flatten(-2)
+    else:
+        pair = kp[..., : D // 2] + kp[..., D // 2:]
+        scale = torch.cat([pair, pair], dim=-1)
     for order in ("plain", "fma_first", "fma_second"):
-        got = H.bits16(_emulated(k, c, s, interleaved, order).float().to(dtype))
+        val = _emulated(k, c, s, interleaved, order).float().to(dtype)
+        got = H.bits16(val)
         diff = got != want
         assert not (diff & ~mask).any(), f"{order}: {int((diff & ~mask).sum())} differences outside the window"
+        # the value test the GPU comparison applies to differing elements
+        g_, x_ = val.double()[diff], k_rot[diff]
+        mag = torch.maximum(g_.abs(), x_.abs())
+        bits, qmin = H._GRID[dtype]
+        e = torch.frexp(torch.where(mag > 0, mag, torch.ones_like(mag))).exponent
+        step = torch.ldexp(torch.ones_like(mag), (e - bits).clamp(min=qmin))
+        assert ((g_ - x_).abs() <= H.MIDPOINT_REL * scale[diff] + step).all()
         n_diff += int(diff.sum())
     # the window is narrow: a small share of all elements
     assert int(mask.sum()) < 0.01 * mask.numel()

@@ -15,7 +15,11 @@ The five workloads are the serving shapes of the Talker decode step:
   * "long"    -- 16 rows, 32 q / 8 kv heads, lengths uniform in [2048, 8192];
   * "high"    -- 256 rows, 32 q / 8 kv heads, pages of 64 tokens, lengths
                  log-uniform in [256, 4096], values N(0, 0.5), 28 layers that
-                 each own a separate KV pool.
+                 each own a separate KV pool;
+  * "fastar"  -- the Fast AR step: 64 rows, 16 q / 8 kv heads, head_dim 64,
+                 a contiguous per-request cache of 11 positions (10 residual
+                 codebooks + 1) per layer, 4 layers, every row at its last
+                 step (length 11).
 
 Layout of one layer's pool (the paged KV layout of the vox-serve "Adding a
 Model" page, section "1. The model code", with the layer axis dropped because
@@ -75,6 +79,7 @@ class Workload:
     layers: int = 1
     pool_pages: int = 0             # minimum pool size (0: just what is needed)
     theta: float = 10000.0
+    layout: str = "NHD"             # default cache layout (see make_case)
 
     @property
     def G(self) -> int:
@@ -96,6 +101,8 @@ WORKLOADS = {
         Workload("long", 3, B=16, Hq=32, Hkv=8, D=128, P=16, len_lo=2048, len_hi=8192),
         Workload("high", 4, B=256, Hq=32, Hkv=8, D=128, P=64, len_lo=256, len_hi=4096,
                  dist="loguniform", sigma=0.5, layers=28),
+        Workload("fastar", 5, B=64, Hq=16, Hkv=8, D=64, P=11, len_lo=11, len_hi=11,
+                 dist="fixed", fixed_lens=(11,) * 64, layers=4, layout="CONTIG"),
     ]
 }
 
@@ -115,17 +122,19 @@ class DecodeInputs:
     q: torch.Tensor            # [B, Hq, D] bf16 / fp16
     k_new: torch.Tensor        # [B, Hkv, D]
     v_new: torch.Tensor        # [B, Hkv, D]
-    pool: torch.Tensor         # NHD: [NP, 2, P, Hkv, D]; HND: [NP, 2, Hkv, P, D] (K at [:,0], V at [:,1])
+    pool: torch.Tensor         # NHD: [NP, 2, P, Hkv, D]; HND: [NP, 2, Hkv, P, D] (K at [:,0], V at [:,1]);
+                               # CONTIG: [2, B, Hkv, P, D] (K at [0], V at [1])
     page_table: torch.Tensor   # [B, MPS] int32
     seq_lens: torch.Tensor     # [B] int32
     active: torch.Tensor       # [B] int32
     meta: dict = field(default_factory=dict)
-    layout: str = "NHD"        # "NHD": token-major pages; "HND": head-major pages
+    layout: str = "NHD"        # "NHD": token-major pages; "HND": head-major pages;
+                               # "CONTIG": one contiguous cache per row, no page table
 
     # element strides of the pool, as the C interface takes them
     @property
     def page_stride(self) -> int:
-        return 2 * self.P * self.Hkv * self.D
+        return self.P * self.Hkv * self.D * (1 if self.layout == "CONTIG" else 2)
 
     @property
     def token_stride(self) -> int:
@@ -135,15 +144,26 @@ class DecodeInputs:
     def head_stride(self) -> int:
         return self.D if self.layout == "NHD" else self.P * self.D
 
+    @property
+    def api_page_table(self):
+        """The page table the library gets: None for contiguous caches."""
+        return None if self.layout == "CONTIG" else self.page_table
+
     def k_cache(self) -> torch.Tensor:
-        """K as a [NP, P, Hkv, D] view (strided for head-major pages)."""
+        """K as a [NP, P, Hkv, D] view (strided unless token-major)."""
+        if self.layout == "CONTIG":
+            return self.pool[0].transpose(1, 2)
         return self.pool[:, 0] if self.layout == "NHD" else self.pool[:, 0].transpose(1, 2)
 
     def v_cache(self) -> torch.Tensor:
+        if self.layout == "CONTIG":
+            return self.pool[1].transpose(1, 2)
         return self.pool[:, 1] if self.layout == "NHD" else self.pool[:, 1].transpose(1, 2)
 
     def nhd_pool(self) -> torch.Tensor:
         """The pool in token-major order [NP, 2, P, Hkv, D] (a view, or the pool itself)."""
+        if self.layout == "CONTIG":
+            return self.pool.permute(1, 0, 3, 2, 4)
         return self.pool if self.layout == "NHD" else self.pool.transpose(2, 3)
 
     def _fields(self, fn) -> "DecodeInputs":
@@ -191,10 +211,13 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     unless the caller passes other lengths for them on purpose.
     `page_order` is "random" (seeded permutation) or "linear" (pages 1, 2, ...).
     `dtype` (torch.bfloat16 or torch.float16) is the type of q, k, v and the pool.
-    `layout` "HND" stores the same pool values head-major ([NP, 2, Hkv, P, D]).
+    `layout` "HND" stores the same pool values head-major ([NP, 2, Hkv, P, D]);
+    "CONTIG" makes one cache of P positions per row (row b owns page b, no
+    page permutation) stored as [2, B, Hkv, P, D], with an identity page
+    table kept for the oracle.
     """
     assert dtype in (torch.bfloat16, torch.float16)
-    assert layout in ("NHD", "HND")
+    assert layout in ("NHD", "HND", "CONTIG")
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     lens = torch.as_tensor(seq_lens, dtype=torch.int64).clone()
@@ -203,18 +226,23 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     mps = max_pages_per_seq if max_pages_per_seq is not None else max(1, -(-int(lens.max()) // P))
     npages_row = [(-(-int(lens[b]) // P)) if act[b] else 0 for b in range(B)]
     used = sum(npages_row)
-    NP = max(pool_pages, used + 2)
-    if page_order == "random":
-        perm = torch.randperm(NP - 2, generator=gen) + 1
+    if layout == "CONTIG":
+        assert mps == 1, "a contiguous cache holds one page of P positions per row"
+        NP = B
+        page_table = torch.arange(B, dtype=torch.int64).view(B, 1)
     else:
-        perm = torch.arange(1, NP - 1)
-    page_table = torch.zeros(B, mps, dtype=torch.int64)
-    nxt = 0
-    for b in range(B):
-        n = npages_row[b]
-        assert n <= mps, "a row needs more pages than max_pages_per_seq"
-        page_table[b, :n] = perm[nxt:nxt + n]
-        nxt += n
+        NP = max(pool_pages, used + 2)
+        if page_order == "random":
+            perm = torch.randperm(NP - 2, generator=gen) + 1
+        else:
+            perm = torch.arange(1, NP - 1)
+        page_table = torch.zeros(B, mps, dtype=torch.int64)
+        nxt = 0
+        for b in range(B):
+            n = npages_row[b]
+            assert n <= mps, "a row needs more pages than max_pages_per_seq"
+            page_table[b, :n] = perm[nxt:nxt + n]
+            nxt += n
 
     # Values are drawn on the target device from a seed derived from the CPU generator.
     dev = torch.device(device)
@@ -239,6 +267,8 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
 
     if layout == "HND":
         pool = pool.transpose(2, 3).contiguous()
+    elif layout == "CONTIG":
+        pool = pool.permute(1, 0, 3, 2, 4).contiguous()
     return DecodeInputs(
         B=B, Hq=Hq, Hkv=Hkv, D=D, P=P, max_pages_per_seq=mps, num_pages=NP, theta=theta, layout=layout,
         q=q, k_new=k_new, v_new=v_new, pool=pool,
@@ -249,7 +279,7 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
 
 
 def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = torch.bfloat16,
-                layout: str = "NHD") -> DecodeInputs:
+                layout: str | None = None) -> DecodeInputs:
     """Inputs of one layer of a named workload (see the module docstring)."""
     w = WORKLOADS[name]
     seed = SEED_BASE + 100 * w.index + layer
@@ -266,7 +296,8 @@ def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = to
     sub_seed = int(torch.randint(0, 2**31 - 1, (1,), generator=gen))
     inp = make_case(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, P=w.P, seq_lens=lens, active=act,
                     max_pages_per_seq=w.max_pages_per_seq, sigma=w.sigma, seed=sub_seed,
-                    device=device, pool_pages=w.pool_pages, theta=w.theta, dtype=dtype, layout=layout)
+                    device=device, pool_pages=w.pool_pages, theta=w.theta, dtype=dtype,
+                    layout=layout or w.layout)
     inp.meta.update({"workload": name, "layer": layer, "workload_seed": seed})
     return inp
 
