@@ -13,9 +13,12 @@ over enough KV-pool replicas to exceed 4x the L2 size, so every step reads
 its K/V from HBM; CUDA events on the launching stream, synchronize and a
 barrier on both sides, max over ranks.  `e2e` goes through the public Python
 call with pinned host buffers: per step the new q/k/v, lengths, flags and page
-table (one input arena) are copied in and the output is copied out, captured
-as one CUDA graph per step the way a serving runtime replays its decode graph
-(`e2e.eager` issues the same copies and call from Python each step).
+table (one input arena) are copied in and the output is copied out.  The
+headline e2e replays a CUDA graph of many steps with two input arenas and two
+outputs, the copies on their own streams overlapping the neighbouring steps'
+kernels, as a serving runtime pipelines its decode steps; `e2e.serial` is one
+graph per step (copy in, call, copy out, in order) and `e2e.eager` issues the
+same copies and call from Python each step.
 
 --impl reference times the float64 CPU oracle on the host cores instead (each
 step one row of the same workload).  --ncu-case runs a few eager launches on
@@ -65,6 +68,8 @@ def parse():
                          "(default: the workload's)")
     ap.add_argument("--interleaved", action="store_true",
                     help="interleaved (2i, 2i+1) RoPE pairing instead of rotate-half")
+    ap.add_argument("--e2e-pdl", type=int, default=0,
+                    help="programmatic dependent launch between the pipelined e2e steps (1/0)")
     ap.add_argument("--qk-norm", action="store_true",
                     help="per-head RMSNorm of q and the new key before RoPE (unit weights, eps 1e-6)")
     ap.add_argument("--layers", type=int, default=None,
@@ -255,11 +260,11 @@ class Setup:
             return pool[:, 0].transpose(1, 2), pool[:, 1].transpose(1, 2)
         return pool[:, 0], pool[:, 1]
 
-    def fused(self, r, pdl=True, src=None):
+    def fused(self, r, pdl=True, src=None, out=None):
         s = src or self.inputs(r)
         k, v = self.kv(r)
-        self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v,
-                                s.api_page_table, s.seq_lens, s.active, self.out, self.wsf, pdl=pdl, **self.norm)
+        self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v, s.api_page_table, s.seq_lens,
+                                s.active, self.out if out is None else out, self.wsf, pdl=pdl, **self.norm)
 
     def three(self, r):
         i = self.inputs(r)
@@ -294,44 +299,53 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
         offs[k] = total
         total += -(-t.numel() * t.element_size() // 256) * 256
     h_arena = torch.zeros(total, dtype=torch.uint8).pin_memory()
-    d_arena = torch.zeros(total, dtype=torch.uint8, device=dev)
-    views = {}
     for k in names:
         t = getattr(inp, k)
         n = t.numel() * t.element_size()
         h_arena[offs[k]:offs[k] + n].copy_(t.contiguous().view(torch.uint8).view(-1).cpu())
-        views[k] = d_arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
-    d_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
-        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool", "layout")}, **views})
-    h_out = torch.empty((s.B, s.Hq, s.D), dtype=s.out.dtype).pin_memory()
+
+    def device_arena():
+        d_arena = torch.zeros(total, dtype=torch.uint8, device=dev)
+        views = {}
+        for k in names:
+            t = getattr(inp, k)
+            n = t.numel() * t.element_size()
+            views[k] = d_arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+        d_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
+            "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool", "layout")}, **views})
+        return d_arena, d_in
+
+    d_arenas, d_ins = zip(*[device_arena() for _ in range(2)])
+    outs = [s.out, torch.empty_like(s.out)]
+    h_outs = [torch.empty((s.B, s.Hq, s.D), dtype=s.out.dtype).pin_memory() for _ in range(2)]
     h2d = total
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
     K_e2e = min(args.steps, 2000)
 
     def e2e_step(r):
-        d_arena.copy_(h_arena, non_blocking=True)
-        s.fused(r, pdl=False, src=d_in)
-        h_out.copy_(s.out, non_blocking=True)
+        d_arenas[0].copy_(h_arena, non_blocking=True)
+        s.fused(r, pdl=False, src=d_ins[0])
+        h_outs[0].copy_(s.out, non_blocking=True)
 
-    def e2e_time(run_step, K):
+    def e2e_time(run, n, per):
         for i in range(3):
-            run_step(i)
+            run(i)
         torch.cuda.synchronize()
         barrier(world)
         t0 = time.perf_counter()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i in range(K):
-            run_step(i)
+        for i in range(n):
+            run(i)
         e1.record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-        return max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world) / K
+        return max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world) / (n * per)
 
     # eager: the Python call issued per step
-    e2e_eager_ms = e2e_time(lambda i: e2e_step(i % R), K_e2e)
-    # serving pattern: one CUDA graph per step (host->device copies of the step's
-    # inputs, the fused call, device->host copy of the output), replayed each step
+    e2e_eager_ms = e2e_time(lambda i: e2e_step(i % R), K_e2e, 1)
+    # one CUDA graph per step (host->device copy of the step's inputs, the
+    # fused call, device->host copy of the output), replayed each step
     graphs = []
     for r in range(R):
         g = torch.cuda.CUDAGraph()
@@ -341,13 +355,58 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
                 e2e_step(r)
         torch.cuda.current_stream().wait_stream(stream)
         graphs.append(g)
-    e2e_ms = e2e_time(lambda i: graphs[i % R].replay(), K_e2e)
+    e2e_serial_ms = e2e_time(lambda i: graphs[i % R].replay(), K_e2e, 1)
+
+    # pipelined serving pattern: two device input arenas and two outputs; the
+    # host->device copy of step i+1 runs on its own stream while step i
+    # computes, the device->host copy of step i on a third stream.  Every
+    # step still copies its whole input arena in and its output out.
+    M = R * max(1, 64 // R)  # steps per graph
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event() for _ in range(M)]
+    k_done = [torch.cuda.Event() for _ in range(M)]
+    d2h_done = [torch.cuda.Event() for _ in range(M)]
+    gp = torch.cuda.CUDAGraph()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(gp, stream=stream):
+            s_h2d.wait_stream(stream)
+            s_d2h.wait_stream(stream)
+            for i in range(M):
+                b = i % 2
+                with torch.cuda.stream(s_h2d):
+                    if i >= 2:
+                        s_h2d.wait_event(k_done[i - 2])  # step i-2 has read this arena
+                    d_arenas[b].copy_(h_arena, non_blocking=True)
+                    h2d_done[i].record(s_h2d)
+                stream.wait_event(h2d_done[i])
+                if i >= 2:
+                    stream.wait_event(d2h_done[i - 2])  # this output has been copied out
+                # programmatic dependent launch on the previous step's kernel: the
+                # inputs this launch reads before its wait come from its own
+                # copy, a full dependency
+                s.fused(i % R, pdl=args.e2e_pdl, src=d_ins[b], out=outs[b])
+                k_done[i].record(stream)
+                with torch.cuda.stream(s_d2h):
+                    s_d2h.wait_event(k_done[i])
+                    h_outs[b].copy_(outs[b], non_blocking=True)
+                    d2h_done[i].record(s_d2h)
+            stream.wait_stream(s_h2d)
+            stream.wait_stream(s_d2h)
+    torch.cuda.current_stream().wait_stream(stream)
+    e2e_ms = e2e_time(lambda i: gp.replay(), max(1, K_e2e // M), M)
     e2e_tps = by["active"] * world / (e2e_ms * 1e-3)
 
     return {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": K_e2e,
-            "call": "paged_len_decode_gb300.vh_decode_fused in a per-step CUDA graph with one "
-                    "pinned-host->device copy of the step's input arena and one output copy",
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": max(1, K_e2e // M) * M,
+            "call": "paged_len_decode_gb300.vh_decode_fused, one pinned-host->device copy of the step's "
+                    "input arena and one device->host copy of its output per step; CUDA graph of "
+                    f"{M} steps with two input arenas and two outputs, the copies on their own streams "
+                    "overlapping the neighbouring steps' kernels"
+                    + (", PDL between the kernels" if args.e2e_pdl else ""),
+            "serial": {"value": round(by["active"] * world / (e2e_serial_ms * 1e-3), 1),
+                       "ms_per_step": round(e2e_serial_ms, 6),
+                       "call": "one CUDA graph per step: copy in, call, copy out, in order"},
             "eager": {"value": round(by["active"] * world / (e2e_eager_ms * 1e-3), 1),
                       "ms_per_step": round(e2e_eager_ms, 6)}}
 
