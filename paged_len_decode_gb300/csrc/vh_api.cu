@@ -89,22 +89,31 @@ int env_int(const char* name, int dflt) {
   return std::atoi(s);
 }
 
-// kv heads per CTA: the largest divisor of Hkv with Hc * D <= 1024 and Hc <= 8
-// (VH_DECODE_HC lowers the cap, for tuning).
+// kv heads per CTA: the largest divisor of Hkv with Hc * D <= 512 (4 heads at
+// head_dim 128, 8 at 64): 32 KB tiles, so that two CTAs share an SM and the
+// work list is cut twice as fine as with whole-SM CTAs (VH_DECODE_HC sets
+// another cap, up to Hc * D <= 1024 and Hc <= 8, for tuning).
 int choose_hc(int Hkv, int D) {
-  int cap = std::min(1024 / D, 8);
+  int cap = std::min(512 / D, 8);
   const int want = env_int("VH_DECODE_HC", 0);
-  if (want >= 1 && want < cap) cap = want;
+  if (want >= 1) cap = std::min(want, std::min(1024 / D, 8));
   int hc = std::min(Hkv, cap);
   while (Hkv % hc != 0) --hc;
   return hc;
 }
 
+// Pipeline stages per CTA.  Two stages of 32 KB per CTA (128 KB in flight
+// per SM with two CTAs) keep HBM saturated on GB300; more bytes in flight
+// only lengthen the queues, which measured slower at the start and the end
+// of a launch (VH_DECODE_STAGES sets another count, for tuning).
+constexpr int kDefaultStages = 2;
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Shared-memory plan of the attention kernel (fused or not).  Prefers at
-// least three pipeline stages: if they do not fit, fewer kv heads go to each
-// CTA.  Returns false if even one head per CTA cannot have two stages.
+// Shared-memory plan of the attention kernel (fused or not): kDefaultStages
+// pipeline stages (or VH_DECODE_STAGES, if they fit); if two stages do not
+// fit, fewer kv heads go to each CTA.  Returns false if even one head per CTA
+// cannot have two stages.
 bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   p.fused = fused ? 1 : 0;
   p.G = p.Hq / p.Hkv;
@@ -128,14 +137,14 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
             2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256 +
             1024 /* alignment of the base */;
     stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
-    if (stages >= 3 || hc == 1) break;
+    if (stages >= 2 || hc == 1) break;
     int next = hc - 1;
     while (next > 1 && p.Hkv % next != 0) --next;
     hc = next;
   }
   if (stages < 2) return false;
   p.groups = p.Hkv / p.Hc;
-  const int want = env_int("VH_DECODE_STAGES", 0);
+  const int want = env_int("VH_DECODE_STAGES", kDefaultStages);
   if (want >= 2 && want < stages) stages = want;
   p.stages = stages;
   size_t off = static_cast<size_t>(stages) * p.stage_bytes;
