@@ -68,6 +68,9 @@ def parse():
                          "(default: the workload's)")
     ap.add_argument("--interleaved", action="store_true",
                     help="interleaved (2i, 2i+1) RoPE pairing instead of rotate-half")
+    ap.add_argument("--pdl-kv", type=int, default=1,
+                    help="fused steps request their first cached K/V tiles before the wait on the "
+                         "previous step (VH_FLAG_PDL_KV; each step reads another pool)")
     ap.add_argument("--e2e-pdl", type=int, default=0,
                     help="programmatic dependent launch between the pipelined e2e steps (1/0)")
     ap.add_argument("--qk-norm", action="store_true",
@@ -237,6 +240,7 @@ class Setup:
         self.ws3 = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.wsf = vh.alloc_workspace(self.B, self.Hq, self.Hkv, self.D, self.P, device=dev)
         self.n_ctas = vh.vh_decode_num_ctas(self.B, self.Hq, self.Hkv, self.D, self.P)
+        self.pdl_kv = False
         self.norm = {"interleaved": interleaved}
         if qk_norm:
             w = torch.ones(self.D, dtype=torch.float32, device=dev)
@@ -264,7 +268,8 @@ class Setup:
         s = src or self.inputs(r)
         k, v = self.kv(r)
         self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v, s.api_page_table, s.seq_lens,
-                                s.active, self.out if out is None else out, self.wsf, pdl=pdl, **self.norm)
+                                s.active, self.out if out is None else out, self.wsf, pdl=pdl,
+                                pdl_kv=pdl and self.pdl_kv, **self.norm)
 
     def three(self, r):
         i = self.inputs(r)
@@ -418,6 +423,7 @@ def run_ours(args, rank, world):
     s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm, dtype=args.dtype,
               interleaved=args.interleaved, layout=args.layout)
     inp, R, L = s.inp, s.R, s.L
+    s.pdl_kv = bool(args.pdl_kv) and R > 1  # consecutive steps read different pools
     by = s.step_bytes()
 
     for r in range(R):  # first calls outside capture (launch attributes, every replica's new slot)
@@ -493,7 +499,8 @@ def run_ours(args, rank, world):
                    "global_batch": s.B * world, "kv_bytes_per_step": by["kv"],
                    "step": (f"{L} layer calls, " if L > 1 else "") +
                            "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
-                           "PDL between launches",
+                           "PDL between launches" + (", first cached K/V tiles requested before the wait "
+                                                     "(VH_FLAG_PDL_KV)" if s.pdl_kv else ""),
                    "layers": L, "qk_norm": bool(args.qk_norm), "rope": "interleaved" if args.interleaved
                    else "rotate-half", "elements": args.dtype, "pages": s.inp.layout,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

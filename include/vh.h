@@ -112,6 +112,7 @@ typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16
 #define VH_FLAG_PDL 1u      /* programmatic dependent launch, see vh_decode_fused (that call only) */
 #define VH_FLAG_FP16 2u     /* 16-bit elements (q, k_new, v_new, cache, out) are IEEE fp16, not bf16 */
 #define VH_FLAG_ROPE_INTERLEAVED 4u /* RoPE pairs elements (2i, 2i+1) instead of (i, i + D/2) */
+#define VH_FLAG_PDL_KV 8u   /* VH_FLAG_PDL, and the cached K/V may be requested before the wait (vh_decode_fused) */
 
 /* Fill the RoPE table used by vh_rope_kv_append.
  * cos_sin: float [max_pos][D]; row p holds cos(p * f_i) in columns 0..D/2-1
@@ -234,6 +235,12 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
  *     positions or page_table (host copies in between are fine); everything
  *     else is read and written only after that kernel has completed.  The
  *     kernel itself always lets a following dependent launch start early.
+ *     VH_FLAG_PDL_KV implies VH_FLAG_PDL and also requests the first tiles
+ *     of the cached keys and values before that kernel has completed: valid
+ *     only when it writes none of the cache pages this call reads (for
+ *     instance the projection kernel of this layer, or this call for another
+ *     layer's cache); the new token's slot is rewritten from k_new / v_new
+ *     after the wait.
  * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,
  * VH_ENODEV, VH_ECUDA. */
 int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,

@@ -32,7 +32,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
 VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3, -4, -5
 VH_ESCRATCH = -6
 VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
-VH_FLAG_PDL, VH_FLAG_FP16, VH_FLAG_ROPE_INTERLEAVED = 1, 2, 4
+VH_FLAG_PDL, VH_FLAG_FP16, VH_FLAG_ROPE_INTERLEAVED, VH_FLAG_PDL_KV = 1, 2, 4, 8
 ELEM_DTYPES = (torch.bfloat16, torch.float16)
 
 
@@ -246,10 +246,11 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
 def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, out,
                     workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
                     pdl: bool = False, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
-                    interleaved: bool = False, stream=None) -> torch.Tensor:
+                    interleaved: bool = False, pdl_kv: bool = False, stream=None) -> torch.Tensor:
     """One whole decode step in one launch (RoPE, append, attention, merge).
     `workspace` must be zero-filled before its first use (alloc_workspace does that).
-    pdl=True sets VH_FLAG_PDL (see include/vh.h for when that is allowed)."""
+    pdl=True sets VH_FLAG_PDL, pdl_kv=True VH_FLAG_PDL_KV (see include/vh.h for
+    when each is allowed)."""
     B, Hq, D = q.shape
     kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     et = k_cache.dtype
@@ -265,7 +266,8 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
         _contig(out, et, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        (VH_FLAG_PDL if pdl else 0) | _elem_flags(k_cache, interleaved), B, Hq, Hkv, D, P,
+        (VH_FLAG_PDL if pdl else 0) | (VH_FLAG_PDL_KV if pdl_kv else 0) | _elem_flags(k_cache, interleaved),
+        B, Hq, Hkv, D, P,
         _stream(stream)), "vh_decode_fused")
     return out
 

@@ -287,6 +287,88 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     if (lane == 0) prefetch_tensormap(&p.tmap_k);
     if (lane == 1) prefetch_tensormap(&p.tmap_v);
   }
+  // ---- producer's box layout (used before and after the wait) --------------
+  const int h0 = gy * Hc;
+  // The tile's copies are boxes of box_heads heads x 8 tokens x 128 bytes:
+  // for K and for V, per 64-element column block hf, per 8-token group g
+  // and per group of box_heads heads.  Box j lands at [hf][g][head][token]
+  // in the K or V half of the stage; lane l issues boxes l and l + 32.  The
+  // same boxes serve token-major and head-major pages (the tensor map holds
+  // the strides).  Group g = 1 is skipped when the tile has <= 8 tokens.
+  const int HG_BOX = Hc / p.box_heads;  // head groups per (column block, token group)
+  const int NB = HALVES * 2 * HG_BOX;   // boxes of K (and of V) per tile
+  int bx_g[2], bx_hf[2], bx_head[2];
+  const void* bx_map[2];
+  uint32_t bx_off[2];
+  bool bx_on[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int j = lane + 32 * u;
+    bx_on[u] = j < 2 * NB;
+    const int kv = j >= NB ? 1 : 0, rem = j - kv * NB;
+    const int hf = rem / (2 * HG_BOX), rem2 = rem - hf * 2 * HG_BOX;
+    const int g = rem2 / HG_BOX, hq = rem2 - g * HG_BOX;
+    bx_g[u] = g;
+    bx_hf[u] = hf;
+    bx_head[u] = h0 + hq * p.box_heads;
+    bx_map[u] = kv ? static_cast<const void*>(&p.tmap_v) : static_cast<const void*>(&p.tmap_k);
+    bx_off[u] = static_cast<uint32_t>(kv * (p.stage_bytes / 2) + hf * Hc * 2048 + g * Hc * 1024 +
+                                      hq * p.box_heads * 1024);
+  }
+  // Tile state of the producer: stage ring position and, for tile t of row
+  // b, its box coordinates, the append slot and the bytes its boxes deliver.
+  int npre = 0;  // tiles whose boxes were requested before the wait
+  auto issue_tile = [&](long long t, int b, long long rt0, long long rt1, int tin_page, int page, bool page_ok,
+                        int stage) {
+    const int tok0 = static_cast<int>(t - rt0) * kTile;
+    const int nvalid = min(kTile, lens[b] - tok0);
+    const bool last_of_row = (t == rt1 - 1);
+    const long long page_off = static_cast<long long>(page) * p.page_stride;
+    const int tokc = tin_page * kTile;
+    const bool two_groups = nvalid > 8;
+    const uint32_t st = smem_addr(smem) + static_cast<uint32_t>(stage) * p.stage_bytes;
+    long long meta_val = -1;
+    if constexpr (FUSED) {
+      if (last_of_row && page_ok)
+        meta_val = page_off + static_cast<long long>(tin_page * kTile + nvalid - 1) * p.token_stride +
+                   static_cast<long long>(h0) * p.head_stride;
+    }
+    // bytes of the boxes issued: both token groups, or the first only
+    const uint32_t tx = static_cast<uint32_t>(two_groups ? p.stage_bytes : p.stage_bytes / 2);
+    const uint32_t fb = full0 + 8 * stage;
+    if (lane == 0) {
+      if constexpr (FUSED) meta[stage] = meta_val;
+      mbar_arrive_expect_tx(fb, tx);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (bx_on[u] && (two_groups || bx_g[u] == 0)) {
+        const int tk = tokc + 8 * bx_g[u];
+        const int c1 = p.tm_tok_dim == 1 ? tk : bx_head[u], c2 = p.tm_tok_dim == 1 ? bx_head[u] : tk;
+        tma_load_4d(st + bx_off[u], bx_map[u], bx_hf[u] * 64, c1, c2, page, fb);
+      }
+    }
+  };
+  if (FUSED && p.prefetch_kv && warp == Hc && c < n_eff) {
+    // The cached K/V of this call are not written by the previous kernel
+    // (the caller's promise with VH_FLAG_PDL_KV), and the new token's row is
+    // rewritten from v_new / the rotated k_new after the wait: the first
+    // stages can be requested before the wait.
+    int b = b0_pre;
+    long long rt1 = cum[b + 1];
+    const long long n = min(static_cast<long long>(S), t1_pre - t0_pre);
+    for (long long t = t0_pre; t < t0_pre + n; ++t) {
+      while (t >= rt1) rt1 = cum[++b + 1];
+      const long long rt0 = cum[b];
+      const int tin_page = static_cast<int>((t - rt0) % tpp);
+      int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - t0_pre));
+      const bool page_ok = page >= 0 && page < p.num_pages;
+      if (!page_ok) page = 0;  // flagged again after the wait
+      issue_tile(t, b, rt0, rt1, tin_page, page, page_ok, static_cast<int>(t - t0_pre));
+      ++npre;
+    }
+  }
   pdl_wait();
 
   // ---- per-row duties, rows b = c (mod N): split plan, zero padding rows ---
@@ -364,33 +446,6 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     // that a released stage is refilled at once: the row walk is incremental,
     // and the page ids come from a 32-tile window that is loaded (one
     // coalesced load per lane) a whole window ahead of its use.
-    const int h0 = gy * Hc;
-    // The tile's copies are boxes of box_heads heads x 8 tokens x 128 bytes:
-    // for K and for V, per 64-element column block hf, per 8-token group g
-    // and per group of box_heads heads.  Box j lands at [hf][g][head][token]
-    // in the K or V half of the stage; lane l issues boxes l and l + 32.  The
-    // same boxes serve token-major and head-major pages (the tensor map holds
-    // the strides).  Group g = 1 is skipped when the tile has <= 8 tokens.
-    const int HG_BOX = Hc / p.box_heads;  // head groups per (column block, token group)
-    const int NB = HALVES * 2 * HG_BOX;   // boxes of K (and of V) per tile
-    int bx_g[2], bx_hf[2], bx_head[2];
-    const void* bx_map[2];
-    uint32_t bx_off[2];
-    bool bx_on[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int j = lane + 32 * u;
-      bx_on[u] = j < 2 * NB;
-      const int kv = j >= NB ? 1 : 0, rem = j - kv * NB;
-      const int hf = rem / (2 * HG_BOX), rem2 = rem - hf * 2 * HG_BOX;
-      const int g = rem2 / HG_BOX, hq = rem2 - g * HG_BOX;
-      bx_g[u] = g;
-      bx_hf[u] = hf;
-      bx_head[u] = h0 + hq * p.box_heads;
-      bx_map[u] = kv ? static_cast<const void*>(&p.tmap_v) : static_cast<const void*>(&p.tmap_k);
-      bx_off[u] = static_cast<uint32_t>(kv * (p.stage_bytes / 2) + hf * Hc * 2048 + g * Hc * 1024 +
-                                        hq * p.box_heads * 1024);
-    }
     long long wb = t0;
     int b = b0;
     long long rt0 = cum[b], rt1 = cum[b + 1];
@@ -413,9 +468,6 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
         win = nxt;
         nxt = tile_page(wb + 32 + lane);
       }
-      const int tok0 = static_cast<int>(t - rt0) * kTile;
-      const int nvalid = min(kTile, lens[b] - tok0);
-      const bool last_of_row = (t == rt1 - 1);
       int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - wb));
       const bool page_ok = page >= 0 && page < p.num_pages;
       if (!page_ok) {
@@ -446,45 +498,21 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
         }
         ++nseg;
       }
-      // the box coordinates of this tile and the append slot (the new token's
-      // row arrives as whatever the cache slot holds; the consumers overwrite
-      // it with the rotated key and v_new)
-      const long long page_off = static_cast<long long>(page) * p.page_stride;
-      const int tokc = tin_page * kTile;
-      const bool two_groups = nvalid > 8;
-      const uint32_t st = smem_addr(smem) + static_cast<uint32_t>(stage) * p.stage_bytes;
-      long long meta_val = -1;
-      if constexpr (FUSED) {
-        if (last_of_row && page_ok)
-          meta_val = page_off + static_cast<long long>(tin_page * kTile + nvalid - 1) * p.token_stride +
-                     static_cast<long long>(h0) * p.head_stride;
-      }
-      // bytes of the boxes issued: both token groups, or the first only
-      const uint32_t tx = static_cast<uint32_t>(two_groups ? p.stage_bytes : p.stage_bytes / 2);
-
-      if (issued >= S && !mbar_wait(empty0 + 8 * stage, (round - 1) & 1)) {
-        if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
-        *abort_flag = 1;
-        aborted = true;
-        break;
-      }
-      if (*abort_flag) {
-        aborted = true;
-        break;
-      }
-      const uint32_t fb = full0 + 8 * stage;
-      if (lane == 0) {
-        if constexpr (FUSED) meta[stage] = meta_val;
-        mbar_arrive_expect_tx(fb, tx);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (bx_on[u] && (two_groups || bx_g[u] == 0)) {
-          const int tk = tokc + 8 * bx_g[u];
-          const int c1 = p.tm_tok_dim == 1 ? tk : bx_head[u], c2 = p.tm_tok_dim == 1 ? bx_head[u] : tk;
-          tma_load_4d(st + bx_off[u], bx_map[u], bx_hf[u] * 64, c1, c2, page, fb);
+      // the boxes of this tile (the new token's row arrives as whatever the
+      // cache slot holds; the consumers overwrite it with the rotated key and
+      // v_new), unless they were requested before the wait
+      if (issued >= npre) {
+        if (issued >= S && !mbar_wait(empty0 + 8 * stage, (round - 1) & 1)) {
+          if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+          *abort_flag = 1;
+          aborted = true;
+          break;
         }
+        if (*abort_flag) {
+          aborted = true;
+          break;
+        }
+        issue_tile(t, b, rt0, rt1, tin_page, page, page_ok, stage);
       }
       if (++stage == S) {
         stage = 0;
@@ -492,9 +520,11 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       }
     }
     if (aborted) {
-      // Let the copies already issued land before the CTA's shared memory goes away.
-      const long long n = min(issued, static_cast<long long>(S));
-      for (long long k = issued - n; k < issued; ++k)
+      // Let the copies already issued land before the CTA's shared memory goes away
+      // (including those requested before the wait).
+      const long long req = max(issued, static_cast<long long>(npre));
+      const long long n = min(req, static_cast<long long>(S));
+      for (long long k = req - n; k < req; ++k)
         (void)mbar_wait(full0 + 8 * static_cast<int>(k % S), static_cast<uint32_t>((k / S) & 1));
       if (nseg > 0) (void)mbar_wait(qfull, (nseg - 1) & 1);
     }

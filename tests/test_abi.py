@@ -130,7 +130,8 @@ def test_fused_argument_checks():
                  None)
 
     assert call(q=None) == v.VH_EINVAL
-    assert call(flags=8) == v.VH_EINVAL            # unknown flag
+    assert call(flags=16) == v.VH_EINVAL           # unknown flag
+    assert call(flags=v.VH_FLAG_PDL_KV, out=ODD) == v.VH_EALIGN
     assert call(flags=v.VH_FLAG_PDL | v.VH_FLAG_FP16 | v.VH_FLAG_ROPE_INTERLEAVED, out=ODD) == v.VH_EALIGN
     assert call(Hq=24) == v.VH_EINVAL
     assert call(eps=-0.5) == v.VH_EINVAL

@@ -414,3 +414,22 @@ def test_head_major_padding_rows_leave_page_zero_alone(path):
     before = H.bits16(inp.nhd_pool().cpu())
     got = H.run_step(inp, path=path)
     assert torch.equal(H.bits16(got["pool_after"][0]), before[0]), "dummy page 0 was written"
+
+
+# ---------------------------------------------------------------- cached K/V requested before the wait
+
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("name", ["tiny", "c64", "padded", "long"])
+def test_fused_kv_requested_before_dependency_wait(name, graph):
+    # two identical calls in a row on one cache: the only slot the first call
+    # writes is the one the second rewrites from k_new / v_new, so the second
+    # may request its cached tiles before the first has completed
+    inp = workloads.make_inputs(name, device="cuda")
+    H.full_check(inp, path="fused", pdl=True, pdl_kv=True, graph=graph, repeat=2)
+
+
+@pytest.mark.parametrize("layout", ["HND", "CONTIG"])
+def test_fused_kv_requested_early_other_layouts(layout):
+    name = "fastar" if layout == "CONTIG" else "c64"
+    inp = workloads.make_inputs(name, device="cuda", layout=layout, dtype=torch.float16)
+    H.full_check(inp, path="fused", pdl=True, pdl_kv=True, graph=True, repeat=3, interleaved=True)
