@@ -283,6 +283,18 @@ int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k_cache, con
                                  vh_bf16* out, float sm_scale, int num_ctas, int32_t* err_flag,
                                  int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
+/* Self-test of the failure path of the kernels' pipeline waits.  The source
+ * pages have no counterpart: every wait of the attention kernels on an
+ * mbarrier (a stage landing, a stage released, a partial result written) is
+ * bounded by about a second of SM clock; when it runs out, the kernel ORs
+ * VH_ERR_TIMEOUT into *err_flag and winds down instead of hanging the GPU.
+ * This call launches one warp that runs that same bounded wait on a barrier
+ * nothing ever arrives on, so the wait gives up (after about a second) and
+ * VH_ERR_TIMEOUT is set; the CUDA context stays usable afterwards.
+ * err_flag: device int32*, required (4-byte aligned).
+ * Errors: VH_EINVAL (NULL err_flag), VH_EALIGN, VH_ENODEV, VH_ECUDA. */
+int vh_selftest_wait_timeout(int32_t* err_flag, void* stream);
+
 /* Static text for a return code. */
 const char* vh_status_string(int status);
 

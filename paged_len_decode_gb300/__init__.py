@@ -14,7 +14,7 @@ selects a contiguous cache (row b owns pages b*m .. b*m+m-1, m = pages / B).
 Functions mirror the C entry points by name:
     vh_rope_table, vh_rope_kv_append, vh_decode_num_ctas,
     vh_decode_workspace_bytes, vh_paged_decode_attn, vh_decode_combine,
-    vh_decode_fused, vh_paged_decode_attn_noalloc, vh_status_string
+    vh_decode_fused, vh_paged_decode_attn_noalloc, vh_selftest_wait_timeout, vh_status_string
 plus `decode_step`, which issues the three calls of one decode step.
 """
 from __future__ import annotations
@@ -48,6 +48,8 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     P, I, I64, F, D, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                            ctypes.c_double, ctypes.c_size_t)
+    lib.vh_selftest_wait_timeout.argtypes = [P, P]
+    lib.vh_selftest_wait_timeout.restype = I
     lib.vh_status_string.argtypes = [I]
     lib.vh_status_string.restype = ctypes.c_char_p
     lib.vh_rope_table.argtypes = [P, I, I, D, P]
@@ -147,6 +149,13 @@ def _table(page_table, B: int, NP: int):
 
 def _elem_flags(k_cache: torch.Tensor, interleaved: bool = False) -> int:
     return (VH_FLAG_FP16 if k_cache.dtype == torch.float16 else 0) | (VH_FLAG_ROPE_INTERLEAVED if interleaved else 0)
+
+
+def vh_selftest_wait_timeout(err_flag: torch.Tensor, stream=None) -> None:
+    """Run the kernels' bounded pipeline wait on a barrier nothing arrives on;
+    VH_ERR_TIMEOUT is ORed into err_flag (int32 CUDA tensor) after about a second."""
+    _check(lib.vh_selftest_wait_timeout(_contig(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "vh_selftest_wait_timeout")
 
 
 def vh_rope_table(cos_sin: torch.Tensor, theta: float = 10000.0, stream=None) -> torch.Tensor:

@@ -169,6 +169,24 @@ __global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p
   }
 }
 
+// The library's bounded pipeline wait on a barrier that nothing ever arrives
+// on: it must give up after its time limit and report VH_ERR_TIMEOUT, leaving
+// the context usable (the failure path of every pipeline wait).
+__global__ void wait_timeout_selftest_kernel(int32_t* err_flag) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (!mbar_wait(smem_addr(&bar), 0) && threadIdx.x == 0) flag_error(err_flag, VH_ERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_selftest(int32_t* err_flag, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err_flag);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, cudaStream_t stream) {
   const long long n = static_cast<long long>(max_pos) * (D / 2);
   int blocks = static_cast<int>((n + 255) / 256);

@@ -284,6 +284,14 @@ const char* vh_status_string(int status) {
   }
 }
 
+int vh_selftest_wait_timeout(int32_t* err_flag, void* stream) {
+  if (!err_flag) return VH_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(err_flag) & 3u) != 0) return VH_EALIGN;
+  if (!device_info()) return VH_ENODEV;
+  return vh::launch_wait_timeout_selftest(err_flag, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK
+                                                                                                    : VH_ECUDA;
+}
+
 int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void* stream) {
   if (!cos_sin || max_pos < 1 || (head_dim != 64 && head_dim != 128) || !(theta > 0.0)) return VH_EINVAL;
   if (!aligned16(cos_sin)) return VH_EALIGN;

@@ -106,6 +106,7 @@ struct CombineParams {
 };
 
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int D, double theta, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(int32_t* err_flag, cudaStream_t stream);
 cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream);
 cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device, every variant
 cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pdl);

@@ -171,3 +171,15 @@ def test_contiguous_cache_arguments_pass_host_checks_without_device():
     if torch.cuda.is_available():
         pytest.skip("a device is present")
     assert attn(pt=None, npages=4, mps=1, P=11) == v.VH_ENODEV
+
+
+def test_wait_timeout_selftest_arguments():
+    assert v.lib.vh_selftest_wait_timeout(None, None) == v.VH_EINVAL
+    assert v.lib.vh_selftest_wait_timeout(ctypes.c_void_p(0x10002), None) == v.VH_EALIGN
+
+
+def test_wait_timeout_selftest_without_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert v.lib.vh_selftest_wait_timeout(FAKE, None) == v.VH_ENODEV
