@@ -48,7 +48,8 @@ METRIC = "decode-attn tokens/s and achieved HBM GB/s (% of GB300 peak) at c=64"
 WORKLOAD = "c64"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["paged_len_decode_gb300/csrc/decode_attn.cu", "paged_len_decode_gb300/csrc/vh_common.cuh",
-                  "paged_len_decode_gb300/csrc/vh_kernels.h", "paged_len_decode_gb300/csrc/vh_api.cu"]
+                  "paged_len_decode_gb300/csrc/vh_kernels.h", "paged_len_decode_gb300/csrc/vh_plan.cu",
+                  "paged_len_decode_gb300/csrc/vh_plan.h"]
 
 
 def parse():

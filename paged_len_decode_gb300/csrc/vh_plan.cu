@@ -1,0 +1,258 @@
+// vh_plan.cu -- launch planning of the decode kernels (host side).
+//
+// Per device: the checks and kernel attributes set once.  Per call: kv heads
+// per CTA, pipeline stages and the shared-memory layout, the CTA count, the
+// workspace layout, and the tensor maps of the K and V caches.  The entry
+// points in vh_api.cu validate arguments and call these.
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
+#include "vh_plan.h"
+
+namespace vh {
+
+namespace {
+constexpr int kMaxStages = 8;
+// Lower bound on tiles per CTA when the work list is short.  One tile: a
+// short list (the Fast AR step: 64 one-tile rows) then spreads over as many
+// CTAs as it has tiles, which measured 2.1x faster there than four tiles per
+// CTA and the same on the long lists (VH_DECODE_MIN_TILES, for tuning).
+constexpr int kMinTilesPerCta = 1;
+}  // namespace
+
+DeviceInfo g_dev[kMaxDevices];
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  DeviceInfo& d = g_dev[dev];
+  std::call_once(d.once, [&]() {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    // The kernels are built for sm_103a only.
+    if (major != 10 || minor != 3) return;
+    for (int D : {64, 128})
+      for (int G : {1, 2, 4, 8})
+        if (vh::prepare_decode_attn(D, G, d.smem_optin) != cudaSuccess) {
+          cudaGetLastError();
+          return;
+        }
+    d.ok = true;
+  });
+  return d.ok ? &d : nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool valid_gqa(int Hq, int Hkv) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return false;
+  const int G = Hq / Hkv;
+  return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+bool valid_shape(int B, int Hq, int Hkv, int D, int P) {
+  return B >= 1 && B <= 65535 && valid_gqa(Hq, Hkv) && (D == 64 || D == 128) && P >= 1 && P <= 1024 &&
+         Hkv <= 1024;
+}
+
+// Pages of a row hold whole 16-token tiles, unless a row has a single page.
+bool valid_paging(int P, int max_pages_per_seq) {
+  return max_pages_per_seq >= 1 && (P % 16 == 0 || max_pages_per_seq == 1);
+}
+
+// Without a page table, row b's pages are b * max_pages_per_seq + j: they must exist.
+bool valid_table(const int32_t* page_table, int B, int max_pages_per_seq, int num_pages) {
+  return page_table != nullptr || static_cast<long long>(B) * max_pages_per_seq <= num_pages;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return dflt;
+  return std::atoi(s);
+}
+
+// kv heads per CTA: the largest divisor of Hkv with Hc * D <= 512 (4 heads at
+// head_dim 128, 8 at 64): 32 KB tiles, so that two CTAs share an SM and the
+// work list is cut twice as fine as with whole-SM CTAs (VH_DECODE_HC sets
+// another cap, up to Hc * D <= 1024 and Hc <= 8, for tuning).
+static int choose_hc(int Hkv, int D) {
+  int cap = std::min(512 / D, 8);
+  const int want = env_int("VH_DECODE_HC", 0);
+  if (want >= 1) cap = std::min(want, std::min(1024 / D, 8));
+  int hc = std::min(Hkv, cap);
+  while (Hkv % hc != 0) --hc;
+  return hc;
+}
+
+// Pipeline stages per CTA.  Two stages of 32 KB per CTA (128 KB in flight
+// per SM with two CTAs) keep HBM saturated on GB300; more bytes in flight
+// only lengthen the queues, which measured slower at the start and the end
+// of a launch (VH_DECODE_STAGES sets another count, for tuning).
+constexpr int kDefaultStages = 2;
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory plan of the attention kernel (fused or not): kDefaultStages
+// pipeline stages (or VH_DECODE_STAGES, if they fit); if two stages do not
+// fit, fewer kv heads go to each CTA.  Returns false if even one head per CTA
+// cannot have two stages.
+bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
+  p.fused = fused ? 1 : 0;
+  p.G = p.Hq / p.Hkv;
+  const size_t budget = static_cast<size_t>(dev.smem_optin);
+  int hc = choose_hc(p.Hkv, p.D);
+  size_t fixed = 0;
+  int stages = 0;
+  for (;;) {
+    p.Hc = hc;
+    // K and V of a 16-token tile, as swizzled 16 x 128-byte boxes (no padding
+    // needed for conflict-free ldmatrix): 2 * 16 * Hc * D * 2 bytes, a
+    // multiple of 2048 so every box stays 1024-byte aligned
+    p.stage_bytes = 2 * 16 * hc * p.D * 2;
+    const size_t hg = static_cast<size_t>(hc) * p.G;
+    // staged q rows, contiguous: one bulk copy per segment
+    p.q_row_bytes = fused ? p.D * 2 : p.D * 4;
+    p.q_tx_bytes = static_cast<int>(fused ? hg * p.D * 2 + p.D * 4 : hg * p.D * 4);
+    p.q_bytes = static_cast<int>(hg * p.q_row_bytes + (fused ? p.D * 4 : 0));
+    const size_t qs_bytes = fused ? static_cast<size_t>(hc) * p.G * (p.D * 4 + 32) : 0;
+    fixed = align_up(p.q_bytes, 128) + align_up(qs_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
+            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256 +
+            1024 /* alignment of the base */;
+    stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
+    if (stages >= 2 || hc == 1) break;
+    int next = hc - 1;
+    while (next > 1 && p.Hkv % next != 0) --next;
+    hc = next;
+  }
+  if (stages < 2) return false;
+  p.groups = p.Hkv / p.Hc;
+  const int want = env_int("VH_DECODE_STAGES", kDefaultStages);
+  if (want >= 2 && want < stages) stages = want;
+  p.stages = stages;
+  size_t off = static_cast<size_t>(stages) * p.stage_bytes;
+  p.q_off = static_cast<int>(off);
+  off += align_up(p.q_bytes, 128);
+  p.qs_off = static_cast<int>(off);
+  if (fused) off += align_up(static_cast<size_t>(p.Hc) * p.G * (p.D * 4 + 32), 128);
+  p.cum_off = static_cast<int>(off);
+  off += align_up(4 * (static_cast<size_t>(p.B) + 1), 16);
+  p.len_off = static_cast<int>(off);
+  off += align_up(4 * static_cast<size_t>(p.B), 16);
+  p.pos_off = static_cast<int>(off);
+  off += align_up(4 * static_cast<size_t>(p.B), 16);
+  p.meta_off = static_cast<int>(off);
+  off += 8 * static_cast<size_t>(stages);
+  p.bar_off = static_cast<int>(align_up(off, 16));
+  off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 4) + 48 * 4;
+  // + up to 1024 bytes that the kernel skips to align its base for the boxes
+  p.smem_bytes = static_cast<int>(align_up(off, 128) + 1024);
+  p.min_tiles = std::max(1, env_int("VH_DECODE_MIN_TILES", kMinTilesPerCta));
+  return static_cast<size_t>(p.smem_bytes) <= budget;
+}
+
+int auto_ctas(const AttnParams& p, const DeviceInfo& dev) {
+  int per_sm = 0;
+  if (vh::decode_attn_occupancy(p, &per_sm) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int want = env_int("VH_DECODE_CTAS_PER_SM", 0);
+  if (want >= 1 && want < per_sm) per_sm = want;
+  return std::max(1, dev.sm_count * per_sm / p.groups);
+}
+
+// Workspace: per-row split plan (int4 [B]); per-(head group, row) counters of
+// the fused merge (int [Hkv][B], an upper bound on groups); partial lse
+// [groups][N][2][Hq/groups] and partial outputs [...][D] (groups * Hq/groups == Hq).
+
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int N) {
+  WsLayout w;
+  w.plan = 0;
+  w.counters = align_up(static_cast<size_t>(B) * 16, 256);
+  w.lse = w.counters + align_up(static_cast<size_t>(B) * Hkv * 4, 256);
+  w.o = w.lse + align_up(static_cast<size_t>(N) * 2 * Hq * 4, 256);
+  w.total = w.o + static_cast<size_t>(N) * 2 * Hq * D * 4;
+  return w;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor maps of the K and V caches for the attention kernel's tile copies:
+// 4-D tensors of 16-bit elements (dimension 0 = head_dim, 3 = page) with the
+// 128-byte swizzle, boxes of 64 elements x 8 tokens x box_heads heads, which
+// land in shared memory as [head][token][128 bytes].  Preferred: dimension
+// 1 = token, 2 = head and box_heads = Hc, so a tile is two boxes (token
+// groups) per 64-column block of K and of V.  If the encoder rejects that order (the strides of
+// token-major pages decrease from dimension 1 to 2), dimensions 1 and 2 are
+// token and head in increasing stride order and each box holds one head.
+// Sets p.tm_tok_dim and p.box_heads.  Returns false if no encoding is accepted.
+bool encode_cache_maps(AttnParams& p) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  // L2 fill granularity of the tile reads (VH_TMA_L2 = 0, 64, 128 or 256 bytes, for tuning)
+  CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  switch (env_int("VH_TMA_L2", 256)) {
+    case 0: promo = CU_TENSOR_MAP_L2_PROMOTION_NONE; break;
+    case 64: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_64B; break;
+    case 128: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B; break;
+    default: break;
+  }
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  auto encode = [&](bool tok_first, cuuint32_t heads) -> bool {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.D), static_cast<cuuint64_t>(tok_first ? p.P : p.Hkv),
+                                static_cast<cuuint64_t>(tok_first ? p.Hkv : p.P),
+                                static_cast<cuuint64_t>(p.num_pages)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(2 * (tok_first ? p.token_stride : p.head_stride)),
+                                   static_cast<cuuint64_t>(2 * (tok_first ? p.head_stride : p.token_stride)),
+                                   static_cast<cuuint64_t>(2 * p.page_stride)};
+    const cuuint32_t box[4] = {64, tok_first ? 8u : 1u, tok_first ? heads : 8u, 1};
+    for (int kv = 0; kv < 2; ++kv) {
+      CUtensorMap* m = kv ? &p.tmap_v : &p.tmap_k;
+      void* base = const_cast<uint16_t*>(kv ? p.v_cache : p.k_cache);
+      if (enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    }
+    p.tm_tok_dim = tok_first ? 1 : 2;
+    p.box_heads = static_cast<int>(heads);
+    return true;
+  };
+  if (env_int("VH_TMA_BOX_HEADS", 0) != 1 && encode(true, static_cast<cuuint32_t>(p.Hc))) return true;
+  return encode(p.token_stride <= p.head_stride, 1);
+}
+
+bool too_many_tiles(int B, int max_pages_per_seq, int P) {
+  const long long max_len = static_cast<long long>(max_pages_per_seq) * P;
+  return max_len > (1LL << 24) || static_cast<long long>(B) * ((max_len + 15) / 16) >= (1LL << 31);
+}
+
+}  // namespace vh
