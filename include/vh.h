@@ -64,7 +64,11 @@
  *
  * Shapes: B rows, Hq q heads, Hkv kv heads (Hq % Hkv == 0, G = Hq / Hkv
  * in {1, 2, 4, 8}), head dim D in {64, 128}, page size 1 <= P <= 1024, a
- * multiple of 16 when max_pages_per_seq > 1, 1 <= B <= 65535.  seq_len
+ * multiple of 16 when max_pages_per_seq > 1, 1 <= B <= 65535 and small
+ * enough for the attention kernels' shared-memory plan, which keeps 12
+ * bytes per row (tile count, length, position) in every CTA: up to about
+ * 17,000 rows (fewer kv heads per CTA as B grows); beyond that the calls
+ * that plan return VH_EINVAL before any launch.  seq_len
  * counts the token being appended: row b attends over logical slots
  * 0 .. seq_lens[b]-1, and the new token is slot seq_lens[b]-1, i.e. page
  * page_table[b][(L-1)/P], offset (L-1) % P.  page_table is int32

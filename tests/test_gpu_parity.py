@@ -433,3 +433,27 @@ def test_fused_kv_requested_early_other_layouts(layout):
     name = "fastar" if layout == "CONTIG" else "c64"
     inp = workloads.make_inputs(name, device="cuda", layout=layout, dtype=torch.float16)
     H.full_check(inp, path="fused", pdl=True, pdl_kv=True, graph=True, repeat=3, interleaved=True)
+
+
+# ---------------------------------------------------------------- batch-size limit of the plan
+
+def test_batch_beyond_the_shared_memory_plan_is_rejected_on_the_host():
+    v = H.vh()
+    assert v.vh_decode_num_ctas(16384, 16, 8, 128, 16) > 0
+    with pytest.raises(v.VHError) as e:
+        v.vh_decode_num_ctas(20000, 16, 8, 128, 16)
+    assert e.value.status == v.VH_EINVAL
+    assert v.lib.vh_decode_workspace_bytes(20000, 16, 8, 128, 16, 0) == 0
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_batch_near_the_plan_limit(path):
+    # 16384 one-token and short rows, a quarter of them padding
+    g = torch.Generator().manual_seed(90)
+    B = 16384
+    act = (torch.rand(B, generator=g) > 0.25).int().tolist()
+    lens = [int(x) if a else 1 for x, a in zip(torch.randint(1, 40, (B,), generator=g).tolist(), act)]
+    inp = workloads.make_case(B=B, Hq=2, Hkv=1, D=64, P=16, seq_lens=lens, active=act, seed=91,
+                              device="cuda", max_pages_per_seq=3)
+    rows = list(range(0, B, 97))  # the oracle checks a sample of rows; the append is checked everywhere
+    H.full_check(inp, path=path, rows=rows)
