@@ -113,7 +113,7 @@ typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16
 #define VH_ERR_TIMEOUT 8    /* an internal pipeline wait ran out of time: the CTA gave up */
 
 /* flags (the `flags` argument of the calls that take one) */
-#define VH_FLAG_PDL 1u      /* programmatic dependent launch, see vh_decode_fused (that call only) */
+#define VH_FLAG_PDL 1u      /* programmatic dependent launch (vh_decode_fused, vh_paged_decode_attn) */
 #define VH_FLAG_FP16 2u     /* 16-bit elements (q, k_new, v_new, cache, out) are IEEE fp16, not bf16 */
 #define VH_FLAG_ROPE_INTERLEAVED 4u /* RoPE pairs elements (2i, 2i+1) instead of (i, i + D/2) */
 #define VH_FLAG_PDL_KV 8u   /* VH_FLAG_PDL, and the cached K/V may be requested before the wait (vh_decode_fused) */
@@ -191,7 +191,11 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
  *     per-row split plan and the fp32 partial results.  No initialisation
  *     is needed.  Calls that overlap on the device must use distinct
  *     workspaces.
- * flags: 0 or VH_FLAG_FP16 (cache and out are fp16).
+ * flags: VH_FLAG_FP16 (cache and out are fp16) and VH_FLAG_PDL: launch as a
+ *     programmatic dependent of the previous kernel on the stream (for
+ *     instance vh_rope_kv_append): lengths, flags and page ids are read before
+ *     that kernel has completed and must not be written by it; q_rot and the
+ *     cache are read after.
  * Softmax in fp32 with a running max, exp2 with log2(e) folded into the
  * scale; keys beyond seq_len (tail of the last page) are never used.  With
  * fp16, q_rot is split into an fp16 high part and residual for the tensor

@@ -209,7 +209,8 @@ def vh_decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, page_size: int,
 
 
 def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
-                         sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None, stream=None) -> None:
+                         sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None, pdl: bool = False,
+                         stream=None) -> None:
     B, Hq, D = q_rot.shape
     kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     if Dc != D or out.shape != (B, Hq, D):
@@ -220,7 +221,8 @@ def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, 
         _contig(out, k_cache.dtype, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        _elem_flags(k_cache), B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn")
+        _elem_flags(k_cache) | (VH_FLAG_PDL if pdl else 0), B, Hq, Hkv, D, P, _stream(stream)),
+        "vh_paged_decode_attn")
 
 
 def vh_decode_combine(workspace, out, Hkv: int, page_size: int, num_ctas: int = 0, stream=None) -> None:
@@ -296,8 +298,10 @@ def decode_step(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens
     vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
                       q_rot, positions=positions, err_flag=err_flag, q_norm_w=q_norm_w,
                       k_norm_w=k_norm_w, norm_eps=norm_eps, interleaved=interleaved, stream=stream)
+    # the attention launch depends programmatically on the append kernel just
+    # before it, which writes neither lengths, flags nor the page table
     vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
-                         sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, stream=stream)
+                         sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, pdl=True, stream=stream)
     vh_decode_combine(workspace, out, k_cache.shape[2], k_cache.shape[1], num_ctas=num_ctas,
                       stream=stream)
     return out

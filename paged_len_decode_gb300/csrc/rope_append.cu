@@ -43,6 +43,7 @@ __global__ void rope_table_kernel(float* __restrict__ cos_sin, int max_pos, int 
 // (written to the cache).  V is copied 16 bytes per thread.
 template <typename E>
 __global__ void __launch_bounds__(1024) rope_kv_append_kernel(RopeAppendParams p) {
+  pdl_launch_dependents();  // an attention launch that depends on this one may start planning
   const int b = blockIdx.x;
   if (!p.active[b]) return;
   const int L = p.seq_lens[b];

@@ -162,7 +162,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
                          void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                          int B, int Hq, int Hkv, int D, int page_size, void* stream) {
   if (!q_rot || !k_cache || !v_cache || !seq_lens || !active || !out ||
-      (flags & ~static_cast<unsigned>(VH_FLAG_FP16)) != 0 || !valid_paging(page_size, max_pages_per_seq) ||
+      (flags & ~(VH_FLAG_FP16 | VH_FLAG_PDL)) != 0 || !valid_paging(page_size, max_pages_per_seq) ||
       !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
@@ -207,7 +207,9 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
   p.part_o = reinterpret_cast<float*>(ws + w.o);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
-  return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? VH_OK : VH_ECUDA;
+  return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), (flags & VH_FLAG_PDL) != 0) == cudaSuccess
+             ? VH_OK
+             : VH_ECUDA;
 }
 
 int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out, int num_ctas,

@@ -70,7 +70,7 @@ def attn(**over):
     (dict(hs=68), v.VH_EALIGN),               # head stride not a multiple of 16 bytes
     (dict(ws=None), v.VH_EWORKSPACE),
     (dict(ws=ODD), v.VH_EALIGN),
-    (dict(flags=v.VH_FLAG_PDL), v.VH_EINVAL),                 # not a flag of this call
+    (dict(flags=v.VH_FLAG_PDL_KV), v.VH_EINVAL),              # not a flag of this call
     (dict(flags=v.VH_FLAG_ROPE_INTERLEAVED), v.VH_EINVAL),    # nor this one (no RoPE here)
     (dict(flags=8), v.VH_EINVAL),
     (dict(flags=v.VH_FLAG_FP16, q_rot=ODD), v.VH_EALIGN),     # fp16 passes the flag check
