@@ -118,7 +118,8 @@ typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16
 #define VH_FLAG_ROPE_INTERLEAVED 4u /* RoPE pairs elements (2i, 2i+1) instead of (i, i + D/2) */
 #define VH_FLAG_PDL_KV 8u   /* VH_FLAG_PDL, and the cached K/V may be requested before the wait (vh_decode_fused) */
 
-/* Fill the RoPE table used by vh_rope_kv_append.
+/* Fill the RoPE table used by vh_rope_kv_append.  Source: "Engineering TTS
+ * inference in vLLM-Omni", Qwen3-TTS section 4 (RoPE cos/sin kept in fp32).
  * cos_sin: float [max_pos][D]; row p holds cos(p * f_i) in columns 0..D/2-1
  * and sin(p * f_i) in columns D/2..D-1, f_i = theta^(-2i/D).  Angles and
  * cos/sin are evaluated in double and stored as float (the pages keep RoPE
@@ -127,7 +128,10 @@ typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16
  * theta <= 0; VH_EALIGN if cos_sin is not 16-byte aligned. */
 int vh_rope_table(float* cos_sin, int max_pos, int head_dim, double theta, void* stream);
 
-/* RoPE + KV append, one CTA per row.
+/* RoPE + KV append, one CTA per row.  Sources: "Adding a Model" (vox-serve),
+ * section "1. The model code" (RoPE on q and k, then the new key and value
+ * written into the paged cache before attention); "Engineering TTS inference
+ * in vLLM-Omni", Qwen3-TTS section 4 (RMSNorm variance and RoPE in fp32).
  * q      e16 [B][Hq][D]   new queries (contiguous)
  * k_new  e16 [B][Hkv][D]  new keys, rotated here before they are stored
  * v_new  e16 [B][Hkv][D]  new values, stored bit for bit
@@ -166,16 +170,25 @@ int vh_rope_kv_append(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                       int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
 /* Number of CTAs per kv-head group that vh_paged_decode_attn launches on the
- * current device when num_ctas == 0 (a multiple of the SM count).  Returns a
+ * current device when num_ctas == 0 (a multiple of the SM count).  A host
+ * helper of this library's split plan (the pages have no counterpart; their
+ * kernel picks its split from a CPU upper bound of the length).  Returns a
  * negative VH_E* status on bad shapes or when no device is usable. */
 int vh_decode_num_ctas(int B, int Hq, int Hkv, int D, int page_size);
 
 /* Bytes of workspace vh_paged_decode_attn / vh_decode_combine / vh_decode_fused
  * need for this shape and CTA count (num_ctas == 0: enough for the automatic
- * count of either path on the current device).  Returns 0 on bad arguments. */
+ * count of either path on the current device).  Returns 0 on bad arguments.
+ * A host helper (the pages have no counterpart): the workspace holds the
+ * per-segment partial results of the split rows, see vh_decode_combine. */
 size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int num_ctas);
 
 /* Paged GQA decode attention.
+ * Source: "Engineering TTS inference in vLLM-Omni", Fish Speech S2 Pro,
+ * "model-specific attention kernel": q_len = 1 attention of every request
+ * over its cache blocks, one kv head serving its group of q heads, long
+ * sequences cut into segments that write partial (max, sum, accumulator)
+ * results, the choice made without a device-to-host sync.
  * q_rot float [B][Hq][D] (from vh_rope_kv_append); cache as above.
  * out e16 [B][Hq][D]: rows whose keys one CTA covered entirely are written
  *     here directly; rows with active == 0 (or flagged VH_ERR_SEQLEN) are
@@ -210,7 +223,9 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
                          int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
 /* Merge the partial results of split rows into out (e16 [B][Hq][D]; flags 0 or
- * VH_FLAG_FP16, as given to vh_paged_decode_attn):
+ * VH_FLAG_FP16, as given to vh_paged_decode_attn).  Source: the same Fish
+ * Speech section ("split-partial-combine" for long sequences, merged by the
+ * online-softmax recurrence):
  * M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s (lse in
  * base 2).  Rows that were not split are left as vh_paged_decode_attn wrote
  * them.  Must run after vh_paged_decode_attn on the same stream with the same
@@ -219,7 +234,9 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
 int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out, int num_ctas,
                       unsigned flags, int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
-/* The whole decode step of one layer in ONE launch: optional per-head RMSNorm
+/* The whole decode step of one layer in ONE launch (the steps of
+ * vh_rope_kv_append, vh_paged_decode_attn and vh_decode_combine, with their
+ * sources; the pages run them as separate kernels): optional per-head RMSNorm
  * and RoPE of q and of the new key, append of the new key/value into the
  * cache, attention and the merge of split rows.  Same inputs and outputs as vh_rope_kv_append +
  * vh_paged_decode_attn + vh_decode_combine (apart from q_rot, which is not
@@ -303,7 +320,7 @@ int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k_cache, con
  * Errors: VH_EINVAL (NULL err_flag), VH_EALIGN, VH_ENODEV, VH_ECUDA. */
 int vh_selftest_wait_timeout(int32_t* err_flag, void* stream);
 
-/* Static text for a return code. */
+/* Static text for a return code (a host helper; the pages have no counterpart). */
 const char* vh_status_string(int status);
 
 #ifdef __cplusplus
