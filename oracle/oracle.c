@@ -9,8 +9,8 @@
  *   oracle_rope_kv_append  -- optional per-head RMSNorm, then RoPE on the new
  *                             q and k of every active row at
  *                             position seq_len-1, then the append of the
- *                             rotated k (rounded to bf16) and of v into the
- *                             row's current page;
+ *                             rotated k (rounded to the element type, bf16
+ *                             or fp16) and of v into the row's current page;
  *   oracle_decode_attn     -- single-token GQA attention over the page table,
  *                             written as the plain softmax definition;
  *   oracle_decode_attn_split + oracle_lse_combine
@@ -19,13 +19,14 @@
  *                             log-sum-exp (the long-sequence path), used only
  *                             to check the combine algebra.
  *
- * Numbers: bf16 inputs are read as exact doubles; all arithmetic is float64;
- * the only rounding to a narrow type is the bf16 round-to-nearest-even of the
- * rotated key before it is stored in the cache.
+ * Numbers: bf16 / fp16 inputs are read as exact doubles; all arithmetic is
+ * float64; the only rounding to a narrow type is the round-to-nearest-even of
+ * the rotated key to the element type before it is stored in the cache.
  *
  * Readings of the pages that this file encodes (where they are silent):
- *   - RoPE pairs element i with element i + D/2 ("rotate half") and uses
- *     angle pos * theta^(-2i/D), i = 0 .. D/2-1;
+ *   - RoPE pairs element i with element i + D/2 ("rotate half"), or 2i with
+ *     2i + 1 when asked ("interleaved"), and uses angle pos * theta^(-2i/D),
+ *     i = 0 .. D/2-1;
  *   - the cached keys are stored already rotated; only the new key is rotated;
  *   - seq_len counts the new token, which lands in logical slot seq_len-1;
  *   - the softmax scale is 1/sqrt(D) unless the caller passes another;
@@ -183,7 +184,7 @@ static void rope_rotate(double* x, int D, double pos, double theta, int interlea
  * q_norm_w, k_norm_w: per-dim RMSNorm weights [D] applied to every q / new-k
  *   head before RoPE, or NULL for none; norm_eps is the epsilon.
  * q_rot: float64 [B][Hq][D] out; rows with active == 0 are left untouched.
- * k_rot: float64 [B][Hkv][D] out or NULL: the rotated key before its bf16
+ * k_rot: float64 [B][Hkv][D] out or NULL: the rotated key before its
  *        rounding (rows that are skipped are left untouched).
  * k_pre: float64 [B][Hkv][D] out or NULL: the key fed to RoPE (after the
  *        RMSNorm when there is one).
