@@ -18,9 +18,9 @@
 //
 // Design for GB300 (HBM-bound: 2-4 flops per byte of K/V):
 //  * Work list.  Every active row contributes ceil(L/16) tiles of 16 tokens;
-//    the list of all tiles in row order is cut into N equal contiguous
-//    ranges, one per CTA, on the device (each CTA prefix-sums the row tile
-//    counts in shared memory).  No host sync, a static grid, and the load is
+//    the list of all tiles in row order is cut into N contiguous ranges
+//    that differ by at most one tile, one per CTA, on the device (each CTA
+//    prefix-sums the row tile counts in shared memory).  No host sync, a static grid, and the load is
 //    balanced to within one tile whatever the length mix; a row is split
 //    where its tiles straddle two CTAs (at most two partial segments per CTA).
 //  * Data movement.  One producer warp streams each tile into a ring of
@@ -60,13 +60,20 @@ namespace {
 constexpr int kMaxHc = 8;                    // kv heads (consumer warps) per CTA
 constexpr int kThreadsMax = 32 * (kMaxHc + 2);  // consumers, producer, merge warp
 
+// CTA c of n takes q = T / n tiles, and the first r = T mod n CTAs one more:
+// they are the first launched, so under programmatic dependent launch (CTAs
+// entering as the previous kernel's leave) the extra tiles go to the CTAs
+// that start streaming first.
 __device__ __forceinline__ long long range_begin(int c, int n_eff, long long T) {
-  return (static_cast<long long>(c) * T) / n_eff;
+  const long long q = T / n_eff, r = T - q * n_eff;
+  return static_cast<long long>(c) * q + min(static_cast<long long>(c), r);
 }
 
-// CTA whose range [c T / n, (c+1) T / n) holds tile s.
+// CTA whose range holds tile s (n_eff <= T, so q >= 1).
 __device__ __forceinline__ int cta_of(long long s, int n_eff, long long T) {
-  return static_cast<int>(((s + 1) * n_eff - 1) / T);
+  const long long q = T / n_eff, r = T - q * n_eff;
+  const long long big = r * (q + 1);  // tiles of the first r CTAs
+  return static_cast<int>(s < big ? s / (q + 1) : r + (s - big) / q);
 }
 
 // In-place inclusive prefix sum of cum[1..n] (cum[0] = 0 already).
