@@ -64,16 +64,17 @@ constexpr int kThreadsMax = 32 * (kMaxHc + 2);  // consumers, producer, merge wa
 // they are the first launched, so under programmatic dependent launch (CTAs
 // entering as the previous kernel's leave) the extra tiles go to the CTAs
 // that start streaming first.
+// (The tile list has fewer than 2^31 tiles, so 32-bit arithmetic is exact.)
 __device__ __forceinline__ long long range_begin(int c, int n_eff, long long T) {
-  const long long q = T / n_eff, r = T - q * n_eff;
-  return static_cast<long long>(c) * q + min(static_cast<long long>(c), r);
+  const int q = static_cast<int>(T) / n_eff, r = static_cast<int>(T) - q * n_eff;
+  return static_cast<long long>(c * q + min(c, r));
 }
 
 // CTA whose range holds tile s (n_eff <= T, so q >= 1).
 __device__ __forceinline__ int cta_of(long long s, int n_eff, long long T) {
-  const long long q = T / n_eff, r = T - q * n_eff;
-  const long long big = r * (q + 1);  // tiles of the first r CTAs
-  return static_cast<int>(s < big ? s / (q + 1) : r + (s - big) / q);
+  const int q = static_cast<int>(T) / n_eff, r = static_cast<int>(T) - q * n_eff;
+  const int big = r * (q + 1), si = static_cast<int>(s);  // tiles of the first r CTAs
+  return si < big ? si / (q + 1) : r + (si - big) / q;
 }
 
 // In-place inclusive prefix sum of cum[1..n] (cum[0] = 0 already).
