@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   __syncthreads();
   block_inclusive_scan(cum, p.B, misc + kMiscWarpTot);
   const long long T = cum[p.B];
-  const int n_eff =
-      T == 0 ? 0 : static_cast<int>(min(static_cast<long long>(p.N), (T + p.min_tiles - 1) / p.min_tiles));
+  // (T < 2^31: 32-bit arithmetic is exact)
+  const int n_eff = T == 0 ? 0 : min(p.N, (static_cast<int>(T) + p.min_tiles - 1) / p.min_tiles);
 
   // This CTA's tile range and its first row.
   const long long t0_pre = n_eff > 0 ? range_begin(c, n_eff, T) : 0;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     for (long long t = t0_pre; t < t0_pre + n; ++t) {
       while (t >= rt1) rt1 = cum[++b + 1];
       const long long rt0 = cum[b];
-      const int tin_page = static_cast<int>((t - rt0) % tpp);
+      const int tin_page = static_cast<int>(t - rt0) % tpp;
       int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - t0_pre));
       const bool page_ok = page >= 0 && page < p.num_pages;
       if (!page_ok) page = 0;  // flagged again after the wait
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     long long wb = t0;
     int b = b0;
     long long rt0 = cum[b], rt1 = cum[b + 1];
-    int tin_page = static_cast<int>((t0 - rt0) % tpp);  // tile index within its page
+    int tin_page = static_cast<int>(t0 - rt0) % tpp;  // tile index within its page
     int stage = 0, round = 0, nseg = 0;
     long long issued = 0;
     bool aborted = false;
