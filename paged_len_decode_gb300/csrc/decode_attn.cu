@@ -29,9 +29,9 @@
 //    through a second mbarrier.  The cache is described to the copy engine as
 //    a 4-D tensor (head_dim, token, kv head, page) whose strides come from the
 //    caller, so token-major and head-major pages take the same path: per
-//    64-element column block and per 8-token group, one box holds all of the
-//    CTA's kv heads (8 copies per 16-token tile at head_dim 128), and the
-//    second group is skipped when a row's last tile has at most 8 tokens.
+//    64-element column block, one box of 16 tokens x all of the CTA's kv
+//    heads (4 copies per tile at head_dim 128); a row's last tile with at
+//    most 8 live tokens takes one-head boxes of 8 tokens instead.
 //    Boxes land with the 128-byte swizzle, so ldmatrix reads of 8 rows at the
 //    same column hit 8 different bank groups without padding.  The q rows of
 //    the next segment are copied (plain bulk copy) into a staging buffer
@@ -297,32 +297,18 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   }
   // ---- producer's box layout (used before and after the wait) --------------
   const int h0 = gy * Hc;
-  // The tile's copies are boxes of box_heads heads x 8 tokens x 128 bytes:
-  // for K and for V, per 64-element column block hf, per 8-token group g
-  // and per group of box_heads heads.  Box j lands at [hf][g][head][token]
-  // in the K or V half of the stage; lane l issues boxes l and l + 32.  The
-  // same boxes serve token-major and head-major pages (the tensor map holds
-  // the strides).  Group g = 1 is skipped when the tile has <= 8 tokens.
-  const int HG_BOX = Hc / p.box_heads;  // head groups per (column block, token group)
-  const int NB = HALVES * 2 * HG_BOX;   // boxes of K (and of V) per tile
-  int bx_g[2], bx_hf[2], bx_head[2];
-  const void* bx_map[2];
-  uint32_t bx_off[2];
-  bool bx_on[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int j = lane + 32 * u;
-    bx_on[u] = j < 2 * NB;
-    const int kv = j >= NB ? 1 : 0, rem = j - kv * NB;
-    const int hf = rem / (2 * HG_BOX), rem2 = rem - hf * 2 * HG_BOX;
-    const int g = rem2 / HG_BOX, hq = rem2 - g * HG_BOX;
-    bx_g[u] = g;
-    bx_hf[u] = hf;
-    bx_head[u] = h0 + hq * p.box_heads;
-    bx_map[u] = kv ? static_cast<const void*>(&p.tmap_v) : static_cast<const void*>(&p.tmap_k);
-    bx_off[u] = static_cast<uint32_t>(kv * (p.stage_bytes / 2) + hf * Hc * 2048 + g * Hc * 1024 +
-                                      hq * p.box_heads * 1024);
-  }
+  // The tile's copies land at [64-column block hf][head][16 tokens][128 B] of
+  // the K or V half of the stage.  Full tiles (more than 8 live tokens): one
+  // box of 16 tokens x Hc heads per (K or V, hf), lanes 0 .. 2*HALVES-1.
+  // Tiles with at most 8 live tokens, and every tile when full_boxes == 0: one
+  // box of 8 tokens x 1 head per (K or V, hf, head, 8-token group), lane
+  // (((group * Hc + head) * HALVES + hf) * 2 + kv).
+  const int l_kv = lane & 1, l_hf = (lane >> 1) % HALVES;
+  const int l_head = (lane / (2 * HALVES)) % Hc, l_g = lane / (2 * HALVES * Hc);
+  const void* l_map16 = l_kv ? static_cast<const void*>(&p.tmap_v) : static_cast<const void*>(&p.tmap_k);
+  const void* l_map8 = l_kv ? static_cast<const void*>(&p.tmap_v8) : static_cast<const void*>(&p.tmap_k8);
+  const uint32_t l_off16 = static_cast<uint32_t>(l_kv * (p.stage_bytes / 2) + l_hf * Hc * 2048);
+  const uint32_t l_off8 = l_off16 + static_cast<uint32_t>(l_head * 2048 + l_g * 1024);
   // Tile state of the producer: stage ring position and, for tile t of row
   // b, its box coordinates, the append slot and the bytes its boxes deliver.
   int npre = 0;  // tiles whose boxes were requested before the wait
@@ -349,13 +335,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       mbar_arrive_expect_tx(fb, tx);
     }
     __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (bx_on[u] && (two_groups || bx_g[u] == 0)) {
-        const int tk = tokc + 8 * bx_g[u];
-        const int c1 = p.tm_tok_dim == 1 ? tk : bx_head[u], c2 = p.tm_tok_dim == 1 ? bx_head[u] : tk;
-        tma_load_4d(st + bx_off[u], bx_map[u], bx_hf[u] * 64, c1, c2, page, fb);
-      }
+    if (two_groups && p.full_boxes) {
+      if (lane < 2 * HALVES) tma_load_4d(st + l_off16, l_map16, l_hf * 64, tokc, h0, page, fb);
+    } else if (lane < 2 * HALVES * Hc * (two_groups ? 2 : 1)) {
+      const int tk = tokc + 8 * l_g;
+      const int c1 = p.tm_tok_dim == 1 ? tk : h0 + l_head, c2 = p.tm_tok_dim == 1 ? h0 + l_head : tk;
+      tma_load_4d(st + l_off8, l_map8, l_hf * 64, c1, c2, page, fb);
     }
   };
   if (FUSED && p.prefetch_kv && warp == Hc && c < n_eff) {
@@ -552,12 +537,10 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   const int ka_row = (lane & 7) + 8 * ((lane >> 3) & 1);
   const int va_row = (lane & 7) + 8 * (lane >> 4);
   const int ksw = (lane >> 4) ^ (ka_row & 7), vsw = ((lane >> 3) & 1) ^ (va_row & 7);
-  // Stage layout of K (and then V): [64-column block][8-token group][head][8 tokens][128 B];
-  // row r of head w of a column block is at row_off(r) + w * 1024.
+  // Stage layout of K (and then V): [64-column block][head][16 tokens][128 B];
+  // row r of head w of a column block is at row_off(r).
   const uint32_t half_bytes = static_cast<uint32_t>(Hc) * 2048u;  // one 64-column block of all heads
-  auto row_off = [&](int r) -> uint32_t {
-    return static_cast<uint32_t>((r >> 3) * Hc * 1024 + w * 1024 + (r & 7) * 128);
-  };
+  auto row_off = [&](int r) -> uint32_t { return static_cast<uint32_t>(w * 2048 + r * 128); };
   const uint32_t k_lane = row_off(ka_row);
   const uint32_t v_lane = static_cast<uint32_t>(p.stage_bytes / 2) + row_off(va_row);
 
@@ -752,7 +735,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       *abort_flag = 1;
       return;
     }
-    // this stage: K boxes [D/64][2][Hc][8][128 B], then V boxes, all swizzled
+    // this stage: K boxes [D/64][Hc][16][128 B], then V boxes, all swizzled
     unsigned char* stg = smem + static_cast<long long>(stage) * p.stage_bytes;
     unsigned char* vst = stg + p.stage_bytes / 2;
     bool touched = false;

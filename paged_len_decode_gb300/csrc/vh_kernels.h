@@ -38,12 +38,15 @@ struct RopeAppendParams {
 // Shared-memory plan of the attention kernel (byte offsets from the dynamic
 // shared-memory base, rounded up to 1024 bytes) and the split plan parameters.
 struct AttnParams {
-  // K and V caches as 4-D tensors (head_dim, then token and head in stride
-  // order, then page) with 64-element x 16-token boxes and the 128-byte swizzle
+  // K and V caches as 4-D tensors (head_dim, token, kv head, page) with the
+  // 128-byte swizzle: boxes of 64 elements x 16 tokens x Hc heads for full
+  // tiles (tmap_k, tmap_v), and of 64 x 8 tokens x 1 head (tmap_k8, tmap_v8)
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
-  int tm_tok_dim;              // tensor-map dimension of the token index (1 or 2; the head index is the other)
-  int box_heads;               // kv heads per box: Hc (one box per 64-column block) or 1
+  CUtensorMap tmap_k8;
+  CUtensorMap tmap_v8;
+  int tm_tok_dim;              // dimension of the token index in the 8-token maps (1 or 2; the head is the other)
+  int full_boxes;              // 1: full tiles take the 16-token maps; 0: every tile takes 8-token boxes
   // attention over the cache (both kernels)
   const float* q_rot;          // [B][Hq][D] fp32 rotated q (three-call path)
   const uint16_t* k_cache;

@@ -208,13 +208,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Tensor maps of the K and V caches for the attention kernel's tile copies:
 // 4-D tensors of 16-bit elements (dimension 0 = head_dim, 3 = page) with the
-// 128-byte swizzle, boxes of 64 elements x 8 tokens x box_heads heads, which
-// land in shared memory as [head][token][128 bytes].  Preferred: dimension
-// 1 = token, 2 = head and box_heads = Hc, so a tile is two boxes (token
-// groups) per 64-column block of K and of V.  If the encoder rejects that order (the strides of
-// token-major pages decrease from dimension 1 to 2), dimensions 1 and 2 are
-// token and head in increasing stride order and each box holds one head.
-// Sets p.tm_tok_dim and p.box_heads.  Returns false if no encoding is accepted.
+// 128-byte swizzle.  Full tiles: boxes of 64 elements x 16 tokens x Hc heads
+// (dimension 1 = token, 2 = head), landing in shared memory as
+// [head][16 tokens][128 bytes]; tiles with at most 8 live tokens: boxes of
+// 64 x 8 tokens x 1 head into the first 8 rows of each head.  Token-major
+// pages give dimensions 1 and 2 decreasing strides; if the encoder rejects
+// that order (or VH_TMA_BOX_HEADS=1, for testing), the 8-token maps take the
+// token and head dimensions in increasing stride order and every tile is
+// copied as 8-token boxes (p.full_boxes = 0).  Returns false if no encoding
+// is accepted.
 bool encode_cache_maps(AttnParams& p) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
@@ -227,27 +229,37 @@ bool encode_cache_maps(AttnParams& p) {
     default: break;
   }
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  auto encode = [&](bool tok_first, cuuint32_t heads) -> bool {
+  // one pair of maps (K, V) with token and head in the given dimension order
+  auto encode = [&](CUtensorMap* mk, CUtensorMap* mv, bool tok_first, cuuint32_t tokens,
+                    cuuint32_t heads) -> bool {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.D), static_cast<cuuint64_t>(tok_first ? p.P : p.Hkv),
                                 static_cast<cuuint64_t>(tok_first ? p.Hkv : p.P),
                                 static_cast<cuuint64_t>(p.num_pages)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(2 * (tok_first ? p.token_stride : p.head_stride)),
                                    static_cast<cuuint64_t>(2 * (tok_first ? p.head_stride : p.token_stride)),
                                    static_cast<cuuint64_t>(2 * p.page_stride)};
-    const cuuint32_t box[4] = {64, tok_first ? 8u : 1u, tok_first ? heads : 8u, 1};
+    const cuuint32_t box[4] = {64, tok_first ? tokens : heads, tok_first ? heads : tokens, 1};
     for (int kv = 0; kv < 2; ++kv) {
-      CUtensorMap* m = kv ? &p.tmap_v : &p.tmap_k;
       void* base = const_cast<uint16_t*>(kv ? p.v_cache : p.k_cache);
-      if (enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      if (enc(kv ? mv : mk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     }
-    p.tm_tok_dim = tok_first ? 1 : 2;
-    p.box_heads = static_cast<int>(heads);
     return true;
   };
-  if (env_int("VH_TMA_BOX_HEADS", 0) != 1 && encode(true, static_cast<cuuint32_t>(p.Hc))) return true;
-  return encode(p.token_stride <= p.head_stride, 1);
+  const bool forced = env_int("VH_TMA_BOX_HEADS", 0) == 1;
+  if (!forced && encode(&p.tmap_k, &p.tmap_v, true, 16, static_cast<cuuint32_t>(p.Hc)) &&
+      encode(&p.tmap_k8, &p.tmap_v8, true, 8, 1)) {
+    p.full_boxes = 1;
+    p.tm_tok_dim = 1;
+    return true;
+  }
+  const bool tok_first = p.token_stride <= p.head_stride;
+  if (!encode(&p.tmap_k8, &p.tmap_v8, tok_first, 8, 1)) return false;
+  p.full_boxes = 0;
+  p.tm_tok_dim = tok_first ? 1 : 2;
+  return true;
 }
 
 bool too_many_tiles(int B, int max_pages_per_seq, int P) {

@@ -47,7 +47,8 @@ struct WsLayout {
 WsLayout ws_layout(int B, int Hq, int Hkv, int D, int N);
 
 // Tensor maps of the K and V caches for the tile copies (sets p.tmap_k,
-// p.tmap_v, p.tm_tok_dim, p.box_heads).  False if the encoder rejects them.
+// p.tmap_v, p.tmap_k8, p.tmap_v8, p.tm_tok_dim, p.full_boxes).  False if the
+// encoder rejects them.
 bool encode_cache_maps(AttnParams& p);
 
 }  // namespace vh

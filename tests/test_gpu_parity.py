@@ -457,3 +457,17 @@ def test_batch_near_the_plan_limit(path):
                               device="cuda", max_pages_per_seq=3)
     rows = list(range(0, B, 97))  # the oracle checks a sample of rows; the append is checked everywhere
     H.full_check(inp, path=path, rows=rows)
+
+
+# ---------------------------------------------------------------- fallback tile copies
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_one_head_box_fallback(layout, path, monkeypatch):
+    # the copy path used if the tensor-map encoder rejected the multi-head box
+    # order: every tile as one-head 8-token boxes, dimensions in stride order
+    monkeypatch.setenv("VH_TMA_BOX_HEADS", "1")
+    inp = workloads.make_inputs("c64", device="cuda", layout=layout)
+    H.full_check(inp, path=path)
+    inp = case([17, 9, 300, 1], Hq=16, Hkv=8, D=64, seed=95, layout=layout, dtype=torch.float16)
+    H.full_check(inp, path=path, interleaved=True)
