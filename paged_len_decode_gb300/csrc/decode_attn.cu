@@ -33,7 +33,10 @@
 //    heads (4 copies per tile at head_dim 128); a row's last tile with at
 //    most 8 live tokens takes one-head boxes of 8 tokens instead.
 //    Boxes land with the 128-byte swizzle, so ldmatrix reads of 8 rows at the
-//    same column hit 8 different bank groups without padding.  The q rows of
+//    same column hit 8 different bank groups without padding.  Right after
+//    the dependency wait the tile after the first stages is prefetched into
+//    L2 (tensor prefetch, no shared memory), so the stream's start does not
+//    wait on HBM latency while the q rows arrive.  The q rows of
 //    the next segment are copied (plain bulk copy) into a staging buffer
 //    while the current segment is still being consumed.
 //  * Math on tensor cores.  One consumer warp per kv head.  With 16 keys per
@@ -274,13 +277,18 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   // The producer's first page ids are read before the wait as well.
   // tiles per page (P is a multiple of 16, or a row has one page of any size)
   const int tpp = (p.P + kTile - 1) / kTile;
-  auto tile_page = [&](long long tt) -> int {
-    if (tt >= t1_pre) return 0;
-    int lo = b0_pre, hi = p.B - 1;  // row of tile tt: first row with cum[row + 1] > tt
+  // row of tile tt of this CTA's range: first row with cum[row + 1] > tt
+  auto row_of_from = [&](long long tt) -> int {
+    int lo = b0_pre, hi = p.B - 1;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
       if (cum[mid + 1] > tt) hi = mid; else lo = mid + 1;
     }
+    return lo;
+  };
+  auto tile_page = [&](long long tt) -> int {
+    if (tt >= t1_pre) return 0;
+    const int lo = row_of_from(tt);
     const int tk = static_cast<int>(tt - cum[lo]);
     const long long lp = static_cast<long long>(lo) * p.max_pages_per_seq + tk / tpp;
     // no page table: a contiguous cache, row b's pages are b * max_pages_per_seq + j
@@ -341,6 +349,27 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       const int tk = tokc + 8 * l_g;
       const int c1 = p.tm_tok_dim == 1 ? tk : h0 + l_head, c2 = p.tm_tok_dim == 1 ? h0 + l_head : tk;
       tma_load_4d(st + l_off8, l_map8, l_hf * 64, c1, c2, page, fb);
+    }
+  };
+  // L2 prefetch (no shared memory, no completion) of this CTA's tiles [ta, tb),
+  // tb - t0 <= 32 (page ids from the first window)
+  auto prefetch_l2 = [&](long long ta, long long tb) {
+    int b = row_of_from(ta);
+    long long rt1 = cum[b + 1];
+    for (long long t = ta; t < tb; ++t) {
+      while (t >= rt1) rt1 = cum[++b + 1];
+      const long long rt0 = cum[b];
+      const int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - t0_pre));
+      if (page < 0 || page >= p.num_pages) continue;  // flagged when the tile is copied
+      const int nvalid = min(kTile, lens[b] - static_cast<int>(t - rt0) * kTile);
+      const int tokc = (static_cast<int>(t - rt0) % tpp) * kTile;
+      if (nvalid > 8 && p.full_boxes) {
+        if (lane < 2 * HALVES) tma_prefetch_l2_4d(l_map16, l_hf * 64, tokc, h0, page);
+      } else if (lane < 2 * HALVES * Hc * (nvalid > 8 ? 2 : 1)) {
+        const int tk = tokc + 8 * l_g;
+        const int c1 = p.tm_tok_dim == 1 ? tk : h0 + l_head, c2 = p.tm_tok_dim == 1 ? h0 + l_head : tk;
+        tma_prefetch_l2_4d(l_map8, l_hf * 64, c1, c2, page);
+      }
     }
   };
   if (FUSED && p.prefetch_kv && warp == Hc && c < n_eff) {
@@ -490,6 +519,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
           }
         }
         ++nseg;
+        if (t == t0 && p.l2_tiles > 0) {
+          // while the q rows and the first stages arrive, the next tiles
+          // (which have no free stage yet) are read into L2
+          const long long ta = t0 + S;
+          prefetch_l2(ta, min(t1, min(t0 + 32, ta + p.l2_tiles)));
+        }
       }
       // the boxes of this tile (the new token's row arrives as whatever the
       // cache slot holds; the consumers overwrite it with the rotated key and

@@ -163,6 +163,19 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   return static_cast<size_t>(p.smem_bytes) <= budget;
 }
 
+// Fused launches that request their first stages before the dependency wait
+// (VH_FLAG_PDL_KV): right after the wait, while the q rows are in flight,
+// each CTA prefetches the next kL2PrefetchTiles tiles (no free stage yet) into
+// L2, so the start of the stream does not wait for HBM.  One tile measured
+// best (c64 30.19 -> 29.81 us, padded 13.41 -> 12.90 us, long 62.0 -> 61.6 us);
+// more delay the q copies that gate the consumers; the same prefetch issued
+// before the wait slowed the previous kernel's end, and in launches without
+// early stages (three-call attention, fused without PDL) it cost 1.2-1.4 us
+// (VH_DECODE_L2_TILES, for tuning; at most 30, the page-id window).
+constexpr int kL2PrefetchTiles = 1;
+
+int l2_prefetch_tiles() { return std::min(30, std::max(0, env_int("VH_DECODE_L2_TILES", kL2PrefetchTiles))); }
+
 int auto_ctas(const AttnParams& p, const DeviceInfo& dev) {
   int per_sm = 0;
   if (vh::decode_attn_occupancy(p, &per_sm) != cudaSuccess || per_sm < 1) {

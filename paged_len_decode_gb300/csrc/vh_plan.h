@@ -37,6 +37,9 @@ int env_int(const char* name, int dflt);
 bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused);
 // CTAs per head group: resident CTAs per SM times the SM count.
 int auto_ctas(const AttnParams& p, const DeviceInfo& dev);
+// Tiles per CTA prefetched into L2 right after the dependency wait, beyond
+// those the pipeline stages take first.
+int l2_prefetch_tiles();
 
 // Workspace: per-row split plan (int4 [B]); per-(head group, row) counters of
 // the fused merge (int [Hkv][B], an upper bound on groups); partial lse
