@@ -113,6 +113,15 @@ def test_forced_cta_counts_agree(num_ctas, path):
     H.full_check(inp, num_ctas=num_ctas, path=path)
 
 
+@pytest.mark.parametrize("path", H.PATHS)
+def test_rows_split_into_many_pieces(path):
+    # 700 CTAs per head group: rows of up to 512 tiles split into ~70 pieces,
+    # so the fused merge takes several rounds of staged pieces (8 per round at
+    # G = 4) and the three-call combine several register batches
+    inp = workloads.make_inputs("long", device="cuda")
+    H.full_check(inp, num_ctas=700, path=path)
+
+
 def test_split_count_changes_only_rounding():
     inp = workloads.make_inputs("long", device="cuda")
     a = H.run_step(inp, num_ctas=1)["out"].double()
