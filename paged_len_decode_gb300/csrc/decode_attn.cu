@@ -33,12 +33,13 @@
 //    heads (4 copies per tile at head_dim 128); a row's last tile with at
 //    most 8 live tokens takes one-head boxes of 8 tokens instead.
 //    Boxes land with the 128-byte swizzle, so ldmatrix reads of 8 rows at the
-//    same column hit 8 different bank groups without padding.  Right after
-//    the dependency wait the tile after the first stages is prefetched into
-//    L2 (tensor prefetch, no shared memory), so the stream's start does not
-//    wait on HBM latency while the q rows arrive.  The q rows of
-//    the next segment are copied (plain bulk copy) into a staging buffer
-//    while the current segment is still being consumed.
+//    same column hit 8 different bank groups without padding.  In launches
+//    that request their first stages before the dependency wait, the tile
+//    after them is prefetched into L2 right after the wait (tensor prefetch,
+//    no shared memory), so the stream's start does not wait on HBM latency
+//    while the q rows arrive.  The q rows of the next segment are copied
+//    (plain bulk copy) into a staging buffer while the current segment is
+//    still being consumed.
 //  * Math on tensor cores.  One consumer warp per kv head.  With 16 keys per
 //    tile and the G q heads of the kv head padded to 8, the scores are one
 //    m16n8 tile: S^T (keys x heads) = K (keys x D) . q^T, and the output is
