@@ -1,0 +1,65 @@
+"""Seeded random sweep of both CUDA paths against the float64 oracle.
+
+Each case draws its own shape and options from its seed: batch size, GQA
+group, kv heads, head_dim, page size, a length mix (one-token rows, lengths
+on and just past page boundaries, random lengths up to several hundred
+tokens), padding rows, element type, page layout (token-major, head-major,
+contiguous per-row caches), RoPE pairing, RMSNorm of q and k, the CTA count,
+CUDA-graph replay and, on the fused path, programmatic dependent launch with
+and without early K/V requests.  Every case checks q_rot (three-call path),
+the append bits and the output exactly as the named parity tests do."""
+import random
+
+import pytest
+import torch
+
+import gpu_harness as H
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _draw(seed):
+    r = random.Random(seed)
+    G, Hkv, D = r.choice([1, 2, 4, 8]), r.choice([1, 2, 4, 8]), r.choice([64, 128])
+    layout = r.choice(["NHD", "NHD", "HND", "CONTIG"])
+    if layout == "CONTIG":
+        P, mps, maxlen = r.choice([11, 16, 32, 100]), 1, None
+        maxlen = P
+    else:
+        P, mps, maxlen = r.choice([16, 32, 64]), None, r.choice([64, 300, 900])
+    B = r.randint(1, 24)
+    lens = []
+    for _ in range(B):
+        u = r.random()
+        if u < 0.15:
+            lens.append(1)
+        elif u < 0.45:
+            k = P * r.randint(1, max(1, maxlen // P))
+            lens.append(min(maxlen, k + (1 if u >= 0.35 else 0)))
+        else:
+            lens.append(r.randint(1, maxlen))
+    active = [0 if r.random() < 0.15 else 1 for _ in range(B)]
+    if not any(active):
+        active[r.randrange(B)] = 1
+    lens = [L if a else 1 for L, a in zip(lens, active)]
+    dtype = r.choice([torch.bfloat16, torch.float16])
+    path = r.choice(H.PATHS)
+    opts = {"path": path, "num_ctas": r.choice([0, 0, 0, 1, 3, 17, 200]), "interleaved": r.random() < 0.3,
+            "graph": r.random() < 0.2}
+    if r.random() < 0.3:
+        g = torch.Generator().manual_seed(seed)
+        opts["norm"] = {"q": (1.0 + 0.2 * torch.randn(D, generator=g)).float(),
+                        "k": (1.0 + 0.2 * torch.randn(D, generator=g)).float(), "eps": 1e-6}
+    if path == "fused" and r.random() < 0.5:
+        opts["pdl"] = True
+        opts["pdl_kv"] = r.random() < 0.5
+    inp = workloads.make_case(B=B, Hq=G * Hkv, Hkv=Hkv, D=D, P=P, seq_lens=lens, active=active,
+                              max_pages_per_seq=mps, seed=seed, device="cuda", dtype=dtype, layout=layout)
+    return inp, opts
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_case_matches_oracle(seed):
+    inp, opts = _draw(9000 + seed)
+    H.full_check(inp, **opts)
