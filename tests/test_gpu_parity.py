@@ -122,6 +122,14 @@ def test_rows_split_into_many_pieces(path):
     H.full_check(inp, num_ctas=700, path=path)
 
 
+@pytest.mark.parametrize("path", H.PATHS)
+def test_single_very_long_row(path):
+    # one row of 32768 tokens (2048 tiles) with G = 4: every CTA of a head
+    # group takes a piece of it, so one CTA merges ~150 pieces
+    inp = case([32768], Hq=32, Hkv=8, seed=11)
+    H.full_check(inp, path=path)
+
+
 def test_split_count_changes_only_rounding():
     inp = workloads.make_inputs("long", device="cuda")
     a = H.run_step(inp, num_ctas=1)["out"].double()
