@@ -72,6 +72,9 @@ def parse():
     ap.add_argument("--pdl-kv", type=int, default=1,
                     help="fused steps request their first cached K/V tiles before the wait on the "
                          "previous step (VH_FLAG_PDL_KV; each step reads another pool)")
+    ap.add_argument("--pdl", type=int, default=1,
+                    help="programmatic dependent launch between the timed fused steps (1/0; 0 also turns "
+                         "off the early K/V requests)")
     ap.add_argument("--e2e-pdl", type=int, default=0,
                     help="programmatic dependent launch between the pipelined e2e steps (1/0)")
     ap.add_argument("--qk-norm", action="store_true",
@@ -424,7 +427,7 @@ def run_ours(args, rank, world):
     s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm, dtype=args.dtype,
               interleaved=args.interleaved, layout=args.layout)
     inp, R, L = s.inp, s.R, s.L
-    s.pdl_kv = bool(args.pdl_kv) and R > 1  # consecutive steps read different pools
+    s.pdl_kv = bool(args.pdl_kv) and bool(args.pdl) and R > 1  # consecutive steps read different pools
     by = s.step_bytes()
 
     for r in range(R):  # first calls outside capture (launch attributes, every replica's new slot)
@@ -476,7 +479,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
 
     clocks = Clocks(dev.index)
-    ms_fused_total, ck = timed(s.fused, args.steps * L, clocks)  # L layer calls per step
+    ms_fused_total, ck = timed(lambda r: s.fused(r, pdl=bool(args.pdl)), args.steps * L, clocks)  # L calls per step
     ms_step = ms_fused_total / args.steps
     ms_three_total, _ = timed(s.three, args.steps * L)
     ms_three = ms_three_total / args.steps
@@ -499,8 +502,9 @@ def run_ours(args, rank, world):
                                f"D={s.D}, P={s.P}, lengths {w.dist} [{w.len_lo},{w.len_hi}]",
                    "global_batch": s.B * world, "kv_bytes_per_step": by["kv"],
                    "step": (f"{L} layer calls, " if L > 1 else "") +
-                           "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, "
-                           "PDL between launches" + (", first cached K/V tiles requested before the wait "
+                           "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, " +
+                           ("PDL between launches" if args.pdl else "no PDL between launches") +
+                           (", first cached K/V tiles requested before the wait "
                                                      "(VH_FLAG_PDL_KV)" if s.pdl_kv else ""),
                    "layers": L, "qk_norm": bool(args.qk_norm), "rope": "interleaved" if args.interleaved
                    else "rotate-half", "elements": args.dtype, "pages": s.inp.layout,
