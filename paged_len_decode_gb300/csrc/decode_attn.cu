@@ -394,6 +394,23 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   }
   pdl_wait();
 
+  // The first segment's q rows (and, fused, its RoPE row) are requested at
+  // once by thread 0: the consumers cannot start before they arrive, and the
+  // producer may still be busy with the requests it makes before the wait
+  // (page ids, first stages).  Later segments' q rows come from the producer.
+  const bool early_q = p.early_q && c < n_eff;
+  if (early_q && tid == 0) {
+    mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));
+    const long long qrow = static_cast<long long>(b0_pre) * p.Hq + static_cast<long long>(h0) * G;
+    const uint32_t qdst = smem_addr(smem + p.q_off);
+    if constexpr (FUSED) {
+      bulk_g2s(qdst, p.q + qrow * D, HG * D * 2, qfull);
+      bulk_g2s(qdst + HG * p.q_row_bytes, p.cos_sin + static_cast<long long>(posv[b0_pre]) * D, D * 4, qfull);
+    } else {
+      bulk_g2s(qdst, p.q_rot + qrow * D, HG * D * 4, qfull);
+    }
+  }
+
   // ---- per-row duties, rows b = c (mod N): split plan, zero padding rows ---
   for (int b = c; b < p.B; b += p.N) {
     const int nt = cum[b + 1] - cum[b];
@@ -507,7 +524,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
           aborted = true;
           break;
         }
-        if (lane == 0) {
+        if (lane == 0 && !(nseg == 0 && early_q)) {
           // the q rows of the segment's row (one contiguous copy) and, fused, the RoPE row
           mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));
           const long long qrow = static_cast<long long>(b) * p.Hq + static_cast<long long>(h0) * G;

@@ -207,6 +207,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
   p.part_o = reinterpret_cast<float*>(ws + w.o);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.early_q = vh::env_int("VH_DECODE_EARLY_Q", 1) != 0;
   return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), (flags & VH_FLAG_PDL) != 0) == cudaSuccess
              ? VH_OK
              : VH_ECUDA;
@@ -318,6 +319,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   p.part_o = reinterpret_cast<float*>(ws + w.o);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.early_q = vh::env_int("VH_DECODE_EARLY_Q", 1) != 0;
   p.prefetch_kv = (flags & VH_FLAG_PDL_KV) != 0;
   // with the first stages requested before the wait (launches without it measured slower)
   p.l2_tiles = p.prefetch_kv ? vh::l2_prefetch_tiles() : 0;
