@@ -1,28 +1,39 @@
 """Benchmark of the paged q_len=1 decode step (RoPE + append, attention, merge).
 
-Default workload: the c=64 Talker decode batch (64 rows, 16 q / 8 kv heads,
+Headline workload: the c=64 Talker decode batch (64 rows, 16 q / 8 kv heads,
 head_dim 128, pages of 16 tokens, lengths uniform in [200, 1200]).  A "step"
-is the whole path for one layer over the batch.  The headline runs it as one
-launch (vh_decode_fused), each step a programmatic dependent of the previous
-one; the three-call form (vh_rope_kv_append, vh_paged_decode_attn,
-vh_decode_combine) is timed beside it.  Metric: decode tokens/s (active rows
-per layer call per second) and the achieved HBM GB/s of the step.
+is the whole path for one layer over the batch (for the 28-layer workload,
+all 28 layer calls).  The headline runs it as one launch (vh_decode_fused),
+each step a programmatic dependent of the previous one; the same steps
+without programmatic dependent launch (`no_pdl`) and the three-call form
+(vh_rope_kv_append, vh_paged_decode_attn, vh_decode_combine) are timed
+beside it.  Metric: decode tokens/s (active rows per layer call per second)
+and the achieved HBM GB/s of the step, as a fraction of the measured copy
+bandwidth and of the 8 TB/s HBM3e specification.  The default run also
+measures the long-context, padded-batch and 28-layer high-concurrency
+workloads (`workloads` in the JSON line).
 
-Timing: inputs resident in HBM; K steps captured in CUDA graphs that cycle
-over enough KV-pool replicas to exceed 4x the L2 size, so every step reads
-its K/V from HBM; CUDA events on the launching stream, synchronize and a
-barrier on both sides, max over ranks.  `e2e` goes through the public Python
-call with pinned host buffers: per step the new q/k/v, lengths, flags and page
-table (one input arena) are copied in and the output is copied out.  The
-headline e2e replays a CUDA graph of many steps with two input arenas and two
-outputs, the copies on their own streams overlapping the neighbouring steps'
-kernels, as a serving runtime pipelines its decode steps; `e2e.serial` is one
-graph per step (copy in, call, copy out, in order) and `e2e.eager` issues the
-same copies and call from Python each step.
+Timing: inputs resident in HBM; the K steps of one replay are captured in a
+CUDA graph that cycles over enough KV-pool replicas to exceed 4x the L2
+size, so every step reads its K/V from HBM.  The graph is warmed by 3
+replays, then replayed at least 20 times (and for about a second), each
+replay bracketed by CUDA events on the launching stream; ms_per_step is the
+median replay time / K.  A synchronize and a barrier bracket the whole timed
+region, and the max over ranks is taken.  nvidia-smi samples the clocks
+across all replays.  `e2e` goes through the public Python call with pinned
+host buffers: per step the new q/k/v, lengths, flags and page table (one
+input arena) are copied in and the output is copied out.  The headline e2e
+replays a CUDA graph of many steps with two input arenas and two outputs,
+the copies on their own streams overlapping the neighbouring steps'
+kernels, as a serving runtime pipelines its decode steps; `e2e.serial` is
+one graph per step (copy in, call, copy out, in order) and `e2e.eager`
+issues the same copies and call from Python each step.
 
---impl reference times the float64 CPU oracle on the host cores instead (each
-step one row of the same workload).  --ncu-case runs a few eager launches on
-one pool only (for profiler captures).
+`cpu_baseline` and --impl reference time the float64 CPU oracle as it
+stands on whole steps of the same workload (every active row per call),
+on all host cores and on one core, in the same tokens/s and GB/s columns.
+--ncu-case runs a few eager launches on one pool only (for profiler
+captures).
 """
 from __future__ import annotations
 
@@ -55,12 +66,20 @@ KERNEL_SOURCES = ["paged_len_decode_gb300/csrc/decode_attn.cu", "paged_len_decod
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=240,
+                    help="steps per timed graph replay (each replay is timed; the median is reported)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--replays", type=int, default=20, help="minimum number of timed replays")
+    ap.add_argument("--seconds", type=float, default=1.0,
+                    help="the timed replays of each measurement last at least about this long")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="oracle time on all host cores (the one-core sample gets the same budget)")
+    ap.add_argument("--extra-workloads", default=None,
+                    help="comma-separated workloads measured beside the headline (default with the c64 "
+                         "headline and default options: long,padded,high; '' for none)")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="16-bit element type of q, k, v, the cache and the output")
     ap.add_argument("--layout", default=None, choices=["NHD", "HND", "CONTIG"],
@@ -164,7 +183,8 @@ class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
@@ -179,27 +199,43 @@ class Clocks:
             self.proc = None
         time.sleep(0.3)
 
+    @classmethod
+    def summarise(cls, lines) -> dict:
+        """Median SM clock over the samples taken under load (GPU utilisation
+        >= 50 %, or all samples if none is), and every throttle reason seen."""
+        rows = []
+        for line in lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm, smax = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            try:
+                util = float(f[9])
+            except ValueError:
+                util = -1.0
+            try:
+                pw = float(f[3])
+            except ValueError:
+                pw = None
+            rows.append((sm, smax, util, pw, [n for n, v in zip(cls.NAMES, f[5:9]) if v.lower() == "active"]))
+        loaded = [r for r in rows if r[2] >= 50.0]
+        use = loaded or rows
+        reasons = sorted({n for r in use for n in r[4]})
+        pws = [r[3] for r in use if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[0] for r in use) if use else None,
+                "sm_max_mhz": use[-1][1] if use else None, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_median": round(statistics.median(pws), 1) if pws else None}
+
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarise(out.strip().splitlines())
 
 
 class Setup:
@@ -268,12 +304,21 @@ class Setup:
             return pool[:, 0].transpose(1, 2), pool[:, 1].transpose(1, 2)
         return pool[:, 0], pool[:, 1]
 
-    def fused(self, r, pdl=True, src=None, out=None):
+    def fused(self, r, pdl=True, src=None, out=None, planned=False):
         s = src or self.inputs(r)
         k, v = self.kv(r)
         self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v, s.api_page_table, s.seq_lens,
                                 s.active, self.out if out is None else out, self.wsf, pdl=pdl,
-                                pdl_kv=pdl and self.pdl_kv, **self.norm)
+                                pdl_kv=pdl and self.pdl_kv, planned=planned, **self.norm)
+
+    def plan(self, r):
+        """The step's work list for the fused launches (vh_decode_plan)."""
+        s = self.inputs(r)
+        k, _ = self.kv(r)
+        self.vh.vh_decode_plan(s.seq_lens, s.active, s.api_page_table, self.wsf, Hq=self.Hq, Hkv=self.Hkv,
+                               D=self.D, page_size=self.P, num_pages=k.shape[0],
+                               max_pages_per_seq=s.max_pages_per_seq, max_pos=self.cos_sin.shape[0],
+                               fp16=s.pool.dtype == torch.float16)
 
     def three(self, r):
         i = self.inputs(r)
@@ -329,7 +374,7 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
     h_outs = [torch.empty((s.B, s.Hq, s.D), dtype=s.out.dtype).pin_memory() for _ in range(2)]
     h2d = total
     d2h = h_outs[0].numel() * h_outs[0].element_size()
-    K_e2e = min(args.steps, 2000)
+    K_e2e = min(max(args.steps, 640), 2000)
 
     def e2e_step(r):
         d_arenas[0].copy_(h_arena, non_blocking=True)
@@ -420,141 +465,268 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
                       "ms_per_step": round(e2e_eager_ms, 6)}}
 
 
-def run_ours(args, rank, world):
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w = workloads.WORKLOADS[args.workload]
-    s = Setup(args.workload, rank, dev, layers=args.layers, qk_norm=args.qk_norm, dtype=args.dtype,
-              interleaved=args.interleaved, layout=args.layout)
-    inp, R, L = s.inp, s.R, s.L
-    s.pdl_kv = bool(args.pdl_kv) and bool(args.pdl) and R > 1  # consecutive steps read different pools
-    by = s.step_bytes()
+SPEC_HBM_GBS = 8000.0  # HBM3e specification of a GB300 (about 8 TB/s)
+EXTRA_WORKLOADS = ("long", "padded", "high")
+# layer calls that share one per-step plan in a one-layer workload: the
+# 28-layer Talker of the pages' c=64 serving figures (VoxCPM2's MiniCPM4 Talker)
+PLAN_LAYERS = 28
 
-    for r in range(R):  # first calls outside capture (launch attributes, every replica's new slot)
-        s.three(r)
-        s.fused(r, pdl=False)
-    torch.cuda.synchronize()
 
-    stream = torch.cuda.Stream(device=dev)
-
-    def capture(fn, n):
+def step_graphs(s, fn, K, stream, plan_every: int = 0):
+    """CUDA graphs of K steps (K*L launches) that continue one cycle over the
+    R pools: graph j starts at pool (j*K*L) mod R, so replaying the graphs in
+    turn never reads the same pool in two consecutive launches.  plan_every >
+    0: a vh_decode_plan launch before the first launch of each replay and then
+    before every plan_every-th launch."""
+    n_launch = K * s.L
+    n_graphs = s.R // math.gcd(s.R, n_launch)
+    graphs = []
+    for j in range(n_graphs):
+        start = (j * n_launch) % s.R
         g = torch.cuda.CUDAGraph()
         stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    fn(i % R)
+                for i in range(n_launch):
+                    if plan_every and i % plan_every == 0:
+                        s.plan((start + i) % s.R)
+                    fn((start + i) % s.R)
         torch.cuda.current_stream().wait_stream(stream)
-        return g
+        graphs.append(g)
+    return graphs
 
-    chunk = R * max(1, 240 // R)  # steps per graph replay (a multiple of the replica count)
 
-    def timed(fn, K, clocks=None):
-        full = capture(fn, chunk)
-        rem = K % chunk
-        tail = capture(fn, rem) if rem else None
-        with torch.cuda.stream(stream):
-            full.replay()  # warm the graph itself
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        if clocks:
-            clocks.start()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(K // chunk):
-                full.replay()
-            if tail is not None:
-                tail.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ck = clocks.stop() if clocks else None
-        barrier(world)
-        return max_over_ranks(e0.elapsed_time(e1), world), ck
-
-    for i in range(args.warmup):  # untimed warm-up steps
-        s.fused(i % R)
-        s.three(i % R)
+def time_replays(graphs, K, stream, world, min_replays, seconds):
+    """Warm the graphs with 3 replays, then time at least `min_replays` replays
+    (and about `seconds` of them), each bracketed by its own CUDA events on the
+    launching stream.  Returns (median ms per step, mean ms per step, replays),
+    the median taken as the max over ranks."""
+    n_g = len(graphs)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, n_g)):
+            graphs[i % n_g].replay()
     torch.cuda.synchronize()
+    # replay time estimate from 3 more replays
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(3):
+            graphs[i % n_g].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1) / 3, 1e-3)
+    n = int(min(200000, max(min_replays, math.ceil(seconds * 1e3 / est))))
+    n = -(-n // n_g) * n_g
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            ev[i][0].record(stream)
+            graphs[i % n_g].replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    per_step = [a.elapsed_time(b) / K for a, b in ev]
+    med = max_over_ranks(statistics.median(per_step), world)
+    return med, statistics.fmean(per_step), n
+
+
+def rates(by, ms_step, world, peak, L):
+    """tokens/s, GB/s and fractions of one step time."""
+    gbs = by["step"] / (ms_step * 1e-3) / 1e9
+    return {"ms_per_step": round(ms_step, 6), "tokens_per_s": round(by["active"] * world / (ms_step * 1e-3), 1),
+            "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "frac_of_spec": round(gbs / SPEC_HBM_GBS, 4), "ms_per_launch": round(ms_step / L, 6)}
+
+
+def workload_desc(name, s, by):
+    w = workloads.WORKLOADS[name]
+    return (f"{name}: B={s.B} (active {by['active']}), Hq={s.Hq}, Hkv={s.Hkv}, D={s.D}, P={s.P}, "
+            f"lengths {w.dist} [{w.len_lo},{w.len_hi}]" + (f", {s.L} layer calls per step" if s.L > 1 else ""))
+
+
+def l2_desc(s):
+    return ((f"{s.R} KV pools, one per layer call ({s.R // s.L} sets of {s.L} layers, "
+             f"{s.R * s.pool_bytes / 1e6:.0f} MB" if s.L > 1 else
+             f"{s.R} KV-pool replicas cycled ({s.R * s.pool_bytes / 1e6:.0f} MB")
+            + f" >= 4x L2 {s.l2 / 1e6:.0f} MB): inputs larger than L2")
+
+
+def measure_workload(name, args, rank, world, dev, stream, *, headline: bool):
+    """Build one workload's pools and time its fused step with programmatic
+    dependent launch (and early K/V requests), the same steps without it,
+    and (headline only) the three-call step and the end-to-end figures."""
+    s = Setup(name, rank, dev, layers=args.layers if headline else None,
+              qk_norm=args.qk_norm if headline else False, dtype=args.dtype if headline else "bf16",
+              interleaved=args.interleaved if headline else False, layout=args.layout if headline else None)
+    by = s.step_bytes()
+    pdl = bool(args.pdl) if headline else True
+    s.pdl_kv = (bool(args.pdl_kv) if headline else True) and pdl and s.R > 1  # consecutive launches read other pools
+    for r in range(s.R):  # first calls outside capture (launch attributes, every pool's new slot)
+        s.three(r)
+        s.fused(r, pdl=False)
+    for i in range(args.warmup * s.L):  # untimed warm-up steps
+        s.fused(i % s.R)
+        s.three(i % s.R)
+    torch.cuda.synchronize()
+    peak, _ = peaks()
+    K = args.steps
+    res = {"workload": workload_desc(name, s, by), "steps_per_replay": K, "layers": s.L,
+           "algorithmic_bytes_per_step": by["step"], "kv_bytes_per_step": by["kv"], "l2": l2_desc(s),
+           "ctas": s.n_ctas}
+    g = step_graphs(s, lambda r: s.fused(r, pdl=pdl), K, stream)
+    med, mean, n = time_replays(g, K, stream, world, args.replays, args.seconds)
+    del g
+    res.update(rates(by, med, world, peak, s.L))
+    res.update({"ms_per_step_mean": round(mean, 6), "replays": n, "pdl": pdl, "pdl_kv": s.pdl_kv,
+                "traffic": (recorded_traffic(name) if (not headline or (args.dtype == "bf16" and not args.interleaved
+                            and not args.qk_norm and s.inp.layout == "NHD")) else None)})
+    if pdl:
+        g = step_graphs(s, lambda r: s.fused(r, pdl=False), K, stream)
+        med_np, mean_np, n_np = time_replays(g, K, stream, world, args.replays, args.seconds)
+        del g
+        res["no_pdl"] = {**rates(by, med_np, world, peak, s.L), "replays": n_np,
+                         "step": "the same fused launches, each waiting for the previous one to complete"}
+    # the same steps with the work list planned once per model step
+    every = s.L if s.L > 1 else PLAN_LAYERS
+    for key, pl in (("planned", pdl), ("planned_no_pdl", False)) if pdl else (("planned", False),):
+        s.plan(0)
+        s.fused(0, pdl=False, planned=True)
+        torch.cuda.synchronize()
+        g = step_graphs(s, lambda r, pl=pl: s.fused(r, pdl=pl, planned=True), K, stream, plan_every=every)
+        med_p, _, n_p = time_replays(g, K, stream, world, args.replays, args.seconds)
+        del g
+        res[key] = {**rates(by, med_p, world, peak, s.L), "replays": n_p,
+                    "step": (f"one vh_decode_plan launch per {every} layer calls (and at the start of each "
+                             f"replay of {K * s.L}), the fused launches reading it (VH_FLAG_PLANNED)"
+                             + (", PDL between the fused launches" if pl else ", no PDL"))}
+    if headline:
+        g = step_graphs(s, s.three, K, stream)
+        med3, _, n3 = time_replays(g, K, stream, world, args.replays, args.seconds)
+        del g
+        res["three_call"] = {**rates(by, med3, world, peak, s.L), "replays": n3, "launches_per_step": 3 * s.L}
+        res["e2e"] = (e2e_measure(s, s.inp, s.R, by, args, world, dev, stream) if s.L == 1 else
+                      {"value": None, "unit": "tokens/s", "note": "measured for single-layer steps only"})
+        res["_setup"] = s
+        res["_by"] = by
+    else:
+        del s
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = peaks()
+    default_variant = (args.dtype == "bf16" and not args.interleaved and not args.qk_norm and args.layout is None
+                       and args.layers is None and args.pdl and args.pdl_kv)
+    if args.extra_workloads is None:
+        extras = list(EXTRA_WORKLOADS) if (args.workload == WORKLOAD and default_variant) else []
+    else:
+        extras = [x for x in args.extra_workloads.split(",") if x]
 
     clocks = Clocks(dev.index)
-    ms_fused_total, ck = timed(lambda r: s.fused(r, pdl=bool(args.pdl)), args.steps * L, clocks)  # L calls per step
-    ms_step = ms_fused_total / args.steps
-    ms_three_total, _ = timed(s.three, args.steps * L)
-    ms_three = ms_three_total / args.steps
+    clocks.start()
+    h = measure_workload(args.workload, args, rank, world, dev, stream, headline=True)
+    s, by = h.pop("_setup"), h.pop("_by")
+    e2e = h.pop("e2e")
+    inp_cpu = s.inp.to("cpu") if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    del s
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    extra = {}
+    for name in extras:
+        if name == args.workload:
+            continue
+        extra[name] = measure_workload(name, args, rank, world, dev, stream, headline=False)
+    ck = clocks.stop()
 
-    tokens_per_s = by["active"] * world / (ms_step * 1e-3)
-    step_gbs = by["step"] / (ms_step * 1e-3) / 1e9
-    peak, peak_kind = peaks()
-
-    e2e = None
-    if L == 1:
-        e2e = e2e_measure(s, inp, R, by, args, world, dev, stream)
-
+    w = workloads.WORKLOADS[args.workload]
+    L = h["layers"]
+    ms_step = h["ms_per_step"]
+    kname = (f"decode_attn_kernel<{w.D},{w.Hq // w.Hkv},1,{'ElemF16' if args.dtype == 'fp16' else 'ElemBf16'}> "
+             "(fused step)")
+    n_replays = h["replays"]
     res = {
-        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "metric": METRIC, "value": h["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if args.dtype == "fp16" else "bf16",
         "accum_dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: B={s.B} (active {by['active']}), Hq={s.Hq}, Hkv={s.Hkv}, "
-                               f"D={s.D}, P={s.P}, lengths {w.dist} [{w.len_lo},{w.len_hi}]",
-                   "global_batch": s.B * world, "kv_bytes_per_step": by["kv"],
+        "config": {"workload": h["workload"], "global_batch": w.B * world, "kv_bytes_per_step": by["kv"],
                    "step": (f"{L} layer calls, " if L > 1 else "") +
                            "one vh_decode_fused launch (RoPE+append+attention+merge) per layer call, " +
-                           ("PDL between launches" if args.pdl else "no PDL between launches") +
-                           (", first cached K/V tiles requested before the wait "
-                                                     "(VH_FLAG_PDL_KV)" if s.pdl_kv else ""),
+                           ("PDL between launches" if h["pdl"] else "no PDL between launches") +
+                           (", first cached K/V tiles requested before the wait (VH_FLAG_PDL_KV)"
+                            if h["pdl_kv"] else ""),
+                   "timing": (f"CUDA graph of {args.steps} steps, warmed by 3 replays, then {n_replays} timed "
+                              "replays, each bracketed by CUDA events on the launching stream; ms_per_step = "
+                              "median replay time / steps"),
                    "layers": L, "qk_norm": bool(args.qk_norm), "rope": "interleaved" if args.interleaved
-                   else "rotate-half", "elements": args.dtype, "pages": s.inp.layout,
+                   else "rotate-half", "elements": args.dtype, "pages": args.layout or w.layout,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": (f"{R} KV pools, one per layer call ({R // L} sets of {L} layers, "
-                          f"{R * s.pool_bytes / 1e6:.0f} MB" if L > 1 else
-                          f"{R} KV-pool replicas cycled ({R * s.pool_bytes / 1e6:.0f} MB")
-                         + f" >= 4x L2 {s.l2 / 1e6:.0f} MB): inputs larger than L2",
-                   "ctas": s.n_ctas},
-        "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": f"decode_attn_kernel<{s.D},{s.Hq // s.Hkv},1,"
-                               f"{'ElemF16' if args.dtype == 'fp16' else 'ElemBf16'}> (fused step)",
-                     "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(step_gbs / peak, 4), "traffic": (recorded_traffic(args.workload)
-                                                    if args.dtype == "bf16" and not args.interleaved
-                                                    and s.inp.layout == "NHD" else None),
-                     "peak_kind": peak_kind, "ms_per_launch": round(ms_step / L, 6),
-                     "algorithmic_bytes_per_launch": by["step"] // L},
-        "three_call": {"ms_per_step": round(ms_three, 6),
-                       "value": round(by["active"] * world / (ms_three * 1e-3), 1), "unit": "tokens/s",
-                       "launches_per_step": 3 * L},
+                   "l2": h["l2"], "ctas": h["ctas"]},
+        "hbm_gbs": h["hbm_gbs"], "hbm_frac_of_peak": h["frac_of_peak"], "hbm_frac_of_spec": h["frac_of_spec"],
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": h["hbm_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": h["frac_of_peak"], "traffic": h["traffic"], "peak_kind": peak_kind,
+                     "spec_peak": SPEC_HBM_GBS, "frac_of_spec": h["frac_of_spec"],
+                     "ms_per_launch": h["ms_per_launch"], "algorithmic_bytes_per_launch": by["step"] // L},
+        "ms_per_step_mean": h["ms_per_step_mean"],
+        "no_pdl": h.get("no_pdl"),
+        "planned": h.get("planned"),
+        "planned_no_pdl": h.get("planned_no_pdl"),
+        "three_call": h["three_call"],
+        "workloads": extra,
         "clocks": ck,
-        "e2e": e2e if e2e is not None else {"value": None, "unit": "tokens/s",
-                                            "note": "measured for single-layer steps only"},
-        "gpu_launches": args.steps * L,
+        "e2e": e2e,
+        "gpu_launches": n_replays * args.steps * L,
     }
-    return res, inp
+    return res, inp_cpu
 
 
-def cpu_oracle_rate(inp_cpu, seconds: float, max_steps: int | None = None):
-    """Oracle steps on single rows of the workload (round robin): rows/s."""
+def cpu_oracle_steps(inp_cpu, *, seconds: float | None = None, max_steps: int | None = None,
+                     threads: int | None = None):
+    """Whole oracle steps on the workload: RoPE + append of every active row,
+    then the attention of every row (OpenMP over rows and q heads).  Returns
+    (steps/s, steps, seconds, threads used)."""
     import oracle
 
-    pool = inp_cpu.pool.clone()
-    B = inp_cpu.B
-    rows = [b for b in range(B) if int(inp_cpu.active[b])]
-    n, t0 = 0, time.perf_counter()
-    while True:
-        b = rows[n % len(rows)]
-        act = torch.zeros(B, dtype=torch.int32)
-        act[b] = 1
-        q_rot, pool_after, _ = oracle.rope_kv_append(inp_cpu.q, inp_cpu.k_new, inp_cpu.v_new, pool,
-                                                     inp_cpu.page_table, inp_cpu.seq_lens, act,
-                                                     P=inp_cpu.P, theta=inp_cpu.theta, in_place=True)
-        oracle.decode_attn(q_rot, pool_after, inp_cpu.page_table, inp_cpu.seq_lens, act, P=inp_cpu.P,
-                           rows=[b])
-        n += 1
-        el = time.perf_counter() - t0
-        if (max_steps is not None and n >= max_steps) or (max_steps is None and el >= seconds):
-            return n / el, n, el, oracle.num_threads()
+    before = oracle.num_threads()
+    if threads is not None:
+        oracle.set_num_threads(threads)
+    try:
+        used = oracle.num_threads()
+        pool = inp_cpu.pool.contiguous().clone()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            q_rot, pool_after, _ = oracle.rope_kv_append(inp_cpu.q, inp_cpu.k_new, inp_cpu.v_new, pool,
+                                                         inp_cpu.page_table, inp_cpu.seq_lens, inp_cpu.active,
+                                                         P=inp_cpu.P, theta=inp_cpu.theta, in_place=True)
+            oracle.decode_attn(q_rot, pool_after, inp_cpu.page_table, inp_cpu.seq_lens, inp_cpu.active, P=inp_cpu.P)
+            n += 1
+            el = time.perf_counter() - t0
+            if (max_steps is not None and n >= max_steps) or (seconds is not None and el >= seconds):
+                return n / el, n, el, used
+    finally:
+        oracle.set_num_threads(before)
+
+
+def cpu_baseline(inp_cpu, name, seconds: float, max_steps: int | None = None, all_cores=None):
+    """The oracle on all host cores and on one core, in tokens/s and GB/s.
+    all_cores: an (steps/s, steps, seconds, threads) result already taken."""
+    by = step_bytes(inp_cpu)
+    rate, n, el, cores = all_cores or cpu_oracle_steps(inp_cpu, seconds=seconds, max_steps=max_steps)
+    rate1, n1, el1, _ = cpu_oracle_steps(inp_cpu, seconds=seconds, max_steps=max_steps, threads=1)
+    return {"value": round(rate * by["active"], 3), "unit": "tokens/s", "cores": cores, "nproc": os.cpu_count(),
+            "kind": "oracle", "hbm_gbs": round(rate * by["step"] / 1e9, 4), "ms_per_step": round(el / n * 1e3, 3),
+            "sample": f"{n} whole oracle steps (RoPE+append+attention of all {by['active']} active rows) of the "
+                      f"{name} workload in {el:.1f} s on {cores} threads; {n1} steps in {el1:.1f} s on 1 thread",
+            "single_core": {"value": round(rate1 * by["active"], 3), "unit": "tokens/s", "cores": 1,
+                            "hbm_gbs": round(rate1 * by["step"] / 1e9, 4), "ms_per_step": round(el1 / n1 * 1e3, 3)}}
 
 
 def main():
@@ -567,25 +739,27 @@ def main():
         if rank != 0:
             return
         inp = workloads.make_inputs(args.workload, device="cpu")
-        cpu_oracle_rate(inp, 0, max_steps=max(3, args.warmup))
-        rate, n, el, cores = cpu_oracle_rate(inp, 0, max_steps=args.steps)
-        res = {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "tokens/s",
+        by = step_bytes(inp)
+        cpu_oracle_steps(inp, max_steps=max(1, args.warmup))  # untimed warm-up steps
+        rate, n, el, cores = cpu_oracle_steps(inp, max_steps=args.steps)
+        cb = cpu_baseline(inp, args.workload, seconds=min(args.cpu_seconds, 5.0), max_steps=args.steps,
+                          all_cores=(rate, n, el, cores))
+        tps = rate * by["active"]
+        res = {"impl": "reference", "metric": METRIC, "value": round(tps, 3), "unit": "tokens/s",
                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
                "ms_per_step": round(el / n * 1e3, 4), "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-               "config": {"workload": f"{args.workload} (one row per step, round robin)"},
-               "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{n} single-row oracle steps of the {args.workload} workload"},
-               "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+               "hbm_gbs": round(rate * by["step"] / 1e9, 4),
+               "config": {"workload": f"{args.workload} (whole steps: RoPE+append+attention of every active row)",
+                          "global_batch": inp.B},
+               "cpu_baseline": cb,
+               "e2e": {"value": round(tps, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                        "d2h_bytes_per_step": 0}}
         print(json.dumps(res))
         return
-    res, inp = run_ours(args, rank, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, el, cores = cpu_oracle_rate(inp.to("cpu"), args.cpu_seconds)
-        res["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                               "sample": f"{n} single-row oracle steps (RoPE+append+attention) of the "
-                                         f"{args.workload} workload in {el:.1f} s"}
+    res, inp_cpu = run_ours(args, rank, world)
+    if inp_cpu is not None:
+        res["cpu_baseline"] = cpu_baseline(inp_cpu, args.workload, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

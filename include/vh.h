@@ -64,7 +64,8 @@
  *
  * Shapes: B rows, Hq q heads, Hkv kv heads (Hq % Hkv == 0, G = Hq / Hkv
  * in {1, 2, 4, 8}), head dim D in {64, 128}, page size 1 <= P <= 1024, a
- * multiple of 16 when max_pages_per_seq > 1, 1 <= B <= 65535 and small
+ * multiple of 16 or exactly 8 when max_pages_per_seq > 1 (with 8-token pages
+ * every 16-token tile of the attention spans two pages), 1 <= B <= 65535 and small
  * enough for the attention kernels' shared-memory plan, which keeps 12
  * bytes per row (tile count, length, position) in every CTA: up to about
  * 17,000 rows (fewer kv heads per CTA as B grows); beyond that the calls
@@ -74,8 +75,7 @@
  * page_table[b][(L-1)/P], offset (L-1) % P.  page_table is int32
  * [B][max_pages_per_seq], row-major.
  *
- * Contiguous caches: page_table may be NULL (all calls but the one without a
- * workspace); row b's logical page j is then physical page
+ * Contiguous caches: page_table may be NULL; row b's logical page j is then physical page
  * b * max_pages_per_seq + j (B * max_pages_per_seq <= num_pages).  With
  * max_pages_per_seq = 1 and P = the cache length, this is a per-request
  * contiguous cache such as the Fast AR cache of the vLLM-Omni blog's Fish
@@ -117,6 +117,8 @@ typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16
 #define VH_FLAG_FP16 2u     /* 16-bit elements (q, k_new, v_new, cache, out) are IEEE fp16, not bf16 */
 #define VH_FLAG_ROPE_INTERLEAVED 4u /* RoPE pairs elements (2i, 2i+1) instead of (i, i + D/2) */
 #define VH_FLAG_PDL_KV 8u   /* VH_FLAG_PDL, and the cached K/V may be requested before the wait (vh_decode_fused) */
+#define VH_FLAG_PLANNED 16u /* the workspace holds this step's plan from vh_decode_plan (vh_decode_fused, vh_paged_decode_attn) */
+#define VH_FLAG_PLAN_THREE_CALL 32u /* vh_decode_plan: plan for vh_paged_decode_attn instead of vh_decode_fused */
 
 /* Fill the RoPE table used by vh_rope_kv_append.  Source: "Engineering TTS
  * inference in vLLM-Omni", Qwen3-TTS section 4 (RoPE cos/sin kept in fp32).
@@ -208,7 +210,10 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
  *     programmatic dependent of the previous kernel on the stream (for
  *     instance vh_rope_kv_append): lengths, flags and page ids are read before
  *     that kernel has completed and must not be written by it; q_rot and the
- *     cache are read after.
+ *     cache are read after.  VH_FLAG_PLANNED: take the work list from the
+ *     plan vh_decode_plan (with VH_FLAG_PLAN_THREE_CALL) wrote into this
+ *     workspace for the same lengths, flags, page table, shape and num_ctas
+ *     (see vh_decode_plan).
  * Softmax in fp32 with a running max, exp2 with log2(e) folded into the
  * scale; keys beyond seq_len (tail of the last page) are never used.  With
  * fp16, q_rot is split into an fp16 high part and residual for the tensor
@@ -265,7 +270,11 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
  *     only when it writes none of the cache pages this call reads (for
  *     instance the projection kernel of this layer, or this call for another
  *     layer's cache); the new token's slot is rewritten from k_new / v_new
- *     after the wait.
+ *     after the wait.  VH_FLAG_PLANNED: take the work list (tile ranges,
+ *     row arrays, first page ids) from the plan vh_decode_plan wrote into
+ *     this workspace, instead of deriving it from the lengths;
+ *   - the workspace also holds that per-step plan: vh_decode_plan writes a
+ *     region of it that this call only reads (and only with VH_FLAG_PLANNED).
  * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,
  * VH_ENODEV, VH_ECUDA. */
 int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
@@ -278,6 +287,40 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                     int B, int Hq, int Hkv, int D, int page_size, void* stream);
 
+/* Per-step plan of the attention work list, shared by every attention launch
+ * of one decode step (all layers of a model see the same lengths, flags,
+ * positions and page table).  The source pages have no counterpart: their
+ * kernel picks its split from a host-side upper bound; here the split is a
+ * device-side tile list (see vh_paged_decode_attn), and this call derives it
+ * once per step instead of once per launch.
+ * Writes into `workspace` (the one later passed to vh_decode_fused, or with
+ * VH_FLAG_PLAN_THREE_CALL to vh_paged_decode_attn, with VH_FLAG_PLANNED): the
+ * prefix sums of every row's 16-token tile count, the lengths and positions,
+ * each CTA's tile range and the page ids of its first 64 tiles.  Rows that
+ * take part: active rows with 1 <= seq_len <= max_pages_per_seq*P (others
+ * flag VH_ERR_SEQLEN), and, for vh_decode_fused, a position (positions[b], or
+ * seq_len-1) within [0, max_pos) (others flag VH_ERR_POS and are treated as
+ * padding, as vh_decode_fused does).  max_pos is ignored with
+ * VH_FLAG_PLAN_THREE_CALL.
+ * Ordering: this kernel is an ordinary launch (it waits for all earlier work
+ * on the stream) that lets no later kernel start before it completes, so
+ * every later launch on the stream, programmatic dependents included, may
+ * read the plan before its own dependency wait.  Call it again whenever
+ * seq_lens, active, positions or page_table change (normally once per decode
+ * step, after they are written and before the step's first attention
+ * launch); a planned launch whose shape, num_ctas or path does not match the
+ * plan's header ignores the plan and derives the work list itself, but one
+ * made with stale lengths or page ids reads and appends where the old plan
+ * says.  num_ctas: the value the attention launches get (0: automatic).
+ * flags: VH_FLAG_FP16 (the element type of those launches) and
+ * VH_FLAG_PLAN_THREE_CALL.
+ * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,
+ * VH_ENODEV, VH_ECUDA. */
+int vh_decode_plan(const int32_t* positions, int max_pos, int num_pages, const int32_t* page_table,
+                   int max_pages_per_seq, const int32_t* seq_lens, const int32_t* active, int num_ctas,
+                   void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
+                   int B, int Hq, int Hkv, int D, int page_size, void* stream);
+
 /* Attention plus combine for callers that cannot allocate device memory.
  * The source pages have no counterpart to this call; it exists for callers
  * that cannot allocate device memory for a workspace (a runtime that only
@@ -285,14 +328,16 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
  * the CUDA context, a measurement that must not change the memory footprint).
  * Same arguments and result as vh_paged_decode_attn followed by
  * vh_decode_combine with flags 0 (bf16 cache and output) and token-major
- * pages (head_stride = D, so it takes no head_stride), except that there
- * is no workspace: the split-K partial
+ * pages (head_stride = D, so it takes no head_stride); page_table may be NULL
+ * (a contiguous cache, as for the other calls).  There is no workspace: the
+ * split-K partial
  * results go into one fixed array of VH_STATIC_SCRATCH_BYTES (8 MiB) compiled
  * into the library, which every GPU that loads the library keeps until the
  * process exits.  The call itself allocates and frees nothing.
  *   - The first call on each device looks up that device's address of the
  *     array (with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  A failed lookup is not remembered: the call returns
+ *     VH_ECUDA and the next call looks again.
  *   - All calls share the one array and it keeps whatever the last call left
  *     there; nothing in it needs to start at zero.  Calls whose kernels can
  *     overlap on the GPU (different streams, or different host threads) race

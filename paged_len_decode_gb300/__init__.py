@@ -14,7 +14,8 @@ selects a contiguous cache (row b owns pages b*m .. b*m+m-1, m = pages / B).
 Functions mirror the C entry points by name:
     vh_rope_table, vh_rope_kv_append, vh_decode_num_ctas,
     vh_decode_workspace_bytes, vh_paged_decode_attn, vh_decode_combine,
-    vh_decode_fused, vh_paged_decode_attn_noalloc, vh_selftest_wait_timeout, vh_status_string
+    vh_decode_fused, vh_decode_plan, vh_paged_decode_attn_noalloc, vh_selftest_wait_timeout,
+    vh_status_string
 plus `decode_step`, which issues the three calls of one decode step.
 """
 from __future__ import annotations
@@ -33,6 +34,7 @@ VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3,
 VH_ESCRATCH = -6
 VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
 VH_FLAG_PDL, VH_FLAG_FP16, VH_FLAG_ROPE_INTERLEAVED, VH_FLAG_PDL_KV = 1, 2, 4, 8
+VH_FLAG_PLANNED, VH_FLAG_PLAN_THREE_CALL = 16, 32
 ELEM_DTYPES = (torch.bfloat16, torch.float16)
 
 
@@ -73,6 +75,8 @@ def _load() -> ctypes.CDLL:
     lib.vh_decode_fused.argtypes = [P, P, P, P, I, P, P, P, F, P, P, I64, I64, I64, I, P, I, P, P, P, F, I, P,
                                     SZ, P, ctypes.c_uint, I, I, I, I, I, P]
     lib.vh_decode_fused.restype = I
+    lib.vh_decode_plan.argtypes = [P, I, I, P, I, P, P, I, P, SZ, P, U, I, I, I, I, I, P]
+    lib.vh_decode_plan.restype = I
     return lib
 
 
@@ -210,7 +214,7 @@ def vh_decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, page_size: int,
 
 def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
                          sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None, pdl: bool = False,
-                         stream=None) -> None:
+                         planned: bool = False, stream=None) -> None:
     B, Hq, D = q_rot.shape
     kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     if Dc != D or out.shape != (B, Hq, D):
@@ -221,8 +225,8 @@ def vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, 
         _contig(out, k_cache.dtype, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        _elem_flags(k_cache) | (VH_FLAG_PDL if pdl else 0), B, Hq, Hkv, D, P, _stream(stream)),
-        "vh_paged_decode_attn")
+        _elem_flags(k_cache) | (VH_FLAG_PDL if pdl else 0) | (VH_FLAG_PLANNED if planned else 0),
+        B, Hq, Hkv, D, P, _stream(stream)), "vh_paged_decode_attn")
 
 
 def vh_decode_combine(workspace, out, Hkv: int, page_size: int, num_ctas: int = 0, stream=None) -> None:
@@ -240,14 +244,15 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
                                  sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
                                  stream=None) -> None:
     """Attention plus combine into `out` with the library's fixed scratch array,
-    for callers that cannot allocate a workspace (see include/vh.h)."""
+    for callers that cannot allocate a workspace (see include/vh.h).
+    page_table=None selects a contiguous token-major cache (row b owns pages
+    b*m .. b*m+m-1, m = pages / B)."""
     B, Hq, D = q_rot.shape
     kp, vp, ps, ts, _hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache, bf16_only=True)
     if Dc != D or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q_rot, out and the cache")
     _check(lib.vh_paged_decode_attn_noalloc(
-        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, NP,
-        _contig(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _contig(q_rot, torch.float32, "q_rot"), kp, vp, ps, ts, NP, *_table(page_table, B, NP),
         _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
         _contig(out, torch.bfloat16, "out"), float(sm_scale), int(num_ctas),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
@@ -257,11 +262,13 @@ def vh_paged_decode_attn_noalloc(q_rot, k_cache, v_cache, page_table, seq_lens, 
 def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, out,
                     workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
                     pdl: bool = False, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
-                    interleaved: bool = False, pdl_kv: bool = False, stream=None) -> torch.Tensor:
+                    interleaved: bool = False, pdl_kv: bool = False, planned: bool = False,
+                    stream=None) -> torch.Tensor:
     """One whole decode step in one launch (RoPE, append, attention, merge).
     `workspace` must be zero-filled before its first use (alloc_workspace does that).
     pdl=True sets VH_FLAG_PDL, pdl_kv=True VH_FLAG_PDL_KV (see include/vh.h for
-    when each is allowed)."""
+    when each is allowed); planned=True (VH_FLAG_PLANNED) takes the work list
+    from the plan vh_decode_plan wrote into `workspace`."""
     B, Hq, D = q.shape
     kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     et = k_cache.dtype
@@ -277,10 +284,32 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
         _contig(out, et, "out"), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
-        (VH_FLAG_PDL if pdl else 0) | (VH_FLAG_PDL_KV if pdl_kv else 0) | _elem_flags(k_cache, interleaved),
-        B, Hq, Hkv, D, P,
+        (VH_FLAG_PDL if pdl else 0) | (VH_FLAG_PDL_KV if pdl_kv else 0) | _elem_flags(k_cache, interleaved)
+        | (VH_FLAG_PLANNED if planned else 0), B, Hq, Hkv, D, P,
         _stream(stream)), "vh_decode_fused")
     return out
+
+
+def vh_decode_plan(seq_lens, active, page_table, workspace, *, Hq: int, Hkv: int, D: int, page_size: int,
+                   num_pages: int, max_pages_per_seq: int | None = None, positions=None, max_pos: int = 0,
+                   num_ctas: int = 0, err_flag=None, fp16: bool = False, three_call: bool = False,
+                   stream=None) -> None:
+    """Write the step's attention work list into `workspace` (see include/vh.h):
+    for vh_decode_fused(planned=True), or with three_call=True for
+    vh_paged_decode_attn(planned=True).  page_table=None: contiguous cache with
+    max_pages_per_seq pages per row (default num_pages // B)."""
+    B = seq_lens.shape[0]
+    if page_table is None:
+        pt, mps = None, (max_pages_per_seq if max_pages_per_seq is not None else num_pages // B)
+    else:
+        pt, mps = _contig(page_table, torch.int32, "page_table"), page_table.shape[1]
+    _check(lib.vh_decode_plan(
+        None if positions is None else _contig(positions, torch.int32, "positions"), int(max_pos), int(num_pages),
+        pt, mps, _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"), int(num_ctas),
+        _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
+        (VH_FLAG_FP16 if fp16 else 0) | (VH_FLAG_PLAN_THREE_CALL if three_call else 0),
+        B, Hq, Hkv, D, page_size, _stream(stream)), "vh_decode_plan")
 
 
 def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas: int = 0,
@@ -293,15 +322,18 @@ def alloc_workspace(B: int, Hq: int, Hkv: int, D: int, page_size: int, num_ctas:
 def decode_step(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active, q_rot,
                 out, workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0,
                 err_flag=None, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
-                interleaved: bool = False, stream=None) -> torch.Tensor:
-    """One decode step of one layer: (RMSNorm +) RoPE + append, attention, combine."""
+                interleaved: bool = False, planned: bool = False, stream=None) -> torch.Tensor:
+    """One decode step of one layer: (RMSNorm +) RoPE + append, attention, combine.
+    planned=True: the attention takes its work list from the plan vh_decode_plan
+    (three_call=True) wrote into `workspace`."""
     vh_rope_kv_append(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_lens, active,
                       q_rot, positions=positions, err_flag=err_flag, q_norm_w=q_norm_w,
                       k_norm_w=k_norm_w, norm_eps=norm_eps, interleaved=interleaved, stream=stream)
     # the attention launch depends programmatically on the append kernel just
     # before it, which writes neither lengths, flags nor the page table
     vh_paged_decode_attn(q_rot, k_cache, v_cache, page_table, seq_lens, active, out, workspace,
-                         sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, pdl=True, stream=stream)
+                         sm_scale=sm_scale, num_ctas=num_ctas, err_flag=err_flag, pdl=True, planned=planned,
+                         stream=stream)
     vh_decode_combine(workspace, out, k_cache.shape[2], k_cache.shape[1], num_ctas=num_ctas,
                       stream=stream)
     return out

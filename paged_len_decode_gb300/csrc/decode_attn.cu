@@ -81,6 +81,18 @@ __device__ __forceinline__ int cta_of(long long s, int n_eff, long long T) {
   return si < big ? si / (q + 1) : r + (si - big) / q;
 }
 
+// Page id holding tile tk of row `row`: its page (P/16 tiles per page, or
+// one page of any size), or with 8-token pages (p8) page `half` of the two the
+// tile spans; 0 where that page is past the row's page-table entries.  No page
+// table: row b's pages are b * mps .. b * mps + mps - 1.
+__device__ __forceinline__ int tile_page_id(const int32_t* page_table, int mps, bool p8, int tpp, int row, int tk,
+                                            int half) {
+  const int j = p8 ? 2 * tk + half : tk / tpp;
+  if (j >= mps) return 0;
+  const long long lp = static_cast<long long>(row) * mps + j;
+  return page_table ? page_table[lp] : static_cast<int>(lp);
+}
+
 // In-place inclusive prefix sum of cum[1..n] (cum[0] = 0 already).
 __device__ void block_inclusive_scan(int* cum, int n, int* warp_tot) {
   const int tid = threadIdx.x, nthr = blockDim.x;
@@ -214,38 +226,22 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   int* posv = reinterpret_cast<int*>(smem + p.pos_off);
   long long* meta = reinterpret_cast<long long*>(smem + p.meta_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  int* misc = reinterpret_cast<int*>(smem + p.bar_off + 8 * (2 * S + 4));
+  int* misc = reinterpret_cast<int*>(smem + p.bar_off + 8 * (2 * S + 5));
   volatile int* abort_flag = misc + kMiscAbort;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + S);
   const uint32_t qfull = smem_addr(bars + 2 * S), qempty = smem_addr(bars + 2 * S + 1);
   // fused merge: consumers -> merge warp ("partial result written"), merge warp -> consumers ("counted")
   const uint32_t pready = smem_addr(bars + 2 * S + 2), mdone = smem_addr(bars + 2 * S + 3);
   const int max_len = p.max_pages_per_seq * p.P;
+  // 8-token pages: a 16-token tile spans two pages (logical pages 2k and 2k + 1 of its row)
+  const bool p8 = (p.P == 8);
+  const uint32_t rowsbar = smem_addr(bars + 2 * S + 4);
   pdl_launch_dependents();  // the next kernel may start its CTAs as ours finish
 
-  // ---- prologue: tile count of every row and their prefix sum -------------
-  // (lengths, flags, positions and, below, page ids are read before the wait
-  // for the previous kernel: they must not be written by that kernel; every
-  // other access comes after the wait)
-  for (int b = tid; b < p.B; b += blockDim.x) {
-    const int a = p.active[b], L = p.seq_lens[b];
-    int nt = row_tiles(a, L, max_len);
-    if (a && nt == 0 && c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_SEQLEN);
-    if constexpr (FUSED) {
-      if (nt > 0) {
-        const int pos = p.positions ? p.positions[b] : L - 1;
-        if (pos < 0 || pos >= p.max_pos) {
-          nt = 0;
-          if (c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_POS);
-        }
-        posv[b] = pos;
-      }
-    }
-    cum[1 + b] = nt;
-    lens[b] = L;
-  }
+  // ---- prologue: the work list (lengths, flags, positions and page ids are
+  // read before the wait for the previous kernel: they must not be written by
+  // that kernel; every other access comes after the wait) ----------------------
   if (tid == 0) {
-    cum[0] = 0;
     *abort_flag = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -255,28 +251,96 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     mbar_init(qempty, Hc);
     mbar_init(pready, Hc);
     mbar_init(mdone, 1);
+    mbar_init(rowsbar, 1);
     fence_barrier_init();
-  }
-  __syncthreads();
-  block_inclusive_scan(cum, p.B, misc + kMiscWarpTot);
-  const long long T = cum[p.B];
-  // (T < 2^31: 32-bit arithmetic is exact)
-  const int n_eff = T == 0 ? 0 : min(p.N, (static_cast<int>(T) + p.min_tiles - 1) / p.min_tiles);
-
-  // This CTA's tile range and its first row.
-  const long long t0_pre = n_eff > 0 ? range_begin(c, n_eff, T) : 0;
-  const long long t1_pre = n_eff > 0 ? range_begin(c + 1, n_eff, T) : 0;
-  int b0_pre = 0;
-  if (c < n_eff) {
-    int lo = 0, hi = p.B - 1;  // first row with cum[b + 1] > t0
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (cum[mid + 1] > t0_pre) hi = mid; else lo = mid + 1;
+    if (p.planned) {
+      // the step's plan: its per-row arrays land in this CTA's shared arrays
+      // (same layout) with one bulk copy
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(rowsbar, static_cast<uint32_t>(p.rows_bytes));
+      bulk_g2s(smem_addr(cum), p.plan_rows, static_cast<uint32_t>(p.rows_bytes), rowsbar);
     }
-    b0_pre = lo;
   }
-  // The producer's first page ids are read before the wait as well.
-  // tiles per page (P is a multiple of 16, or a row has one page of any size)
+  long long T = 0, t0_pre = 0, t1_pre = 0;
+  int n_eff = 0, b0_pre = 0;
+  int win = 0, nxt = 0, win2 = 0, nxt2 = 0;  // producer: page ids of tiles t0 + lane, t0 + 32 + lane
+  bool use_plan = false;
+  if (p.planned) {
+    // header and this CTA's record in the same round trip as the row arrays
+    const int4 h0 = __ldcg(reinterpret_cast<const int4*>(p.plan_hdr));
+    const int4 h1 = __ldcg(reinterpret_cast<const int4*>(p.plan_hdr) + 1);
+    const int* rec = p.plan_recs + static_cast<long long>(c) * kPlanRecInts;
+    const int4 r = __ldcg(reinterpret_cast<const int4*>(rec));
+    if (warp == Hc) {
+      win = __ldcg(rec + 4 + lane);
+      nxt = __ldcg(rec + 4 + 32 + lane);
+      if (p8) {
+        win2 = __ldcg(rec + 4 + kPlanWindow + lane);
+        nxt2 = __ldcg(rec + 4 + kPlanWindow + 32 + lane);
+      }
+    }
+    // a plan made for another shape or path (or none at all) is not used
+    use_plan = h0.x == kPlanMagic && h0.y == p.B && h0.z == p.N && h1.y == (FUSED ? 1 : 0) &&
+               h1.z == p.max_pages_per_seq && h1.w == p.P && h0.w >= 0 && h1.x >= 0 && h1.x <= p.N &&
+               (c >= h1.x || (r.x >= 0 && r.x < r.y && r.y <= h0.w && r.z >= 0 && r.z < p.B));
+    T = h0.w;
+    n_eff = h1.x;
+    if (c < n_eff) {
+      t0_pre = r.x;
+      t1_pre = r.y;
+      b0_pre = r.z;
+    }
+  }
+  __syncthreads();  // barrier initialisation visible to every thread
+  if (p.planned) {
+    const bool landed = mbar_wait(rowsbar, 0) || mbar_wait(rowsbar, 0);
+    if (__syncthreads_or(!landed)) {
+      if (tid == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+      pdl_wait();
+      return;
+    }
+  }
+  if (!use_plan) {
+    // ---- no plan: tile count of every row and their prefix sum ---------------
+    t0_pre = t1_pre = 0;
+    b0_pre = 0;
+    win = nxt = win2 = nxt2 = 0;
+    for (int b = tid; b < p.B; b += blockDim.x) {
+      const int a = p.active[b], L = p.seq_lens[b];
+      int nt = row_tiles(a, L, max_len);
+      if (a && nt == 0 && c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_SEQLEN);
+      if constexpr (FUSED) {
+        if (nt > 0) {
+          const int pos = p.positions ? p.positions[b] : L - 1;
+          if (pos < 0 || pos >= p.max_pos) {
+            nt = 0;
+            if (c == 0 && gy == 0) flag_error(p.err_flag, VH_ERR_POS);
+          }
+          posv[b] = pos;
+        }
+      }
+      cum[1 + b] = nt;
+      lens[b] = L;
+    }
+    if (tid == 0) cum[0] = 0;
+    __syncthreads();
+    block_inclusive_scan(cum, p.B, misc + kMiscWarpTot);
+    T = cum[p.B];
+    // (T < 2^31: 32-bit arithmetic is exact)
+    n_eff = T == 0 ? 0 : min(p.N, (static_cast<int>(T) + p.min_tiles - 1) / p.min_tiles);
+    // This CTA's tile range and its first row.
+    t0_pre = n_eff > 0 ? range_begin(c, n_eff, T) : 0;
+    t1_pre = n_eff > 0 ? range_begin(c + 1, n_eff, T) : 0;
+    if (c < n_eff) {
+      int lo = 0, hi = p.B - 1;  // first row with cum[b + 1] > t0
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid + 1] > t0_pre) hi = mid; else lo = mid + 1;
+      }
+      b0_pre = lo;
+    }
+  }
+  // tiles per page (P is a multiple of 16, or 8, or a row has one page of any size)
   const int tpp = (p.P + kTile - 1) / kTile;
   // row of tile tt of this CTA's range: first row with cum[row + 1] > tt
   auto row_of_from = [&](long long tt) -> int {
@@ -287,18 +351,23 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     }
     return lo;
   };
-  auto tile_page = [&](long long tt) -> int {
+  // page id of tile tt of this CTA's range: its page, or with 8-token pages
+  // the first (half 0) or second (half 1) of its two pages; 0 past the range
+  auto tile_page = [&](long long tt, int half) -> int {
     if (tt >= t1_pre) return 0;
     const int lo = row_of_from(tt);
-    const int tk = static_cast<int>(tt - cum[lo]);
-    const long long lp = static_cast<long long>(lo) * p.max_pages_per_seq + tk / tpp;
-    // no page table: a contiguous cache, row b's pages are b * max_pages_per_seq + j
-    return p.page_table ? p.page_table[lp] : static_cast<int>(lp);
+    return tile_page_id(p.page_table, p.max_pages_per_seq, p8, tpp, lo, static_cast<int>(tt - cum[lo]), half);
   };
-  int win = 0, nxt = 0;
   if (warp == Hc && c < n_eff) {
-    win = tile_page(t0_pre + lane);
-    nxt = tile_page(t0_pre + 32 + lane);
+    // The producer's first page ids are read before the wait as well.
+    if (!use_plan) {
+      win = tile_page(t0_pre + lane, 0);
+      nxt = tile_page(t0_pre + 32 + lane, 0);
+      if (p8) {
+        win2 = tile_page(t0_pre + lane, 1);
+        nxt2 = tile_page(t0_pre + 32 + lane, 1);
+      }
+    }
     // the tensor-map descriptors live in the launch parameters, not in memory
     // the previous kernel writes: fetch them before the wait as well
     if (lane == 0) prefetch_tensormap(&p.tmap_k);
@@ -309,9 +378,10 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   // The tile's copies land at [64-column block hf][head][16 tokens][128 B] of
   // the K or V half of the stage.  Full tiles (more than 8 live tokens): one
   // box of 16 tokens x Hc heads per (K or V, hf), lanes 0 .. 2*HALVES-1.
-  // Tiles with at most 8 live tokens, and every tile when full_boxes == 0: one
-  // box of 8 tokens x 1 head per (K or V, hf, head, 8-token group), lane
-  // (((group * Hc + head) * HALVES + hf) * 2 + kv).
+  // Tiles with at most 8 live tokens, every tile when full_boxes == 0 and
+  // every tile of 8-token pages: one box of 8 tokens x 1 head per (K or V, hf,
+  // head, 8-token group), lane (((group * Hc + head) * HALVES + hf) * 2 + kv);
+  // with 8-token pages, group g is token 0.. of the tile's page g.
   const int l_kv = lane & 1, l_hf = (lane >> 1) % HALVES;
   const int l_head = (lane / (2 * HALVES)) % Hc, l_g = lane / (2 * HALVES * Hc);
   const void* l_map16 = l_kv ? static_cast<const void*>(&p.tmap_v) : static_cast<const void*>(&p.tmap_k);
@@ -322,18 +392,22 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   // b, its box coordinates, the append slot and the bytes its boxes deliver.
   int npre = 0;  // tiles whose boxes were requested before the wait
   auto issue_tile = [&](long long t, int b, long long rt0, long long rt1, int tin_page, int page, bool page_ok,
-                        int stage) {
+                        int page2, bool page2_ok, int stage) {
     const int tok0 = static_cast<int>(t - rt0) * kTile;
     const int nvalid = min(kTile, lens[b] - tok0);
     const bool last_of_row = (t == rt1 - 1);
-    const long long page_off = static_cast<long long>(page) * p.page_stride;
     const int tokc = tin_page * kTile;
     const bool two_groups = nvalid > 8;
     const uint32_t st = smem_addr(smem) + static_cast<uint32_t>(stage) * p.stage_bytes;
     long long meta_val = -1;
     if constexpr (FUSED) {
-      if (last_of_row && page_ok)
-        meta_val = page_off + static_cast<long long>(tin_page * kTile + nvalid - 1) * p.token_stride +
+      // the new token's cache slot: slot nvalid - 1 of the tile (with 8-token
+      // pages, in the tile's second page if it is past the first 8 tokens)
+      const int sl = nvalid - 1;
+      const bool second = p8 && sl >= 8;
+      if (last_of_row && (second ? page2_ok : page_ok))
+        meta_val = static_cast<long long>(second ? page2 : page) * p.page_stride +
+                   static_cast<long long>(second ? sl - 8 : tokc + sl) * p.token_stride +
                    static_cast<long long>(h0) * p.head_stride;
     }
     // bytes of the boxes issued: both token groups, or the first only
@@ -344,12 +418,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       mbar_arrive_expect_tx(fb, tx);
     }
     __syncwarp();
-    if (two_groups && p.full_boxes) {
+    if (two_groups && p.full_boxes && !p8) {
       if (lane < 2 * HALVES) tma_load_4d(st + l_off16, l_map16, l_hf * 64, tokc, h0, page, fb);
     } else if (lane < 2 * HALVES * Hc * (two_groups ? 2 : 1)) {
-      const int tk = tokc + 8 * l_g;
+      const int tk = p8 ? 0 : tokc + 8 * l_g;
       const int c1 = p.tm_tok_dim == 1 ? tk : h0 + l_head, c2 = p.tm_tok_dim == 1 ? h0 + l_head : tk;
-      tma_load_4d(st + l_off8, l_map8, l_hf * 64, c1, c2, page, fb);
+      tma_load_4d(st + l_off8, l_map8, l_hf * 64, c1, c2, (p8 && l_g) ? page2 : page, fb);
     }
   };
   // L2 prefetch (no shared memory, no completion) of this CTA's tiles [ta, tb),
@@ -361,15 +435,18 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       while (t >= rt1) rt1 = cum[++b + 1];
       const long long rt0 = cum[b];
       const int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - t0_pre));
-      if (page < 0 || page >= p.num_pages) continue;  // flagged when the tile is copied
+      const int page2 = p8 ? __shfl_sync(0xffffffffu, win2, static_cast<int>(t - t0_pre)) : 0;
       const int nvalid = min(kTile, lens[b] - static_cast<int>(t - rt0) * kTile);
       const int tokc = (static_cast<int>(t - rt0) % tpp) * kTile;
-      if (nvalid > 8 && p.full_boxes) {
-        if (lane < 2 * HALVES) tma_prefetch_l2_4d(l_map16, l_hf * 64, tokc, h0, page);
-      } else if (lane < 2 * HALVES * Hc * (nvalid > 8 ? 2 : 1)) {
-        const int tk = tokc + 8 * l_g;
+      const int pg = (p8 && l_g) ? page2 : page;
+      if (nvalid > 8 && p.full_boxes && !p8) {
+        if (lane < 2 * HALVES && page >= 0 && page < p.num_pages)
+          tma_prefetch_l2_4d(l_map16, l_hf * 64, tokc, h0, page);
+      } else if (lane < 2 * HALVES * Hc * (nvalid > 8 ? 2 : 1) && pg >= 0 && pg < p.num_pages) {
+        // (bad page ids are skipped here and flagged when the tile is copied)
+        const int tk = p8 ? 0 : tokc + 8 * l_g;
         const int c1 = p.tm_tok_dim == 1 ? tk : h0 + l_head, c2 = p.tm_tok_dim == 1 ? h0 + l_head : tk;
-        tma_prefetch_l2_4d(l_map8, l_hf * 64, c1, c2, page);
+        tma_prefetch_l2_4d(l_map8, l_hf * 64, c1, c2, pg);
       }
     }
   };
@@ -386,9 +463,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       const long long rt0 = cum[b];
       const int tin_page = static_cast<int>(t - rt0) % tpp;
       int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - t0_pre));
+      int page2 = p8 ? __shfl_sync(0xffffffffu, win2, static_cast<int>(t - t0_pre)) : 0;
       const bool page_ok = page >= 0 && page < p.num_pages;
+      const bool page2_ok = page2 >= 0 && page2 < p.num_pages;
       if (!page_ok) page = 0;  // flagged again after the wait
-      issue_tile(t, b, rt0, rt1, tin_page, page, page_ok, static_cast<int>(t - t0_pre));
+      if (!page2_ok) page2 = 0;
+      issue_tile(t, b, rt0, rt1, tin_page, page, page_ok, page2, page2_ok, static_cast<int>(t - t0_pre));
       ++npre;
     }
   }
@@ -506,13 +586,24 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       if (t == wb + 32) {
         wb += 32;
         win = nxt;
-        nxt = tile_page(wb + 32 + lane);
+        nxt = tile_page(wb + 32 + lane, 0);
+        if (p8) {
+          win2 = nxt2;
+          nxt2 = tile_page(wb + 32 + lane, 1);
+        }
       }
       int page = __shfl_sync(0xffffffffu, win, static_cast<int>(t - wb));
       const bool page_ok = page >= 0 && page < p.num_pages;
       if (!page_ok) {
         if (lane == 0) flag_error(p.err_flag, VH_ERR_PAGE);
         page = 0;
+      }
+      // 8-token pages: the tile's second page, read only when the tile has more than 8 live tokens
+      int page2 = p8 ? __shfl_sync(0xffffffffu, win2, static_cast<int>(t - wb)) : 0;
+      const bool page2_ok = page2 >= 0 && page2 < p.num_pages;
+      if (!page2_ok) {
+        if (p8 && lane == 0 && lens[b] - static_cast<int>(t - rt0) * kTile > 8) flag_error(p.err_flag, VH_ERR_PAGE);
+        page2 = 0;
       }
       if (new_seg) {
         // q rows of this segment's row (fused: 16-bit q and the RoPE row of its
@@ -558,7 +649,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
           aborted = true;
           break;
         }
-        issue_tile(t, b, rt0, rt1, tin_page, page, page_ok, stage);
+        issue_tile(t, b, rt0, rt1, tin_page, page, page_ok, page2, page2_ok, stage);
       }
       if (++stage == S) {
         stage = 0;
@@ -1011,6 +1102,86 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   }
 }
 
+
+// Per-step plan: the work list every attention launch of a decode step
+// derives from the same lengths and page table, computed once.  CTA c of the
+// grid (one per attention CTA) runs the attention kernel's own prologue
+// arithmetic (tile counts, prefix sum, equal ranges) and writes its record:
+// tile range, first and last row, and the page ids of the range's first
+// kPlanWindow tiles; CTA 0 also writes the header and the per-row arrays.
+// The kernel never releases its dependents early, so every kernel after it
+// on the stream starts after it has completed and may read the plan before
+// its own dependency wait.
+__global__ void __launch_bounds__(256) decode_plan_kernel(const PlanParams p) {
+  extern __shared__ int plan_smem[];  // warp totals [32], then cum [B + 1] (all shared memory is dynamic)
+  int* warp_tot = plan_smem;
+  int* pcum = plan_smem + 32;
+  const int tid = threadIdx.x, c = blockIdx.x;
+  const int max_len = p.max_pages_per_seq * p.P;
+  int* g_len = p.rows + p.len_idx;
+  int* g_pos = p.rows + p.pos_idx;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int a = p.active[b], L = p.seq_lens[b];
+    int nt = row_tiles(a, L, max_len);
+    if (a && nt == 0 && c == 0) flag_error(p.err_flag, VH_ERR_SEQLEN);
+    int pos = 0;
+    if (p.fused && nt > 0) {
+      pos = p.positions ? p.positions[b] : L - 1;
+      if (pos < 0 || pos >= p.max_pos) {
+        nt = 0;
+        if (c == 0) flag_error(p.err_flag, VH_ERR_POS);
+      }
+    }
+    pcum[1 + b] = nt;
+    if (c == 0) {
+      g_len[b] = L;
+      g_pos[b] = pos;
+    }
+  }
+  if (tid == 0) pcum[0] = 0;
+  __syncthreads();
+  block_inclusive_scan(pcum, p.B, warp_tot);
+  const long long T = pcum[p.B];
+  const int n_eff = T == 0 ? 0 : min(p.N, (static_cast<int>(T) + p.min_tiles - 1) / p.min_tiles);
+  int t0 = 0, t1 = 0, b0 = 0, bl = 0;
+  // first row with cum[row + 1] > tt, among rows lo .. B-1
+  auto row_of = [&](int lo, long long tt) -> int {
+    int hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pcum[mid + 1] > tt) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+  };
+  if (c < n_eff) {
+    t0 = static_cast<int>(range_begin(c, n_eff, T));
+    t1 = static_cast<int>(range_begin(c + 1, n_eff, T));
+    b0 = row_of(0, t0);
+    bl = row_of(b0, t1 - 1);
+  }
+  int* rec = p.recs + static_cast<long long>(c) * kPlanRecInts;
+  if (tid == 0) *reinterpret_cast<int4*>(rec) = make_int4(t0, t1, b0, bl);
+  const bool p8 = (p.P == 8);
+  const int tpp = (p.P + kTile - 1) / kTile;
+  for (int i = tid; i < 2 * kPlanWindow; i += blockDim.x) {
+    const int half = i / kPlanWindow;
+    const long long tt = t0 + i % kPlanWindow;
+    int pg = 0;
+    if (tt < t1 && (half == 0 || p8)) {
+      const int lo = row_of(b0, tt);
+      pg = tile_page_id(p.page_table, p.max_pages_per_seq, p8, tpp, lo, static_cast<int>(tt - pcum[lo]), half);
+    }
+    rec[4 + i] = pg;
+  }
+  if (c == 0) {
+    for (int b = tid; b <= p.B; b += blockDim.x) p.rows[b] = pcum[b];
+    if (tid == 0) {
+      reinterpret_cast<int4*>(p.hdr)[0] = make_int4(kPlanMagic, p.B, p.N, static_cast<int>(T));
+      reinterpret_cast<int4*>(p.hdr)[1] = make_int4(n_eff, p.fused, p.max_pages_per_seq, p.P);
+    }
+  }
+}
+
 // Three-call path: one CTA per (row, kv-head group), one warp per kv head of
 // the group (its G q heads).  Rows that one CTA finished, and padding rows,
 // return at once.
@@ -1092,6 +1263,22 @@ cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pd
   cfg.numAttrs = pdl ? 1 : 0;
   void* args[] = {const_cast<AttnParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+cudaError_t prepare_decode_plan(int max_smem) {
+  return cudaFuncSetAttribute(decode_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
+cudaError_t launch_decode_plan(const PlanParams& p, cudaStream_t stream) {
+  // an ordinary launch (no programmatic dependency): it waits for all earlier
+  // work on the stream
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.N);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 4 * (32 + static_cast<size_t>(p.B) + 1);
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, decode_plan_kernel, p);
 }
 
 cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream_t stream) {

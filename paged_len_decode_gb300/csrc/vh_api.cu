@@ -25,11 +25,33 @@ using vh::valid_shape;
 using vh::valid_paging;
 using vh::valid_table;
 using vh::plan_attn;
-using vh::auto_ctas;
 using vh::ws_layout;
 using vh::encode_cache_maps;
 using vh::too_many_tiles;
 using vh::kMaxDevices;
+
+// Launch plan, tensor maps and CTA count of an attention launch (p holds the
+// shape, element type, cache pointers and strides).  False if the plan or
+// the tensor-map encoder rejects the shape.
+bool prepare_attn(AttnParams& p, const DeviceInfo& dev, bool fused, int num_ctas) {
+  int auto_n = 0;
+  if (!plan_attn(p, dev, fused, &auto_n)) return false;
+  if (!encode_cache_maps(p)) return false;
+  p.N = num_ctas > 0 ? num_ctas : auto_n;
+  // the first segment's q rows are requested by thread 0 as soon as the
+  // dependency wait returns (measured 0.4-0.5 us faster per launch)
+  p.early_q = 1;
+  return true;
+}
+
+// Point p at the per-step plan region of the workspace (VH_FLAG_PLANNED).
+void attach_plan(AttnParams& p, unsigned char* ws, const WsLayout& w, bool planned) {
+  p.planned = planned ? 1 : 0;
+  p.plan_hdr = reinterpret_cast<const int*>(ws + w.hdr);
+  p.plan_rows = reinterpret_cast<const int*>(ws + w.rows);
+  p.plan_recs = reinterpret_cast<const int*>(ws + w.recs);
+  p.rows_bytes = vh::plan_rows_bytes(p.B);
+}
 
 }  // namespace
 
@@ -129,27 +151,32 @@ int vh_decode_num_ctas(int B, int Hq, int Hkv, int D, int page_size) {
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev, false)) return VH_EINVAL;
-  return auto_ctas(p, *dev);
+  int n = 0;
+  if (!plan_attn(p, *dev, false, &n)) return VH_EINVAL;
+  return n;
 }
 
 size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int num_ctas) {
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_ctas < 0) return 0;
   int N = num_ctas;
   if (N == 0) {
-    // large enough for the automatic CTA count of both the three-call and the fused path
+    // large enough for the automatic CTA count of both the three-call and the
+    // fused path, with either element type
     const DeviceInfo* dev = device_info();
     if (!dev) return 0;
-    for (bool fused : {false, true}) {
-      AttnParams p{};
-      p.B = B;
-      p.Hq = Hq;
-      p.Hkv = Hkv;
-      p.D = D;
-      p.P = page_size;
-      if (!plan_attn(p, *dev, fused)) return 0;
-      N = std::max(N, auto_ctas(p, *dev));
-    }
+    for (bool fused : {false, true})
+      for (int f16 : {0, 1}) {
+        AttnParams p{};
+        p.B = B;
+        p.Hq = Hq;
+        p.Hkv = Hkv;
+        p.D = D;
+        p.P = page_size;
+        p.f16 = f16;
+        int n = 0;
+        if (!plan_attn(p, *dev, fused, &n)) return 0;
+        N = std::max(N, n);
+      }
   }
   return ws_layout(B, Hq, Hkv, D, N).total;
 }
@@ -162,7 +189,7 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
                          void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                          int B, int Hq, int Hkv, int D, int page_size, void* stream) {
   if (!q_rot || !k_cache || !v_cache || !seq_lens || !active || !out ||
-      (flags & ~(VH_FLAG_FP16 | VH_FLAG_PDL)) != 0 || !valid_paging(page_size, max_pages_per_seq) ||
+      (flags & ~(VH_FLAG_FP16 | VH_FLAG_PDL | VH_FLAG_PLANNED)) != 0 || !valid_paging(page_size, max_pages_per_seq) ||
       !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
@@ -196,18 +223,16 @@ int vh_paged_decode_attn(const float* q_rot, const vh_e16* k_cache, const vh_e16
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev, false)) return VH_EINVAL;
-  if (!encode_cache_maps(p)) return VH_EINVAL;
-  p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
+  if (!prepare_attn(p, *dev, false, num_ctas)) return VH_EINVAL;
   const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   p.plan = reinterpret_cast<int4*>(ws + w.plan);
   p.part_lse = reinterpret_cast<float*>(ws + w.lse);
   p.part_o = reinterpret_cast<float*>(ws + w.o);
+  attach_plan(p, ws, w, (flags & VH_FLAG_PLANNED) != 0);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.early_q = vh::env_int("VH_DECODE_EARLY_Q", 1) != 0;
   return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream), (flags & VH_FLAG_PDL) != 0) == cudaSuccess
              ? VH_OK
              : VH_ECUDA;
@@ -229,8 +254,10 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
   a.Hkv = Hkv;
   a.D = D;
   a.P = page_size;
-  if (!plan_attn(a, *dev, false)) return VH_EINVAL;
-  const int N = num_ctas > 0 ? num_ctas : auto_ctas(a, *dev);
+  a.f16 = (flags & VH_FLAG_FP16) != 0;  // the attention launch's plan: same element type
+  int auto_n = 0;
+  if (!plan_attn(a, *dev, false, &auto_n)) return VH_EINVAL;
+  const int N = num_ctas > 0 ? num_ctas : auto_n;
   const WsLayout w = ws_layout(B, Hq, Hkv, D, N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
   const unsigned char* ws = static_cast<const unsigned char*>(workspace);
@@ -260,7 +287,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                     int B, int Hq, int Hkv, int D, int page_size, void* stream) {
   if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !seq_lens || !active || !out ||
-      (flags & ~(VH_FLAG_PDL | VH_FLAG_PDL_KV | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED)) != 0 ||
+      (flags & ~(VH_FLAG_PDL | VH_FLAG_PDL_KV | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED | VH_FLAG_PLANNED)) != 0 ||
       !valid_paging(page_size, max_pages_per_seq) || !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
@@ -307,9 +334,7 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev, true)) return VH_EINVAL;
-  if (!encode_cache_maps(p)) return VH_EINVAL;
-  p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
+  if (!prepare_attn(p, *dev, true, num_ctas)) return VH_EINVAL;
   const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (workspace_bytes < w.total) return VH_EWORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -317,9 +342,9 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   p.counters = reinterpret_cast<int*>(ws + w.counters);
   p.part_lse = reinterpret_cast<float*>(ws + w.lse);
   p.part_o = reinterpret_cast<float*>(ws + w.o);
+  attach_plan(p, ws, w, (flags & VH_FLAG_PLANNED) != 0);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.early_q = vh::env_int("VH_DECODE_EARLY_Q", 1) != 0;
   p.prefetch_kv = (flags & VH_FLAG_PDL_KV) != 0;
   // with the first stages requested before the wait (launches without it measured slower)
   p.l2_tiles = p.prefetch_kv ? vh::l2_prefetch_tiles() : 0;
@@ -327,6 +352,54 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                                 (flags & (VH_FLAG_PDL | VH_FLAG_PDL_KV)) != 0) == cudaSuccess
              ? VH_OK
              : VH_ECUDA;
+}
+
+int vh_decode_plan(const int32_t* positions, int max_pos, int num_pages, const int32_t* page_table,
+                   int max_pages_per_seq, const int32_t* seq_lens, const int32_t* active, int num_ctas,
+                   void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
+                   int B, int Hq, int Hkv, int D, int page_size, void* stream) {
+  if (!seq_lens || !active || (flags & ~(VH_FLAG_FP16 | VH_FLAG_PLAN_THREE_CALL)) != 0 ||
+      !valid_paging(page_size, max_pages_per_seq) || !valid_table(page_table, B, max_pages_per_seq, num_pages))
+    return VH_EINVAL;
+  const bool fused = (flags & VH_FLAG_PLAN_THREE_CALL) == 0;
+  if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || num_ctas < 0 ||
+      num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) || (fused && max_pos < 1))
+    return VH_EINVAL;
+  if (!workspace) return VH_EWORKSPACE;
+  if (!aligned16(workspace)) return VH_EALIGN;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return VH_ENODEV;
+  AttnParams a{};
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.P = page_size;
+  a.f16 = (flags & VH_FLAG_FP16) != 0;
+  int auto_n = 0;
+  if (!plan_attn(a, *dev, fused, &auto_n)) return VH_EINVAL;
+  const int N = num_ctas > 0 ? num_ctas : auto_n;
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, N);
+  if (workspace_bytes < w.total) return VH_EWORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  vh::PlanParams p{};
+  p.seq_lens = seq_lens;
+  p.active = active;
+  p.positions = positions;
+  p.page_table = page_table;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.max_pos = max_pos;
+  p.P = page_size;
+  p.B = B;
+  p.N = N;
+  p.min_tiles = a.min_tiles;
+  p.fused = fused ? 1 : 0;
+  p.hdr = reinterpret_cast<int*>(ws + w.hdr);
+  p.rows = reinterpret_cast<int*>(ws + w.rows);
+  p.recs = reinterpret_cast<int*>(ws + w.recs);
+  vh::plan_rows_bytes(B, &p.len_idx, &p.pos_idx);
+  p.err_flag = err_flag;
+  return vh::launch_decode_plan(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VH_OK : VH_ECUDA;
 }
 
 }  // extern "C"
@@ -347,31 +420,31 @@ static __device__ __align__(256) unsigned char g_static_scratch[VH_STATIC_SCRATC
 
 namespace {
 
-struct StaticScratch {
-  std::once_flag once;
-  void* ptr = nullptr;  // device address of g_static_scratch on this device
-};
-StaticScratch g_static[kMaxDevices];
+// Device address of g_static_scratch on each device, once a lookup succeeded.
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
 
-// Device address of the fixed scratch array on the current device.  Resolved
-// once per device, with that device current; in host code the array's name is
-// only a host-side stand-in and must never be handed to a kernel.
+// Device address of the fixed scratch array on the current device, looked up
+// with that device current.  In host code the array's name is only a
+// host-side stand-in and must never be handed to a kernel.  Only a successful
+// lookup is kept: after a failed one (for instance a first call made during
+// a stream capture) the next call tries again.
 void* static_scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return nullptr;
   }
-  StaticScratch& s = g_static[dev];
-  std::call_once(s.once, [&]() {
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
       cudaGetLastError();
-      return;
+      return nullptr;
     }
-    s.ptr = p;
-  });
-  return s.ptr;
+    g_static_ptr[dev] = p;
+  }
+  return g_static_ptr[dev];
 }
 
 }  // namespace
@@ -382,8 +455,8 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
                                             const int32_t* seq_lens, const int32_t* active,
                                             vh_bf16* out, float sm_scale, int num_ctas, int32_t* err_flag,
                                             int B, int Hq, int Hkv, int D, int page_size, void* stream) {
-  if (!q_rot || !k_cache || !v_cache || !page_table || !seq_lens || !active || !out ||
-      !valid_paging(page_size, max_pages_per_seq))
+  if (!q_rot || !k_cache || !v_cache || !seq_lens || !active || !out ||
+      !valid_paging(page_size, max_pages_per_seq) || !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || num_pages < 1 || max_pages_per_seq < 1 || page_stride < 1 ||
       token_stride < 1 || num_ctas < 0 || num_ctas > 65535 || too_many_tiles(B, max_pages_per_seq, page_size) ||
@@ -413,9 +486,7 @@ extern "C" int vh_paged_decode_attn_noalloc(const float* q_rot, const vh_bf16* k
   p.Hkv = Hkv;
   p.D = D;
   p.P = page_size;
-  if (!plan_attn(p, *dev, false)) return VH_EINVAL;
-  if (!encode_cache_maps(p)) return VH_EINVAL;
-  p.N = num_ctas > 0 ? num_ctas : auto_ctas(p, *dev);
+  if (!prepare_attn(p, *dev, false, num_ctas)) return VH_EINVAL;
   const WsLayout w = ws_layout(B, Hq, Hkv, D, p.N);
   if (w.total > static_cast<size_t>(VH_STATIC_SCRATCH_BYTES)) return VH_ESCRATCH;
   unsigned char* ws = static_cast<unsigned char*>(static_scratch_address());

@@ -8,6 +8,16 @@
 
 namespace vh {
 
+// Per-step plan (vh_decode_plan): a header of 8 ints (kPlanMagic, B, N, T,
+// n_eff, fused rules, max_pages_per_seq, P), the per-row arrays in the
+// attention kernel's shared-memory layout (tile prefix sums cum[B+1], lengths
+// [B], positions [B], each 16-byte aligned), and one record of kPlanRecInts
+// ints per CTA: t0, t1, first row, last row, then the page ids of the range's
+// first 64 tiles and, for 8-token pages, of the second page of each of them.
+constexpr int kPlanMagic = 0x56485031;
+constexpr int kPlanWindow = 64;
+constexpr int kPlanRecInts = 4 + 2 * kPlanWindow;
+
 struct RopeAppendParams {
   const uint16_t* q;
   const uint16_t* k_new;
@@ -66,6 +76,12 @@ struct AttnParams {
   float* part_o;               // [groups][N][2][Hc*G][D]
   float* part_lse;             // [groups][N][2][Hc*G]   (base-2 log-sum-exp)
   int32_t* err_flag;
+  // per-step plan written by vh_decode_plan (used when planned != 0)
+  const int* plan_hdr;
+  const int* plan_rows;        // copied as one block into the shared arrays at cum_off
+  const int* plan_recs;
+  int planned;
+  int rows_bytes;              // bytes of the per-row arrays (cum | lens | pos)
   // fused step only: RoPE of q and k, append of the new token, in-kernel combine
   const uint16_t* q;           // [B][Hq][D] new queries (bf16 / fp16)
   const uint16_t* k_new;       // [B][Hkv][D]
@@ -101,6 +117,24 @@ struct AttnParams {
   int fused;
 };
 
+// The per-step plan kernel: the same work list the attention kernel would
+// derive, written once for every attention launch of a decode step.
+struct PlanParams {
+  const int32_t* seq_lens;
+  const int32_t* active;
+  const int32_t* positions;    // fused rules only; null: seq_len - 1
+  const int32_t* page_table;   // null: contiguous cache
+  int max_pages_per_seq;
+  int max_pos;
+  int P, B, N, min_tiles;
+  int fused;                   // fused rules: rows with a position outside [0, max_pos) get no tiles
+  int* hdr;
+  int* rows;                   // cum [B+1] | lens [B] at len_idx | pos [B] at pos_idx
+  int* recs;
+  int len_idx, pos_idx;
+  int32_t* err_flag;
+};
+
 struct CombineParams {
   const int4* plan;
   const float* part_o;
@@ -116,6 +150,8 @@ cudaError_t launch_rope_kv_append(const RopeAppendParams& p, cudaStream_t stream
 cudaError_t prepare_decode_attn(int D, int G, int max_smem);  // once per device, every variant
 cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_decode_combine(const CombineParams& p, int groups, cudaStream_t stream);
+cudaError_t prepare_decode_plan(int max_smem);  // once per device
+cudaError_t launch_decode_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t decode_attn_occupancy(const AttnParams& p, int* blocks_per_sm);
 
 }  // namespace vh

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <unordered_map>
 
 #include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 
@@ -20,7 +21,7 @@ constexpr int kMaxStages = 8;
 // Lower bound on tiles per CTA when the work list is short.  One tile: a
 // short list (the Fast AR step: 64 one-tile rows) then spreads over as many
 // CTAs as it has tiles, which measured 2.1x faster there than four tiles per
-// CTA and the same on the long lists (VH_DECODE_MIN_TILES, for tuning).
+// CTA and the same on the long lists.
 constexpr int kMinTilesPerCta = 1;
 }  // namespace
 
@@ -34,6 +35,7 @@ const DeviceInfo* device_info() {
   }
   DeviceInfo& d = g_dev[dev];
   std::call_once(d.once, [&]() {
+    d.index = dev;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -50,6 +52,10 @@ const DeviceInfo* device_info() {
           cudaGetLastError();
           return;
         }
+    if (vh::prepare_decode_plan(d.smem_optin) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
     d.ok = true;
   });
   return d.ok ? &d : nullptr;
@@ -68,9 +74,10 @@ bool valid_shape(int B, int Hq, int Hkv, int D, int P) {
          Hkv <= 1024;
 }
 
-// Pages of a row hold whole 16-token tiles, unless a row has a single page.
+// Pages of a row hold whole 16-token tiles, or exactly half of one (P = 8:
+// every tile then spans two pages), unless a row has a single page.
 bool valid_paging(int P, int max_pages_per_seq) {
-  return max_pages_per_seq >= 1 && (P % 16 == 0 || max_pages_per_seq == 1);
+  return max_pages_per_seq >= 1 && (P % 16 == 0 || P == 8 || max_pages_per_seq == 1);
 }
 
 // Without a page table, row b's pages are b * max_pages_per_seq + j: they must exist.
@@ -86,12 +93,10 @@ int env_int(const char* name, int dflt) {
 
 // kv heads per CTA: the largest divisor of Hkv with Hc * D <= 512 (4 heads at
 // head_dim 128, 8 at 64): 32 KB tiles, so that two CTAs share an SM and the
-// work list is cut twice as fine as with whole-SM CTAs (VH_DECODE_HC sets
-// another cap, up to Hc * D <= 1024 and Hc <= 8, for tuning).
+// work list is cut twice as fine as with whole-SM CTAs.  (Hc * HALVES <= 8
+// also keeps every one-head box of a tile within the producer warp's lanes.)
 static int choose_hc(int Hkv, int D) {
-  int cap = std::min(512 / D, 8);
-  const int want = env_int("VH_DECODE_HC", 0);
-  if (want >= 1) cap = std::min(want, std::min(1024 / D, 8));
+  const int cap = std::min(512 / D, 8);
   int hc = std::min(Hkv, cap);
   while (Hkv % hc != 0) --hc;
   return hc;
@@ -100,16 +105,15 @@ static int choose_hc(int Hkv, int D) {
 // Pipeline stages per CTA.  Two stages of 32 KB per CTA (128 KB in flight
 // per SM with two CTAs) keep HBM saturated on GB300; more bytes in flight
 // only lengthen the queues, which measured slower at the start and the end
-// of a launch (VH_DECODE_STAGES sets another count, for tuning).
+// of a launch.
 constexpr int kDefaultStages = 2;
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Shared-memory plan of the attention kernel (fused or not): kDefaultStages
-// pipeline stages (or VH_DECODE_STAGES, if they fit); if two stages do not
-// fit, fewer kv heads go to each CTA.  Returns false if even one head per CTA
-// cannot have two stages.
-bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
+// pipeline stages; if two stages do not fit, fewer kv heads go to each CTA.
+// Returns false if even one head per CTA cannot have two stages.
+static bool plan_attn_uncached(AttnParams& p, const DeviceInfo& dev, bool fused) {
   p.fused = fused ? 1 : 0;
   p.G = p.Hq / p.Hkv;
   const size_t budget = static_cast<size_t>(dev.smem_optin);
@@ -129,7 +133,7 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
     p.q_bytes = static_cast<int>(hg * p.q_row_bytes + (fused ? p.D * 4 : 0));
     const size_t qs_bytes = fused ? static_cast<size_t>(hc) * p.G * (p.D * 4 + 32) : 0;
     fixed = align_up(p.q_bytes, 128) + align_up(qs_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
-            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 4) + 48 * 4 + 256 +
+            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 5) + 48 * 4 + 256 +
             1024 /* alignment of the base */;
     stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
     if (stages >= 2 || hc == 1) break;
@@ -139,8 +143,7 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   }
   if (stages < 2) return false;
   p.groups = p.Hkv / p.Hc;
-  const int want = env_int("VH_DECODE_STAGES", kDefaultStages);
-  if (want >= 2 && want < stages) stages = want;
+  stages = std::min(stages, kDefaultStages);
   p.stages = stages;
   size_t off = static_cast<size_t>(stages) * p.stage_bytes;
   p.q_off = static_cast<int>(off);
@@ -156,11 +159,109 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
   p.meta_off = static_cast<int>(off);
   off += 8 * static_cast<size_t>(stages);
   p.bar_off = static_cast<int>(align_up(off, 16));
-  off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 4) + 48 * 4;
+  off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 5) + 48 * 4;
   // + up to 1024 bytes that the kernel skips to align its base for the boxes
   p.smem_bytes = static_cast<int>(align_up(off, 128) + 1024);
-  p.min_tiles = std::max(1, env_int("VH_DECODE_MIN_TILES", kMinTilesPerCta));
+  p.min_tiles = kMinTilesPerCta;
   return static_cast<size_t>(p.smem_bytes) <= budget;
+}
+
+static int auto_ctas_uncached(const AttnParams& p, const DeviceInfo& dev) {
+  int per_sm = 0;
+  if (vh::decode_attn_occupancy(p, &per_sm) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  return std::max(1, dev.sm_count * per_sm / p.groups);
+}
+
+namespace {
+// The launch-plan fields of AttnParams for one (device, shape, path, element
+// type), and the automatic CTA count, computed on first use and then reused
+// (the plan and the occupancy query cost more host time than the launch).
+struct CachedPlan {
+  bool ok;
+  int auto_n;
+  int fused, G, Hc, groups, stages, min_tiles, stage_bytes, q_bytes, q_row_bytes, q_tx_bytes;
+  int q_off, qs_off, cum_off, len_off, pos_off, meta_off, bar_off, smem_bytes;
+};
+std::mutex g_plan_mu;
+std::unordered_map<uint64_t, CachedPlan> g_plans;
+constexpr size_t kMaxCachedPlans = 4096;
+
+uint64_t plan_key(int dev, const AttnParams& p, bool fused) {
+  // B < 2^16, Hq and Hkv <= 8192 / 1024 (checked by valid_shape: Hkv <= 1024, G <= 8), D / 64, P <= 1024
+  uint64_t k = static_cast<uint64_t>(dev & 63);
+  k = (k << 16) | static_cast<uint64_t>(p.B & 0xFFFF);
+  k = (k << 11) | static_cast<uint64_t>(p.Hkv & 0x7FF);
+  k = (k << 4) | static_cast<uint64_t>(p.Hq / p.Hkv & 0xF);
+  k = (k << 2) | static_cast<uint64_t>(p.D / 64 & 0x3);
+  k = (k << 11) | static_cast<uint64_t>(p.P & 0x7FF);
+  k = (k << 1) | (fused ? 1u : 0u);
+  k = (k << 1) | (p.f16 ? 1u : 0u);
+  return k;
+}
+}  // namespace
+
+bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused, int* auto_n) {
+  const uint64_t key = plan_key(dev.index, p, fused);
+  CachedPlan c{};
+  bool hit = false;
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      c = it->second;
+      hit = true;
+    }
+  }
+  if (!hit) {
+    AttnParams q = p;
+    c.ok = plan_attn_uncached(q, dev, fused);
+    c.auto_n = c.ok ? auto_ctas_uncached(q, dev) : 0;
+    c.fused = q.fused;
+    c.G = q.G;
+    c.Hc = q.Hc;
+    c.groups = q.groups;
+    c.stages = q.stages;
+    c.min_tiles = q.min_tiles;
+    c.stage_bytes = q.stage_bytes;
+    c.q_bytes = q.q_bytes;
+    c.q_row_bytes = q.q_row_bytes;
+    c.q_tx_bytes = q.q_tx_bytes;
+    c.q_off = q.q_off;
+    c.qs_off = q.qs_off;
+    c.cum_off = q.cum_off;
+    c.len_off = q.len_off;
+    c.pos_off = q.pos_off;
+    c.meta_off = q.meta_off;
+    c.bar_off = q.bar_off;
+    c.smem_bytes = q.smem_bytes;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (g_plans.size() >= kMaxCachedPlans) g_plans.clear();
+    g_plans[key] = c;
+  }
+  if (!c.ok) return false;
+  p.fused = c.fused;
+  p.G = c.G;
+  p.Hc = c.Hc;
+  p.groups = c.groups;
+  p.stages = c.stages;
+  p.min_tiles = c.min_tiles;
+  p.stage_bytes = c.stage_bytes;
+  p.q_bytes = c.q_bytes;
+  p.q_row_bytes = c.q_row_bytes;
+  p.q_tx_bytes = c.q_tx_bytes;
+  p.q_off = c.q_off;
+  p.qs_off = c.qs_off;
+  p.cum_off = c.cum_off;
+  p.len_off = c.len_off;
+  p.pos_off = c.pos_off;
+  p.meta_off = c.meta_off;
+  p.bar_off = c.bar_off;
+  p.smem_bytes = c.smem_bytes;
+  if (auto_n) *auto_n = c.auto_n;
+  return true;
 }
 
 // Fused launches that request their first stages before the dependency wait
@@ -170,26 +271,21 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused) {
 // best (c64 30.19 -> 29.81 us, padded 13.41 -> 12.90 us, long 62.0 -> 61.6 us);
 // more delay the q copies that gate the consumers; the same prefetch issued
 // before the wait slowed the previous kernel's end, and in launches without
-// early stages (three-call attention, fused without PDL) it cost 1.2-1.4 us
-// (VH_DECODE_L2_TILES, for tuning; at most 30, the page-id window).
+// early stages (three-call attention, fused without PDL) it cost 1.2-1.4 us.
 constexpr int kL2PrefetchTiles = 1;
 
-int l2_prefetch_tiles() { return std::min(30, std::max(0, env_int("VH_DECODE_L2_TILES", kL2PrefetchTiles))); }
-
-int auto_ctas(const AttnParams& p, const DeviceInfo& dev) {
-  int per_sm = 0;
-  if (vh::decode_attn_occupancy(p, &per_sm) != cudaSuccess || per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
-  const int want = env_int("VH_DECODE_CTAS_PER_SM", 0);
-  if (want >= 1 && want < per_sm) per_sm = want;
-  return std::max(1, dev.sm_count * per_sm / p.groups);
-}
+int l2_prefetch_tiles() { return kL2PrefetchTiles; }
 
 // Workspace: per-row split plan (int4 [B]); per-(head group, row) counters of
 // the fused merge (int [Hkv][B], an upper bound on groups); partial lse
 // [groups][N][2][Hq/groups] and partial outputs [...][D] (groups * Hq/groups == Hq).
+
+int plan_rows_bytes(int B, int* len_idx, int* pos_idx) {
+  const size_t c = align_up(4 * (static_cast<size_t>(B) + 1), 16), l = align_up(4 * static_cast<size_t>(B), 16);
+  if (len_idx) *len_idx = static_cast<int>(c / 4);
+  if (pos_idx) *pos_idx = static_cast<int>((c + l) / 4);
+  return static_cast<int>(c + 2 * l);
+}
 
 WsLayout ws_layout(int B, int Hq, int Hkv, int D, int N) {
   WsLayout w;
@@ -197,7 +293,10 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int D, int N) {
   w.counters = align_up(static_cast<size_t>(B) * 16, 256);
   w.lse = w.counters + align_up(static_cast<size_t>(B) * Hkv * 4, 256);
   w.o = w.lse + align_up(static_cast<size_t>(N) * 2 * Hq * 4, 256);
-  w.total = w.o + static_cast<size_t>(N) * 2 * Hq * D * 4;
+  w.hdr = align_up(w.o + static_cast<size_t>(N) * 2 * Hq * D * 4, 256);
+  w.rows = w.hdr + 256;
+  w.recs = w.rows + align_up(static_cast<size_t>(plan_rows_bytes(B)), 256);
+  w.total = w.recs + static_cast<size_t>(N) * kPlanRecInts * 4;
   return w;
 }
 
@@ -233,14 +332,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool encode_cache_maps(AttnParams& p) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  // L2 fill granularity of the tile reads (VH_TMA_L2 = 0, 64, 128 or 256 bytes, for tuning)
-  CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
-  switch (env_int("VH_TMA_L2", 256)) {
-    case 0: promo = CU_TENSOR_MAP_L2_PROMOTION_NONE; break;
-    case 64: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_64B; break;
-    case 128: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B; break;
-    default: break;
-  }
+  // L2 fill granularity of the tile reads: 256 bytes (two 128-byte box rows)
+  const CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   // one pair of maps (K, V) with token and head in the given dimension order
   auto encode = [&](CUtensorMap* mk, CUtensorMap* mv, bool tok_first, cuuint32_t tokens,
@@ -261,7 +354,8 @@ bool encode_cache_maps(AttnParams& p) {
     }
     return true;
   };
-  const bool forced = env_int("VH_TMA_BOX_HEADS", 0) == 1;
+  // (8-token pages: every tile is two pages, copied as 8-token boxes)
+  const bool forced = env_int("VH_TMA_BOX_HEADS", 0) == 1 || p.P == 8;
   if (!forced && encode(&p.tmap_k, &p.tmap_v, true, 16, static_cast<cuuint32_t>(p.Hc)) &&
       encode(&p.tmap_k8, &p.tmap_v8, true, 8, 1)) {
     p.full_boxes = 1;

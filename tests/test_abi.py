@@ -54,7 +54,7 @@ def attn(**over):
     (dict(Hq=12, Hkv=8), v.VH_EINVAL),        # Hq % Hkv != 0
     (dict(Hq=24, Hkv=8), v.VH_EINVAL),        # G = 3
     (dict(D=96), v.VH_EINVAL),
-    (dict(P=8), v.VH_EINVAL),
+    (dict(P=12), v.VH_EINVAL),               # multi-page rows: P a multiple of 16, or 8
     (dict(P=24), v.VH_EINVAL),
     (dict(B=0), v.VH_EINVAL),
     (dict(B=70000), v.VH_EINVAL),
@@ -73,6 +73,8 @@ def attn(**over):
     (dict(flags=v.VH_FLAG_PDL_KV), v.VH_EINVAL),              # not a flag of this call
     (dict(flags=v.VH_FLAG_ROPE_INTERLEAVED), v.VH_EINVAL),    # nor this one (no RoPE here)
     (dict(flags=8), v.VH_EINVAL),
+    (dict(flags=v.VH_FLAG_PLAN_THREE_CALL), v.VH_EINVAL),    # a flag of vh_decode_plan only
+    (dict(flags=v.VH_FLAG_PLANNED, ws=None), v.VH_EWORKSPACE),  # the plan lives in the workspace
     (dict(flags=v.VH_FLAG_FP16, q_rot=ODD), v.VH_EALIGN),     # fp16 passes the flag check
 ])
 def test_attention_argument_checks(over, code):
@@ -130,7 +132,8 @@ def test_fused_argument_checks():
                  None)
 
     assert call(q=None) == v.VH_EINVAL
-    assert call(flags=16) == v.VH_EINVAL           # unknown flag
+    assert call(flags=64) == v.VH_EINVAL           # unknown flag
+    assert call(flags=v.VH_FLAG_PLAN_THREE_CALL) == v.VH_EINVAL   # a flag of vh_decode_plan only
     assert call(flags=v.VH_FLAG_PDL_KV, out=ODD) == v.VH_EALIGN
     assert call(flags=v.VH_FLAG_PDL | v.VH_FLAG_FP16 | v.VH_FLAG_ROPE_INTERLEAVED, out=ODD) == v.VH_EALIGN
     assert call(Hq=24) == v.VH_EINVAL
@@ -183,3 +186,57 @@ def test_wait_timeout_selftest_without_device():
     if torch.cuda.is_available():
         pytest.skip("a device is present")
     assert v.lib.vh_selftest_wait_timeout(FAKE, None) == v.VH_ENODEV
+
+
+def plan(**over):
+    a = dict(pos=None, max_pos=4096, npages=100, pt=FAKE, mps=10, sl=FAKE, act=FAKE, nctas=0, ws=FAKE,
+             wsb=1 << 30, err=None, flags=0, B=4, Hq=16, Hkv=8, D=128, P=16)
+    a.update(over)
+    return v.lib.vh_decode_plan(a["pos"], a["max_pos"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"],
+                                a["nctas"], a["ws"], a["wsb"], a["err"], a["flags"], a["B"], a["Hq"], a["Hkv"],
+                                a["D"], a["P"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(sl=None), v.VH_EINVAL),
+    (dict(act=None), v.VH_EINVAL),
+    (dict(flags=v.VH_FLAG_PDL), v.VH_EINVAL),          # not a flag of this call
+    (dict(flags=64), v.VH_EINVAL),
+    (dict(max_pos=0), v.VH_EINVAL),                    # the fused rules need the RoPE table size
+    (dict(P=12), v.VH_EINVAL),
+    (dict(pt=None, npages=3, mps=1), v.VH_EINVAL),     # contiguous cache: 4 rows, 3 pages
+    (dict(nctas=-1), v.VH_EINVAL),
+    (dict(Hq=12), v.VH_EINVAL),
+    (dict(ws=None), v.VH_EWORKSPACE),
+    (dict(ws=ODD), v.VH_EALIGN),
+])
+def test_plan_argument_checks(over, code):
+    assert plan(**over) == code
+
+
+def test_plans_and_eight_token_pages_pass_host_checks_without_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert plan() == v.VH_ENODEV
+    assert plan(max_pos=0, flags=v.VH_FLAG_PLAN_THREE_CALL) == v.VH_ENODEV   # max_pos unused there
+    assert plan(P=8) == v.VH_ENODEV
+    assert attn(P=8) == v.VH_ENODEV                    # 8-token pages: every tile spans two pages
+    assert attn(flags=v.VH_FLAG_PLANNED) == v.VH_ENODEV
+
+
+def test_noalloc_takes_a_contiguous_cache_without_page_table():
+    import torch
+    f = v.lib.vh_paged_decode_attn_noalloc
+
+    def call(**over):
+        a = dict(q_rot=FAKE, k=FAKE, vv=FAKE, ps=2 * 16 * 8 * 128, ts=8 * 128, npages=100, pt=FAKE, mps=10,
+                 sl=FAKE, act=FAKE, out=FAKE, scale=0.0, nctas=0, err=None, B=4, Hq=16, Hkv=8, D=128, P=16)
+        a.update(over)
+        return f(a["q_rot"], a["k"], a["vv"], a["ps"], a["ts"], a["npages"], a["pt"], a["mps"], a["sl"], a["act"],
+                 a["out"], a["scale"], a["nctas"], a["err"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], None)
+
+    assert call(pt=None, npages=3, mps=1) == v.VH_EINVAL   # 4 rows need 4 pages
+    assert call(q_rot=None) == v.VH_EINVAL
+    if not torch.cuda.is_available():
+        assert call(pt=None, npages=4, mps=1) == v.VH_ENODEV

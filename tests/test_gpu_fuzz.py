@@ -4,9 +4,10 @@ Each case draws its own shape and options from its seed: batch size, GQA
 group, kv heads, head_dim, page size, a length mix (one-token rows, lengths
 on and just past page boundaries, random lengths up to several hundred
 tokens), padding rows, element type, page layout (token-major, head-major,
-contiguous per-row caches), RoPE pairing, RMSNorm of q and k, the CTA count,
-CUDA-graph replay and, on the fused path, programmatic dependent launch with
-and without early K/V requests.  Every case checks q_rot (three-call path),
+contiguous per-row caches), page size (8-token pages included), RoPE pairing,
+RMSNorm of q and k, the CTA count, CUDA-graph replay, a per-step plan and, on
+the fused path, programmatic dependent launch with and without early K/V
+requests.  Every case checks q_rot (three-call path),
 the append bits and the output exactly as the named parity tests do."""
 import os
 import random
@@ -28,7 +29,7 @@ def _draw(seed):
         P, mps, maxlen = r.choice([11, 16, 32, 100]), 1, None
         maxlen = P
     else:
-        P, mps, maxlen = r.choice([16, 32, 64]), None, r.choice([64, 300, 900])
+        P, mps, maxlen = r.choice([8, 16, 32, 64]), None, r.choice([64, 300, 900])
     B = r.randint(1, 24)
     lens = []
     for _ in range(B):
@@ -55,6 +56,7 @@ def _draw(seed):
     if path == "fused" and r.random() < 0.5:
         opts["pdl"] = True
         opts["pdl_kv"] = r.random() < 0.5
+    opts["planned"] = r.random() < 0.35
     inp = workloads.make_case(B=B, Hq=G * Hkv, Hkv=Hkv, D=D, P=P, seq_lens=lens, active=active,
                               max_pages_per_seq=mps, seed=seed, device="cuda", dtype=dtype, layout=layout)
     return inp, opts

@@ -488,3 +488,16 @@ def test_one_head_box_fallback(layout, path, monkeypatch):
     H.full_check(inp, path=path)
     inp = case([17, 9, 300, 1], Hq=16, Hkv=8, D=64, seed=95, layout=layout, dtype=torch.float16)
     H.full_check(inp, path=path, interleaved=True)
+
+
+# ---------------------------------------------------------------- launch plan
+
+def test_launch_plan_keeps_two_ctas_per_sm():
+    # the attention kernels are planned for two resident CTAs per SM (four kv
+    # heads per CTA at head_dim 128, two pipeline stages): a plan whose shared
+    # memory grows past half an SM halves the CTA count and the bandwidth
+    v = H.vh()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = 8 // 4
+    assert v.vh_decode_num_ctas(64, 16, 8, 128, 16) == 2 * sms // groups
+    assert v.vh_decode_num_ctas(256, 32, 8, 128, 64) == 2 * sms // groups

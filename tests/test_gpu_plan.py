@@ -1,0 +1,160 @@
+"""The per-step plan (vh_decode_plan) and 8-token pages, against the float64 oracle.
+
+A plan is written once per decode step and read by every attention launch of
+that step (each layer's call on its own KV pool).  Checked here: both paths
+on every workload with a plan, one plan reused by the 28 layer calls of a
+high-concurrency step (programmatic dependent launches between them, as a
+model runs them), plans that do not match the launch (another CTA count,
+the other path, none written) being ignored, and the data-error flags the
+plan raises.  Pages of 8 tokens (every 16-token tile spans two pages) are
+checked on both paths, both page layouts, with and without a plan.
+"""
+import pytest
+import torch
+
+import gpu_harness as H
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def case(lens, *, active=None, Hq=8, Hkv=2, D=128, P=16, seed=1, mps=None, **kw):
+    return workloads.make_case(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, P=P, seq_lens=lens, active=active,
+                               max_pages_per_seq=mps, seed=seed, device="cuda", **kw)
+
+
+# ---------------------------------------------------------------- planned launches
+
+@pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("name", ["tiny", "c64", "padded", "long", "high", "fastar"])
+def test_planned_workload_parity(name, path):
+    inp = workloads.make_inputs(name, device="cuda")
+    H.full_check(inp, path=path, planned=True, rows=list(range(0, inp.B, 4)) if name == "high" else None)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("name", ["c64", "padded", "long"])
+def test_planned_fused_with_early_kv_and_repeats(name, graph):
+    inp = workloads.make_inputs(name, device="cuda")
+    H.full_check(inp, path="fused", planned=True, pdl=True, pdl_kv=True, graph=graph, repeat=3)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_planned_edge_cases(path):
+    for inp in (case([1, 1, 1], seed=40), case([16, 32, 4096, 1, 17], seed=41),
+                case([200, 1, 500], active=[1, 0, 1], seed=42), case([1], active=[0], seed=43)):
+        H.full_check(inp, path=path, planned=True)
+    for n in (1, 3, 1000):
+        H.full_check(case([300, 17, 1200, 5], Hq=16, Hkv=8, seed=44), path=path, planned=True, num_ctas=n)
+
+
+def _layer_step(path, L, rows_every):
+    """One plan, then L layer calls of the high-concurrency step (each layer
+    its own pool, q, k and v; one batch).  Returns the per-layer outputs and
+    pools after the step."""
+    v = H.vh()
+    layers = [workloads.make_inputs("high", layer=l, device="cuda") for l in range(L)]
+    g0 = layers[0]
+    B, Hq, Hkv, D, P = g0.B, g0.Hq, g0.Hkv, g0.D, g0.P
+    cos_sin = torch.empty((g0.max_pages_per_seq * P, D), dtype=torch.float32, device="cuda")
+    v.vh_rope_table(cos_sin, g0.theta)
+    ws = v.alloc_workspace(B, Hq, Hkv, D, P, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rot = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    outs = [torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    v.vh_decode_plan(g0.seq_lens, g0.active, g0.page_table, ws, Hq=Hq, Hkv=Hkv, D=D, page_size=P,
+                     num_pages=g0.num_pages, max_pos=cos_sin.shape[0], err_flag=err, three_call=path == "three")
+    for l, li in enumerate(layers):
+        if path == "fused":
+            # each launch a programmatic dependent of the previous layer's, its
+            # first cached tiles requested before the wait (another pool)
+            v.vh_decode_fused(li.q, li.k_new, li.v_new, cos_sin, li.pool[:, 0], li.pool[:, 1], g0.page_table,
+                              g0.seq_lens, g0.active, outs[l], ws, err_flag=err, pdl=l > 0, pdl_kv=l > 0,
+                              planned=True)
+        else:
+            v.decode_step(li.q, li.k_new, li.v_new, cos_sin, li.pool[:, 0], li.pool[:, 1], g0.page_table,
+                          g0.seq_lens, g0.active, q_rot, outs[l], ws, err_flag=err, planned=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = list(range(0, B, rows_every))
+    for l, li in enumerate(layers):
+        fresh = workloads.make_inputs("high", layer=l, device="cuda").to("cpu")
+        ref = oracle.reference_step(fresh, rows=rows)
+        H.check_out(fresh, ref["out"], outs[l].cpu(), rows=rows)
+        if l in (0, L - 1):
+            H.check_append(fresh, ref, li.pool.cpu())
+        del fresh, ref
+        layers[l] = None
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_one_plan_reused_by_the_28_layer_calls_of_a_step(path):
+    _layer_step(path, 28, rows_every=16)
+
+
+def test_plan_that_does_not_match_the_launch_is_ignored():
+    v = H.vh()
+    inp = case([300, 17, 1200, 5, 64], Hq=16, Hkv=8, seed=45)
+    cpu = inp.to("cpu")
+    ref = oracle.reference_step(cpu)
+    for plan_kw, call in [({"num_ctas": 7}, {"num_ctas": 0}),          # another CTA count
+                          ({"three_call": True}, {}),                  # planned for the other path
+                          (None, {})]:                                 # never planned
+        g = inp.clone()
+        B, Hq, Hkv, D, P = g.B, g.Hq, g.Hkv, g.D, g.P
+        cos_sin = torch.empty((g.max_pages_per_seq * P, D), dtype=torch.float32, device="cuda")
+        v.vh_rope_table(cos_sin, g.theta)
+        ws = v.alloc_workspace(B, Hq, Hkv, D, P, 7, device="cuda")
+        ws_auto = v.vh_decode_workspace_bytes(B, Hq, Hkv, D, P)
+        if ws.numel() < ws_auto:
+            ws = torch.zeros(ws_auto, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if plan_kw is not None:
+            v.vh_decode_plan(g.seq_lens, g.active, g.page_table, ws, Hq=Hq, Hkv=Hkv, D=D, page_size=P,
+                             num_pages=g.num_pages, max_pos=cos_sin.shape[0], err_flag=err, **plan_kw)
+        v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, g.pool[:, 0], g.pool[:, 1], g.page_table, g.seq_lens,
+                          g.active, out, ws, err_flag=err, planned=True, **call)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        H.check_out(cpu, ref["out"], out.cpu())
+        H.check_append(cpu, ref, g.pool.cpu())
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_plan_flags_bad_lengths_and_positions(path):
+    inp = case([50, 60, 70], seed=46)
+    inp.seq_lens[1] = inp.max_pages_per_seq * inp.P + 5
+    got = H.run_step(inp, path=path, planned=True)
+    assert got["err"] & 1
+    assert not got["out"][1].any()
+    inp = case([20, 30], seed=47)
+    got = H.run_step(inp, positions=torch.tensor([3, 10_000], dtype=torch.int32), max_pos=64, path=path,
+                     planned=True)
+    assert got["err"] & 4
+    if path == "fused":
+        assert not got["out"][1].any(), "a row with an invalid position is treated as padding"
+
+
+# ---------------------------------------------------------------- 8-token pages
+
+@pytest.mark.parametrize("planned", [False, True])
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("path", H.PATHS)
+def test_eight_token_pages(path, layout, planned):
+    # lengths on and around page and tile boundaries: a tile's second page
+    # missing (<= 8 live tokens), present, and the new token in either page
+    for lens, seed in ([1, 7, 8, 9, 15, 16, 17, 24, 25, 300], 50), ([1023, 512, 33, 2], 51):
+        inp = case(lens, P=8, Hq=16, Hkv=8, seed=seed, layout=layout)
+        H.full_check(inp, path=path, planned=planned)
+    inp = case([100, 9, 64], P=8, Hq=8, Hkv=8, D=64, seed=52, layout=layout, dtype=torch.float16)
+    H.full_check(inp, path=path, planned=planned, interleaved=True)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_eight_token_pages_split_rows_and_early_kv(path):
+    inp = case([4000, 3, 2500], P=8, Hq=32, Hkv=8, seed=53)
+    H.full_check(inp, path=path, num_ctas=200)
+    if path == "fused":
+        H.full_check(inp, path=path, pdl=True, pdl_kv=True, graph=True, repeat=2, planned=True)

@@ -51,3 +51,16 @@ def test_head_major_pages_hold_the_token_major_values():
     assert b.v_cache().data_ptr() - b.k_cache().data_ptr() == a.P * a.Hkv * a.D * 2
     c = b.clone()
     assert c.layout == "HND" and torch.equal(_bits(c.pool), _bits(b.pool))
+
+
+def test_layers_of_one_step_share_the_batch_but_not_the_values():
+    # every layer of a multi-layer step sees the same lengths, active rows and
+    # page table; its pool and q/k/v values are its own
+    a = workloads.make_inputs("fastar", layer=0)
+    b = workloads.make_inputs("fastar", layer=3)
+    assert torch.equal(a.seq_lens, b.seq_lens) and torch.equal(a.page_table, b.page_table)
+    assert not torch.equal(_bits(a.q), _bits(b.q)) and not torch.equal(_bits(a.pool), _bits(b.pool))
+    c = workloads.make_inputs("fastar", layer=4)          # the next step: a new draw of everything
+    assert c.meta["step_first_layer"] == 4 and not torch.equal(_bits(c.q), _bits(a.q))
+    # first layer of a step unchanged by the sharing (the draw of a one-layer workload)
+    assert a.meta["step_first_layer"] == 0 and workloads.make_inputs("tiny", layer=5).meta["step_first_layer"] == 5

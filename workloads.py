@@ -15,7 +15,8 @@ The five workloads are the serving shapes of the Talker decode step:
   * "long"    -- 16 rows, 32 q / 8 kv heads, lengths uniform in [2048, 8192];
   * "high"    -- 256 rows, 32 q / 8 kv heads, pages of 64 tokens, lengths
                  log-uniform in [256, 4096], values N(0, 0.5), 28 layers that
-                 each own a separate KV pool;
+                 each own a separate KV pool (the layers of one decode step
+                 share the batch: lengths, active rows and page table);
   * "fastar"  -- the Fast AR step: 64 rows, 16 q / 8 kv heads, head_dim 64,
                  a contiguous per-request cache of 11 positions (10 residual
                  codebooks + 1) per layer, 4 layers, every row at its last
@@ -28,7 +29,10 @@ page_size, num_kv_heads, head_dim], K at [:, 0] and V at [:, 1]; on request
 the same values are stored head-major, [num_pages, 2, num_kv_heads,
 page_size, head_dim] (the other layout generic paged attention offers).
 
-Recipe (seed = 20260000 + 100 * workload_index + layer, torch.Generator):
+Recipe (seed = 20260000 + 100 * workload_index + layer, torch.Generator; for
+the layers of one step of a multi-layer workload, steps 1-3 come from the
+seed of the step's first layer, so every layer sees the same batch, and the
+values of steps 4-5 from the layer's own seed):
   1. seq_lens: integers uniform in [lo, hi], or floor(exp(U(ln lo, ln hi)))
      clamped to [lo, hi] for the log-uniform workload; "tiny" uses its fixed
      list.  A length counts the token being appended (position = len - 1).
@@ -203,7 +207,8 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
               max_pages_per_seq: int | None = None, sigma: float = 1.0, seed: int = 0,
               device="cpu", pool_pages: int = 0, theta: float = 10000.0,
               poison: bool = True, page_order: str = "random",
-              dtype: torch.dtype = torch.bfloat16, layout: str = "NHD") -> DecodeInputs:
+              dtype: torch.dtype = torch.bfloat16, layout: str = "NHD",
+              value_seed: int | None = None) -> DecodeInputs:
     """Draw one layer of inputs for explicit shapes and lengths.
 
     `seq_lens` and `active` are Python sequences (or int64 tensors) of length B.
@@ -211,6 +216,8 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     unless the caller passes other lengths for them on purpose.
     `page_order` is "random" (seeded permutation) or "linear" (pages 1, 2, ...).
     `dtype` (torch.bfloat16 or torch.float16) is the type of q, k, v and the pool.
+    `value_seed` (if given) seeds the pool and q/k/v values instead of `seed`,
+    which then fixes only the page permutation.
     `layout` "HND" stores the same pool values head-major ([NP, 2, Hkv, P, D]);
     "CONTIG" makes one cache of P positions per row (row b owns page b, no
     page permutation) stored as [2, B, Hkv, P, D], with an identity page
@@ -247,7 +254,12 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     # Values are drawn on the target device from a seed derived from the CPU generator.
     dev = torch.device(device)
     dgen = torch.Generator(device=dev)
-    dgen.manual_seed(int(torch.randint(0, 2**62, (1,), generator=gen)))
+    vseed = int(torch.randint(0, 2**62, (1,), generator=gen))
+    if value_seed is not None:
+        vgen = torch.Generator(device="cpu")
+        vgen.manual_seed(value_seed)
+        vseed = int(torch.randint(0, 2**62, (1,), generator=vgen))
+    dgen.manual_seed(vseed)
     pool = (torch.randn((NP, 2, P, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(dtype)
     q = torch.randn((B, Hq, D), generator=dgen, device=dev, dtype=torch.float32).to(dtype)
     k_new = (torch.randn((B, Hkv, D), generator=dgen, device=dev, dtype=torch.float32) * sigma).to(dtype)
@@ -278,13 +290,12 @@ def make_case(*, B: int, Hq: int, Hkv: int, D: int, P: int, seq_lens, active=Non
     )
 
 
-def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = torch.bfloat16,
-                layout: str | None = None) -> DecodeInputs:
-    """Inputs of one layer of a named workload (see the module docstring)."""
+def step_structure(name: str, first_layer: int = 0):
+    """(seq_lens, active, page-permutation seed) of the step whose first layer
+    is `first_layer` (steps 1-2 of the recipe)."""
     w = WORKLOADS[name]
-    seed = SEED_BASE + 100 * w.index + layer
     gen = torch.Generator(device="cpu")
-    gen.manual_seed(seed)
+    gen.manual_seed(SEED_BASE + 100 * w.index + first_layer)
     lens = draw_lengths(w, gen, w.B)
     if w.n_active is not None:
         rows = torch.randperm(w.B, generator=gen)[: w.n_active]
@@ -294,11 +305,25 @@ def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = to
     else:
         act = torch.ones(w.B, dtype=torch.int64)
     sub_seed = int(torch.randint(0, 2**31 - 1, (1,), generator=gen))
+    return lens, act, sub_seed
+
+
+def make_inputs(name: str, layer: int = 0, device="cpu", dtype: torch.dtype = torch.bfloat16,
+                layout: str | None = None) -> DecodeInputs:
+    """Inputs of one layer of a named workload (see the module docstring).
+
+    For a workload of L > 1 layers, layer l belongs to the step whose first
+    layer is l - l % L: the lengths, active rows and page table are those of
+    that first layer, the pool and q/k/v values the layer's own."""
+    w = WORKLOADS[name]
+    seed = SEED_BASE + 100 * w.index + layer
+    first = layer - layer % w.layers
+    lens, act, sub_seed = step_structure(name, first)
     inp = make_case(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, P=w.P, seq_lens=lens, active=act,
                     max_pages_per_seq=w.max_pages_per_seq, sigma=w.sigma, seed=sub_seed,
                     device=device, pool_pages=w.pool_pages, theta=w.theta, dtype=dtype,
-                    layout=layout or w.layout)
-    inp.meta.update({"workload": name, "layer": layer, "workload_seed": seed})
+                    layout=layout or w.layout, value_seed=None if layer == first else seed)
+    inp.meta.update({"workload": name, "layer": layer, "workload_seed": seed, "step_first_layer": first})
     return inp
 
 
