@@ -267,9 +267,10 @@ bool plan_attn(AttnParams& p, const DeviceInfo& dev, bool fused, int* auto_n) {
 // Fused launches that request their first stages before the dependency wait
 // (VH_FLAG_PDL_KV): right after the wait, while the q rows are in flight,
 // each CTA prefetches the next kL2PrefetchTiles tiles (no free stage yet) into
-// L2, so the start of the stream does not wait for HBM.  One tile measured
-// best (c64 30.19 -> 29.81 us, padded 13.41 -> 12.90 us, long 62.0 -> 61.6 us);
-// more delay the q copies that gate the consumers; the same prefetch issued
+// L2, so the start of the stream does not wait for HBM (the kernel adds one
+// more for long ranges).  One tile measured best for every range (c64 30.19
+// -> 29.81 us, padded 13.41 -> 12.90 us, long 62.0 -> 61.6 us); more delay the
+// q copies that gate the consumers of short ranges; the same prefetch issued
 // before the wait slowed the previous kernel's end, and in launches without
 // early stages (three-call attention, fused without PDL) it cost 1.2-1.4 us.
 constexpr int kL2PrefetchTiles = 1;
