@@ -102,6 +102,8 @@ def parse():
                     help="layer calls per step (default: the workload's own count, 28 for 'high')")
     ap.add_argument("--ncu-case", action="store_true",
                     help="eager launches of the fused and the three-call step on one pool (profiling)")
+    ap.add_argument("--planned", action="store_true",
+                    help="with --ncu-case: the launches read a per-step plan (vh_decode_plan, written once)")
     return ap.parse_args()
 
 
@@ -328,13 +330,16 @@ class Setup:
 
 
 def run_ncu_case(args):
-    """A few eager launches on one pool: 3 fused, 3 three-call steps."""
+    """A few eager launches on one pool: 3 fused, 3 three-call steps (with
+    --planned the fused launches read a plan written once before them)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     s = Setup(args.workload, 0, dev, replicas=1, layers=1, dtype=args.dtype, interleaved=args.interleaved,
               layout=args.layout)
+    if args.planned:
+        s.plan(0)
     for _ in range(3):
-        s.fused(0, pdl=False)
+        s.fused(0, pdl=False, planned=args.planned)
     for _ in range(3):
         s.three(0)
     torch.cuda.synchronize()

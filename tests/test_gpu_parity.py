@@ -87,7 +87,7 @@ def test_gqa_groups_and_head_dims(G, D, path):
 
 
 @pytest.mark.parametrize("path", H.PATHS)
-@pytest.mark.parametrize("P", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("P", [8, 16, 32, 64, 128, 256])
 def test_page_sizes(P, path):
     H.full_check(case([1, P - 1, P, P + 1, 3 * P + 5], P=P, Hq=8, Hkv=4, seed=P), path=path)
 
