@@ -214,6 +214,126 @@ __device__ __forceinline__ void merge_pieces(const float* __restrict__ part_lse,
   }
 }
 
+// Merge of a row's pieces for the fused kernel, staged through shared memory
+// (used for rows of many pieces): the warp's own slices of the pipeline stages
+// are free once its tile loop is done (kv head w's 2 KB rows of every
+// 64-column block of K and V, of every stage: 2 * HALVES * S slices), so each
+// round brings up to `nchunk / SUB` pieces (G*D*4 bytes each, SUB 2 KB copies)
+// with bulk copies completed on the warp's own mbarrier, while the lanes load
+// the pieces' lse values; then the round is folded into the running max / sum
+// / accumulator as merge_pieces does.  One round trip per 8 pieces (4 at
+// head_dim 64 or G = 8) instead of one per 16/G pieces.  The warp initialises
+// its mbarrier on first use (phase 0 then).  Returns false if a wait ran out
+// of time (after a second bounded wait for the copies of the round).
+template <int D, int G, typename E>
+__device__ __forceinline__ bool merge_pieces_staged(const float* __restrict__ part_lse,
+                                                    const float* __restrict__ part_o, long long slot_base, int HG,
+                                                    int wg, int cf, int np, int first_slot,
+                                                    uint16_t* __restrict__ out_row, int lane, uint32_t stage0,
+                                                    int stage_bytes, int S, int Hc, int w, uint32_t bar,
+                                                    uint32_t& phase) {
+  constexpr int PER = D / 32;
+  constexpr int HALVES = D / 64;
+  constexpr int PIECE = G * D * 4;                 // bytes of one piece for this warp's G heads
+  constexpr int SUB = (PIECE + 2047) / 2048;       // 2 KB slices per piece
+  constexpr int HPS = 2048 / (D * 4);              // heads per slice
+  constexpr int PR = (2 * HALVES * 2) / SUB;       // pieces per round with two stages (upper bound)
+  const float NEG_INF = __int_as_float(0xff800000);
+  const int nchunk = 2 * HALVES * S;
+  const int pr = min(PR, nchunk / SUB);
+  auto chunk = [&](int i) -> uint32_t {
+    const int st = i / (2 * HALVES), rem = i % (2 * HALVES), kv = rem / HALVES, hf = rem % HALVES;
+    return stage0 + static_cast<uint32_t>(st * stage_bytes + kv * (stage_bytes / 2) + hf * Hc * 2048 + w * 2048);
+  };
+  auto idx_of = [&](int j) -> long long {
+    return (slot_base + 2LL * (cf + j) + (j == 0 ? first_slot : 0)) * HG + wg;
+  };
+  float M[G], o[G][PER], ws[G];
+#pragma unroll
+  for (int n = 0; n < G; ++n) {
+    M[n] = NEG_INF;
+    ws[n] = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[n][i] = 0.f;
+  }
+  if (phase == 0u && lane == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  // the warp's slices were last read by ldmatrix and written by the tile copies
+  // and the new-token patch: order those accesses before the bulk copies
+  fence_proxy_async_smem();
+  __syncwarp();
+  for (int j0 = 0; j0 < np; j0 += pr) {
+    const int nr = min(pr, np - j0);
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * PIECE));
+    __syncwarp();
+    if (lane < nr * SUB) {
+      const int u = lane / SUB, sb = lane % SUB;
+      const int bytes = min(2048, PIECE - sb * 2048);
+      bulk_g2s(chunk(lane), part_o + idx_of(j0 + u) * D + sb * (2048 / 4), static_cast<uint32_t>(bytes), bar);
+    }
+    float lv[PR][G];
+#pragma unroll
+    for (int u = 0; u < PR; ++u) {
+      const int j = j0 + u;
+      const long long ix = idx_of(u < nr ? j : j0);  // (pieces past the row are not loaded)
+#pragma unroll
+      for (int n = 0; n < G; ++n) lv[u][n] = (u < nr) ? __ldcg(part_lse + ix + n) : NEG_INF;
+    }
+    const bool ok = mbar_wait(bar, phase & 1u) || mbar_wait(bar, phase & 1u);
+    ++phase;
+    if (!ok) return false;
+#pragma unroll
+    for (int n = 0; n < G; ++n) {
+      float mb = M[n];
+#pragma unroll
+      for (int u = 0; u < PR; ++u) mb = fmaxf(mb, lv[u][n]);
+      const float sc = exp2f(M[n] - mb);  // 0 on the first round (M = -inf)
+      ws[n] *= sc;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) o[n][i] *= sc;
+#pragma unroll
+      for (int u = 0; u < PR; ++u) {
+        if (u < nr) {
+          const float wgt = exp2f(lv[u][n] - mb);
+          ws[n] += wgt;
+          const uint32_t a = chunk(u * SUB + n / HPS) + static_cast<uint32_t>((n % HPS) * D * 4 + lane * PER * 4);
+          if constexpr (PER == 4) {
+            float4 t;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(t.x), "=f"(t.y), "=f"(t.z), "=f"(t.w) : "r"(a));
+            o[n][0] += wgt * t.x;
+            o[n][1] += wgt * t.y;
+            o[n][2] += wgt * t.z;
+            o[n][3] += wgt * t.w;
+          } else {
+            float2 t;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(t.x), "=f"(t.y) : "r"(a));
+            o[n][0] += wgt * t.x;
+            o[n][1] += wgt * t.y;
+          }
+        }
+      }
+      M[n] = mb;
+    }
+    // the next round's copies overwrite the slices just read
+    __syncwarp();
+    fence_proxy_async_smem();
+  }
+#pragma unroll
+  for (int n = 0; n < G; ++n) {
+    const float iw = 1.f / ws[n];
+    uint16_t* dst = out_row + static_cast<long long>(n) * D + lane * PER;
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(E::pack2(o[n][0] * iw, o[n][1] * iw), E::pack2(o[n][2] * iw, o[n][3] * iw));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = E::pack2(o[n][0] * iw, o[n][1] * iw);
+    }
+  }
+  return true;
+}
+
 template <int D, int G, bool FUSED, typename E>
 __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __grid_constant__ AttnParams p) {
   constexpr int KSTEPS = D / 16;  // k-steps of the score product = m-tiles of the value product
@@ -231,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
   int* posv = reinterpret_cast<int*>(smem + p.pos_off);
   long long* meta = reinterpret_cast<long long*>(smem + p.meta_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  int* misc = reinterpret_cast<int*>(smem + p.bar_off + 8 * (2 * S + 5));
+  int* misc = reinterpret_cast<int*>(smem + p.bar_off + 8 * (2 * S + 5 + kMaxHc));
   volatile int* abort_flag = misc + kMiscAbort;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + S);
   const uint32_t qfull = smem_addr(bars + 2 * S), qempty = smem_addr(bars + 2 * S + 1);
@@ -1103,12 +1223,25 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
         return;
       }
       const int nv = *reinterpret_cast<volatile int*>(misc + kMiscNVerdict);
+      uint32_t mphase = 0;
       for (int k = 0; k < nv; ++k) {
         const int* v = misc + kMiscVerdict + 5 * k;
         if (!v[0]) continue;
-        merge_pieces<D, G, E>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, v[2],
-                           v[3] - v[2] + 1, v[4],
-                           p.out + (static_cast<long long>(v[1]) * p.Hq + static_cast<long long>(h) * G) * D, lane);
+        const int np = v[3] - v[2] + 1;
+        uint16_t* orow = p.out + (static_cast<long long>(v[1]) * p.Hq + static_cast<long long>(h) * G) * D;
+        if (np > 32 / G) {
+          // rows of many pieces (three or more batches of register loads): bring the
+          // pieces in through the warp's free stage slices, 2 KB bulk copies
+          if (!merge_pieces_staged<D, G, E>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G,
+                                            v[2], np, v[4], orow, lane, smem_addr(smem), p.stage_bytes, S, Hc, w,
+                                            smem_addr(bars + 2 * S + 5 + w), mphase)) {
+            if (lane == 0) flag_error(p.err_flag, VH_ERR_TIMEOUT);
+            return;
+          }
+        } else {
+          merge_pieces<D, G, E>(p.part_lse, p.part_o, static_cast<long long>(gy) * p.N * 2, HG, w * G, v[2], np,
+                             v[4], orow, lane);
+        }
       }
     }
   }

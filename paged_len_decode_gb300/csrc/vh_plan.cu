@@ -133,7 +133,7 @@ static bool plan_attn_uncached(AttnParams& p, const DeviceInfo& dev, bool fused)
     p.q_bytes = static_cast<int>(hg * p.q_row_bytes + (fused ? p.D * 4 : 0));
     const size_t qs_bytes = fused ? static_cast<size_t>(hc) * p.G * (p.D * 4 + 32) : 0;
     fixed = align_up(p.q_bytes, 128) + align_up(qs_bytes, 128) + align_up(4 * (static_cast<size_t>(p.B) + 1), 16) +
-            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 5) + 48 * 4 + 256 +
+            2 * align_up(4 * static_cast<size_t>(p.B), 16) + 8 * kMaxStages + 8 * (2 * kMaxStages + 5 + 8) + 48 * 4 + 256 +
             1024 /* alignment of the base */;
     stages = fixed < budget ? static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / p.stage_bytes)) : 0;
     if (stages >= 2 || hc == 1) break;
@@ -159,7 +159,7 @@ static bool plan_attn_uncached(AttnParams& p, const DeviceInfo& dev, bool fused)
   p.meta_off = static_cast<int>(off);
   off += 8 * static_cast<size_t>(stages);
   p.bar_off = static_cast<int>(align_up(off, 16));
-  off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 5) + 48 * 4;
+  off = p.bar_off + 8 * (2 * static_cast<size_t>(stages) + 5 + 8) + 48 * 4;
   // + up to 1024 bytes that the kernel skips to align its base for the boxes
   p.smem_bytes = static_cast<int>(align_up(off, 128) + 1024);
   p.min_tiles = kMinTilesPerCta;

@@ -123,6 +123,17 @@ def test_rows_split_into_many_pieces(path):
 
 
 @pytest.mark.parametrize("path", H.PATHS)
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_many_pieces_every_group_and_head_dim(G, D, path):
+    # a 3000-token and a 700-token row over 96 CTAs per head group: the long
+    # row splits into ~78 pieces, so the fused merge stages them through
+    # shared memory in every slice layout (one 2 KB slice per piece, two at
+    # G = 8 and head_dim 128; 8 pieces per round at head_dim 128, 4 at 64)
+    H.full_check(case([3000, 700, 5], Hq=G * 4, Hkv=4, D=D, seed=200 + G * 10 + D), path=path, num_ctas=96)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
 def test_single_very_long_row(path):
     # one row of 32768 tokens (2048 tiles) with G = 4: every CTA of a head
     # group takes a piece of it, so one CTA merges ~150 pieces
