@@ -80,3 +80,29 @@ def test_traffic_record_must_match_kernel_sources(tmp_path):
     f.write_text("kernel source sha256[:16]: 0000000000000000\ndram bytes per launch (read + write): 1\n")
     assert bench.recorded_traffic("c64", str(f)) is None
     assert bench.recorded_traffic("c64", str(tmp_path / "missing.md")) is None
+
+
+def test_clock_summary_uses_samples_under_load_and_collects_throttle_reasons():
+    # nvidia-smi csv rows: index, sm, max sm, power, active reasons, hw_slowdown,
+    # hw_thermal, sw_thermal, sw_power_cap, utilisation
+    rows = ["0, 1000, 2070, 200.0, 0x0, Not Active, Not Active, Not Active, Not Active, 0",
+            "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active, 100",
+            "0, 2055, 2070, 950.0, 0x4, Not Active, Not Active, Not Active, Active, 98",
+            "0, 2070, 2070, 910.0, 0x0, Not Active, Not Active, Not Active, Not Active, 99",
+            "garbage line"]
+    c = bench.Clocks.summarise(rows)
+    assert c["samples"] == 4 and c["samples_under_load"] == 3
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0       # the idle 1000 MHz sample is left out
+    assert c["reasons"] == ["sw_power_cap"]
+    assert c["power_w_median"] == 910.0
+    idle = bench.Clocks.summarise(rows[:1])                           # no sample under load: all samples
+    assert idle["samples_under_load"] == 0 and idle["sm_mhz"] == 1000.0
+
+
+def test_rates_fractions_of_measured_peak_and_specification():
+    by = {"step": 6_000_000, "active": 64}
+    r = bench.rates(by, ms_step=0.001, world=2, peak=6000.0, L=4)     # 1 us per step
+    assert r["hbm_gbs"] == 6000.0 and r["frac_of_peak"] == 1.0
+    assert r["frac_of_spec"] == round(6000.0 / bench.SPEC_HBM_GBS, 4)
+    assert r["tokens_per_s"] == 64 * 2 / 1e-6                        # whole job: both ranks
+    assert r["ms_per_launch"] == 0.00025
