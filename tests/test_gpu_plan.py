@@ -6,8 +6,10 @@ on every workload with a plan, one plan reused by the 28 layer calls of a
 high-concurrency step (programmatic dependent launches between them, as a
 model runs them), plans that do not match the launch (another CTA count,
 the other path, none written) being ignored, and the data-error flags the
-plan raises.  Pages of 8 tokens (every 16-token tile spans two pages) are
-checked on both paths, both page layouts, with and without a plan.
+plan raises, and the benchmark's chain (one plan, then layer launches
+linked by programmatic dependent launch) captured in a CUDA graph.  Pages of
+8 tokens (every 16-token tile spans two pages) are checked on both paths,
+both page layouts, with and without a plan.
 """
 import pytest
 import torch
@@ -158,3 +160,69 @@ def test_eight_token_pages_split_rows_and_early_kv(path):
     H.full_check(inp, path=path, num_ctas=200)
     if path == "fused":
         H.full_check(inp, path=path, pdl=True, pdl_kv=True, graph=True, repeat=2, planned=True)
+
+
+def test_plan_and_layer_chain_captured_in_a_graph():
+    # the chain the benchmark times: one plan, then four layers' fused launches
+    # (each its own pool, one batch), each a programmatic dependent of the
+    # previous with its first K/V tiles requested before the wait, captured
+    # in a CUDA graph and replayed twice
+    v = H.vh()
+    base = workloads.make_inputs("c64", device="cuda")
+    layers = []
+    for l in range(4):
+        li = base.clone()
+        g = torch.Generator(device="cuda").manual_seed(900 + l)
+        live = ~torch.isnan(li.pool.float())
+        li.pool[live] = torch.randn(int(live.sum()), generator=g, device="cuda").to(li.pool.dtype)
+        li.q.copy_(torch.randn(li.q.shape, generator=g, device="cuda").to(li.q.dtype))
+        li.k_new.copy_(torch.randn(li.k_new.shape, generator=g, device="cuda").to(li.k_new.dtype))
+        li.v_new.copy_(torch.randn(li.v_new.shape, generator=g, device="cuda").to(li.v_new.dtype))
+        layers.append(li)
+    refs = [oracle.reference_step(li.to("cpu")) for li in layers]
+    B, Hq, Hkv, D, P = base.B, base.Hq, base.Hkv, base.D, base.P
+    cos_sin = torch.empty((base.max_pages_per_seq * P, D), dtype=torch.float32, device="cuda")
+    v.vh_rope_table(cos_sin, base.theta)
+    ws = v.alloc_workspace(B, Hq, Hkv, D, P, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in layers]
+    pools0 = [li.pool.clone() for li in layers]
+
+    def step():
+        v.vh_decode_plan(base.seq_lens, base.active, base.page_table, ws, Hq=Hq, Hkv=Hkv, D=D, page_size=P,
+                         num_pages=base.num_pages, max_pos=cos_sin.shape[0], err_flag=err)
+        for l, li in enumerate(layers):
+            v.vh_decode_fused(li.q, li.k_new, li.v_new, cos_sin, li.pool[:, 0], li.pool[:, 1], base.page_table,
+                              base.seq_lens, base.active, outs[l], ws, err_flag=err, pdl=l > 0, pdl_kv=l > 0,
+                              planned=True)
+
+    step()  # first calls outside the capture
+    torch.cuda.synchronize()
+    cg = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(cg, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for l, li in enumerate(layers):
+            li.pool.copy_(pools0[l])
+            outs[l].fill_(float("nan"))
+        cg.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for l, li in enumerate(layers):
+            cpu = li.to("cpu")
+            H.check_out(cpu, refs[l]["out"], outs[l].cpu())
+            H.check_append(cpu, refs[l], li.pool.cpu())  # (uses the lengths, flags and page table only)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_many_pieces_fp16_interleaved_rmsnorm(path):
+    # the staged merge of many pieces with fp16 outputs, next to the other options
+    g = torch.Generator().manual_seed(61)
+    norm = {"q": (1.0 + 0.2 * torch.randn(128, generator=g)).float(),
+            "k": (1.0 + 0.2 * torch.randn(128, generator=g)).float(), "eps": 1e-6}
+    inp = case([2500, 900, 3], Hq=16, Hkv=4, D=128, seed=62, dtype=torch.float16, layout="HND")
+    H.full_check(inp, path=path, num_ctas=80, interleaved=True, norm=norm)
