@@ -94,8 +94,9 @@ def parse():
     ap.add_argument("--pdl", type=int, default=1,
                     help="programmatic dependent launch between the timed fused steps (1/0; 0 also turns "
                          "off the early K/V requests)")
-    ap.add_argument("--e2e-pdl", type=int, default=0,
-                    help="programmatic dependent launch between the pipelined e2e steps (1/0)")
+    ap.add_argument("--e2e-pdl", type=int, default=1,
+                    help="programmatic dependent launch between the pipelined e2e steps' kernels (1/0; each "
+                         "kernel still waits for its own input copy)")
     ap.add_argument("--qk-norm", action="store_true",
                     help="per-head RMSNorm of q and the new key before RoPE (unit weights, eps 1e-6)")
     ap.add_argument("--layers", type=int, default=None,
@@ -441,9 +442,10 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
                 stream.wait_event(h2d_done[i])
                 if i >= 2:
                     stream.wait_event(d2h_done[i - 2])  # this output has been copied out
-                # programmatic dependent launch on the previous step's kernel: the
-                # inputs this launch reads before its wait come from its own
-                # copy, a full dependency
+                # programmatic dependent launch on the previous step's kernel
+                # (which writes another pool and the other output): the inputs
+                # this launch reads before its wait come from its own copy, a
+                # full dependency of the launch
                 s.fused(i % R, pdl=args.e2e_pdl, src=d_ins[b], out=outs[b])
                 k_done[i].record(stream)
                 with torch.cuda.stream(s_d2h):
