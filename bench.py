@@ -22,12 +22,15 @@ median replay time / K.  A synchronize and a barrier bracket the whole timed
 region, and the max over ranks is taken.  nvidia-smi samples the clocks
 across all replays.  `e2e` goes through the public Python call with pinned
 host buffers: per step the new q/k/v, lengths, flags and page table (one
-input arena) are copied in and the output is copied out.  The headline e2e
-replays a CUDA graph of many steps with two input arenas and two outputs,
-the copies on their own streams overlapping the neighbouring steps'
-kernels, as a serving runtime pipelines its decode steps; `e2e.serial` is
-one graph per step (copy in, call, copy out, in order) and `e2e.eager`
-issues the same copies and call from Python each step.
+input arena) move from host to device and the output back.  The headline
+e2e lets each step's kernel read its inputs from the pinned host arena and
+write its output to pinned host memory in place (VH_FLAG_HOST_IO, over the
+NVLink-C2C link), in a CUDA graph of many steps linked by programmatic
+dependent launch; `e2e.copies` copies the arena in and the output out with
+copy operations on their own streams overlapping the neighbouring steps'
+kernels, as a runtime without host I/O in the kernel pipelines its steps;
+`e2e.serial` is one graph per step (copy in, call, copy out, in order) and
+`e2e.eager` issues the same copies and call from Python each step.
 
 `cpu_baseline` and --impl reference time the float64 CPU oracle as it
 stands on whole steps of the same workload (every active row per call),
@@ -307,12 +310,12 @@ class Setup:
             return pool[:, 0].transpose(1, 2), pool[:, 1].transpose(1, 2)
         return pool[:, 0], pool[:, 1]
 
-    def fused(self, r, pdl=True, src=None, out=None, planned=False):
+    def fused(self, r, pdl=True, src=None, out=None, planned=False, host_io=False):
         s = src or self.inputs(r)
         k, v = self.kv(r)
         self.vh.vh_decode_fused(s.q, s.k_new, s.v_new, self.cos_sin, k, v, s.api_page_table, s.seq_lens,
                                 s.active, self.out if out is None else out, self.wsf, pdl=pdl,
-                                pdl_kv=pdl and self.pdl_kv, planned=planned, **self.norm)
+                                pdl_kv=pdl and self.pdl_kv, planned=planned, host_io=host_io, **self.norm)
 
     def plan(self, r):
         """The step's work list for the fused launches (vh_decode_plan)."""
@@ -456,20 +459,48 @@ def e2e_measure(s, inp, R, by, args, world, dev, stream):
             stream.wait_stream(s_d2h)
     torch.cuda.current_stream().wait_stream(stream)
     e2e_ms = e2e_time(lambda i: gp.replay(), max(1, K_e2e // M), M)
-    e2e_tps = by["active"] * world / (e2e_ms * 1e-3)
 
-    return {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6), "steps": max(1, K_e2e // M) * M,
-            "call": "paged_len_decode_gb300.vh_decode_fused, one pinned-host->device copy of the step's "
-                    "input arena and one device->host copy of its output per step; CUDA graph of "
-                    f"{M} steps with two input arenas and two outputs, the copies on their own streams "
-                    "overlapping the neighbouring steps' kernels"
-                    + (", PDL between the kernels" if args.e2e_pdl else ""),
-            "serial": {"value": round(by["active"] * world / (e2e_serial_ms * 1e-3), 1),
-                       "ms_per_step": round(e2e_serial_ms, 6),
+    # in place over the host link (VH_FLAG_HOST_IO): every step's kernel reads
+    # the step's inputs from the pinned host arena and writes its output into
+    # pinned host memory; no copy nodes, so no copy-to-kernel joins in the
+    # graph, and each kernel is a programmatic dependent of the previous one
+    h_views = {}
+    for k in names:
+        t = getattr(inp, k)
+        n = t.numel() * t.element_size()
+        h_views[k] = h_arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+    h_in = workloads.DecodeInputs(**{**{k: getattr(inp, k) for k in (
+        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool", "layout")}, **h_views})
+    io_bytes_in = sum(getattr(inp, k).numel() * getattr(inp, k).element_size() for k in names)
+    s.fused(0, pdl=False, src=h_in, out=h_outs[0], host_io=True)
+    torch.cuda.synchronize()
+    gz = torch.cuda.CUDAGraph()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(gz, stream=stream):
+            for i in range(M):
+                s.fused(i % R, pdl=True, src=h_in, out=h_outs[i % 2], host_io=True)
+    torch.cuda.current_stream().wait_stream(stream)
+    io_ms = e2e_time(lambda i: gz.replay(), max(1, K_e2e // M), M)
+
+    rate = lambda ms: round(by["active"] * world / (ms * 1e-3), 1)
+    copies = {"value": rate(e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+              "ms_per_step": round(e2e_ms, 6), "steps": max(1, K_e2e // M) * M,
+              "call": "paged_len_decode_gb300.vh_decode_fused, one pinned-host->device copy of the step's "
+                      "input arena and one device->host copy of its output per step; CUDA graph of "
+                      f"{M} steps with two input arenas and two outputs, the copies on their own streams "
+                      "overlapping the neighbouring steps' kernels"
+                      + (", PDL between the kernels" if args.e2e_pdl else "")}
+    host_io = {"value": rate(io_ms), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes_in,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(io_ms, 6), "steps": max(1, K_e2e // M) * M,
+               "call": "paged_len_decode_gb300.vh_decode_fused with VH_FLAG_HOST_IO: each step's kernel reads "
+                       "the step's inputs (q, k_new, v_new, page table, lengths, flags) from pinned host memory "
+                       "and writes its output to pinned host memory, over the NVLink-C2C link; CUDA graph of "
+                       f"{M} steps, PDL between the kernels"}
+    return {**host_io, "copies": copies,
+            "serial": {"value": rate(e2e_serial_ms), "ms_per_step": round(e2e_serial_ms, 6),
                        "call": "one CUDA graph per step: copy in, call, copy out, in order"},
-            "eager": {"value": round(by["active"] * world / (e2e_eager_ms * 1e-3), 1),
-                      "ms_per_step": round(e2e_eager_ms, 6)}}
+            "eager": {"value": rate(e2e_eager_ms), "ms_per_step": round(e2e_eager_ms, 6)}}
 
 
 SPEC_HBM_GBS = 8000.0  # HBM3e specification of a GB300 (about 8 TB/s)

@@ -119,6 +119,7 @@ typedef uint16_t vh_e16;   /* a 16-bit element: bf16, or fp16 under VH_FLAG_FP16
 #define VH_FLAG_PDL_KV 8u   /* VH_FLAG_PDL, and the cached K/V may be requested before the wait (vh_decode_fused) */
 #define VH_FLAG_PLANNED 16u /* the workspace holds this step's plan from vh_decode_plan (vh_decode_fused, vh_paged_decode_attn) */
 #define VH_FLAG_PLAN_THREE_CALL 32u /* vh_decode_plan: plan for vh_paged_decode_attn instead of vh_decode_fused */
+#define VH_FLAG_HOST_IO 64u /* vh_decode_fused: the per-step inputs and out may be pinned host memory, read and written in place */
 
 /* Fill the RoPE table used by vh_rope_kv_append.  Source: "Engineering TTS
  * inference in vLLM-Omni", Qwen3-TTS section 4 (RoPE cos/sin kept in fp32).
@@ -275,6 +276,16 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
  *     this workspace, instead of deriving it from the lengths;
  *   - the workspace also holds that per-step plan: vh_decode_plan writes a
  *     region of it that this call only reads (and only with VH_FLAG_PLANNED).
+ *   - VH_FLAG_HOST_IO: q, k_new, v_new, positions, seq_lens, active,
+ *     page_table and out may be pinned host memory that the device reaches
+ *     directly (on GB300, over the NVLink-C2C link to the Grace CPU): the
+ *     kernel reads the step's inputs and writes its output in place, so a
+ *     serving loop needs no separate host<->device copies and no copy-to-kernel
+ *     dependencies in its graphs.  q rows are then loaded with plain loads
+ *     (the other inputs always are); cos_sin, the caches, the norm weights,
+ *     err_flag and the workspace stay in device memory.  The caller keeps
+ *     the host buffers unchanged until the launch has completed (double
+ *     buffering across steps), as for any asynchronous read.
  * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,
  * VH_ENODEV, VH_ECUDA. */
 int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,

@@ -34,7 +34,7 @@ VH_OK, VH_EINVAL, VH_EALIGN, VH_EWORKSPACE, VH_ECUDA, VH_ENODEV = 0, -1, -2, -3,
 VH_ESCRATCH = -6
 VH_ERR_SEQLEN, VH_ERR_PAGE, VH_ERR_POS, VH_ERR_TIMEOUT = 1, 2, 4, 8
 VH_FLAG_PDL, VH_FLAG_FP16, VH_FLAG_ROPE_INTERLEAVED, VH_FLAG_PDL_KV = 1, 2, 4, 8
-VH_FLAG_PLANNED, VH_FLAG_PLAN_THREE_CALL = 16, 32
+VH_FLAG_PLANNED, VH_FLAG_PLAN_THREE_CALL, VH_FLAG_HOST_IO = 16, 32, 64
 ELEM_DTYPES = (torch.bfloat16, torch.float16)
 
 
@@ -112,6 +112,20 @@ def _contig(t: torch.Tensor, dtype, name: str) -> ctypes.c_void_p:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return _ptr(t, dtype, name)
+
+
+def _io(t: torch.Tensor, dtype, name: str, host_io: bool) -> ctypes.c_void_p:
+    """Pointer of a per-step input or output: a CUDA tensor, or with host_io a
+    pinned CPU tensor, which the device reads or writes in place."""
+    if host_io and t is not None and t.device.type == "cpu":
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be pinned host memory (or a CUDA tensor)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        return ctypes.c_void_p(t.data_ptr())
+    return _contig(t, dtype, name)
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -263,29 +277,37 @@ def vh_decode_fused(q, k_new, v_new, cos_sin, k_cache, v_cache, page_table, seq_
                     workspace, positions=None, sm_scale: float = 0.0, num_ctas: int = 0, err_flag=None,
                     pdl: bool = False, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
                     interleaved: bool = False, pdl_kv: bool = False, planned: bool = False,
-                    stream=None) -> torch.Tensor:
+                    host_io: bool = False, stream=None) -> torch.Tensor:
     """One whole decode step in one launch (RoPE, append, attention, merge).
     `workspace` must be zero-filled before its first use (alloc_workspace does that).
     pdl=True sets VH_FLAG_PDL, pdl_kv=True VH_FLAG_PDL_KV (see include/vh.h for
     when each is allowed); planned=True (VH_FLAG_PLANNED) takes the work list
-    from the plan vh_decode_plan wrote into `workspace`."""
+    from the plan vh_decode_plan wrote into `workspace`; host_io=True
+    (VH_FLAG_HOST_IO) lets q, k_new, v_new, positions, seq_lens, active,
+    page_table and out be pinned CPU tensors that the kernel reads and writes
+    in place."""
     B, Hq, D = q.shape
     kp, vp, ps, ts, hs, NP, P, Hkv, Dc = _cache_view(k_cache, v_cache)
     et = k_cache.dtype
     if Dc != D or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or out.shape != (B, Hq, D):
         raise ValueError("shape mismatch between q, k_new, v_new, out and the cache")
+    h = host_io
+    if page_table is None:
+        pt, mps = _table(None, B, NP)
+    else:
+        pt, mps = _io(page_table, torch.int32, "page_table", h), page_table.shape[1]
     _check(lib.vh_decode_fused(
-        _contig(q, et, "q"), _contig(k_new, et, "k_new"),
-        _contig(v_new, et, "v_new"), _contig(cos_sin, torch.float32, "cos_sin"),
-        cos_sin.shape[0], None if positions is None else _contig(positions, torch.int32, "positions"),
+        _io(q, et, "q", h), _io(k_new, et, "k_new", h),
+        _io(v_new, et, "v_new", h), _contig(cos_sin, torch.float32, "cos_sin"),
+        cos_sin.shape[0], None if positions is None else _io(positions, torch.int32, "positions", h),
         _norm_w(q_norm_w, D, "q_norm_w"), _norm_w(k_norm_w, D, "k_norm_w"), float(norm_eps),
-        kp, vp, ps, ts, hs, NP, *_table(page_table, B, NP),
-        _contig(seq_lens, torch.int32, "seq_lens"), _contig(active, torch.int32, "active"),
-        _contig(out, et, "out"), float(sm_scale), int(num_ctas),
+        kp, vp, ps, ts, hs, NP, pt, mps,
+        _io(seq_lens, torch.int32, "seq_lens", h), _io(active, torch.int32, "active", h),
+        _io(out, et, "out", h), float(sm_scale), int(num_ctas),
         _contig(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         None if err_flag is None else _contig(err_flag, torch.int32, "err_flag"),
         (VH_FLAG_PDL if pdl else 0) | (VH_FLAG_PDL_KV if pdl_kv else 0) | _elem_flags(k_cache, interleaved)
-        | (VH_FLAG_PLANNED if planned else 0), B, Hq, Hkv, D, P,
+        | (VH_FLAG_PLANNED if planned else 0) | (VH_FLAG_HOST_IO if host_io else 0), B, Hq, Hkv, D, P,
         _stream(stream)), "vh_decode_fused")
     return out
 

@@ -287,7 +287,8 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
                     void* workspace, size_t workspace_bytes, int32_t* err_flag, unsigned flags,
                     int B, int Hq, int Hkv, int D, int page_size, void* stream) {
   if (!q || !k_new || !v_new || !cos_sin || !k_cache || !v_cache || !seq_lens || !active || !out ||
-      (flags & ~(VH_FLAG_PDL | VH_FLAG_PDL_KV | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED | VH_FLAG_PLANNED)) != 0 ||
+      (flags & ~(VH_FLAG_PDL | VH_FLAG_PDL_KV | VH_FLAG_FP16 | VH_FLAG_ROPE_INTERLEAVED | VH_FLAG_PLANNED |
+                 VH_FLAG_HOST_IO)) != 0 ||
       !valid_paging(page_size, max_pages_per_seq) || !valid_table(page_table, B, max_pages_per_seq, num_pages))
     return VH_EINVAL;
   if (!valid_shape(B, Hq, Hkv, D, page_size) || max_pos < 1 || num_pages < 1 || max_pages_per_seq < 1 ||
@@ -346,6 +347,10 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_kv = (flags & VH_FLAG_PDL_KV) != 0;
+  if (flags & VH_FLAG_HOST_IO) {
+    p.host_io = 1;
+    p.q_tx_bytes = D * 4;  // only the RoPE row arrives by bulk copy
+  }
   // with the first stages requested before the wait (launches without it measured slower)
   p.l2_tiles = p.prefetch_kv ? vh::l2_prefetch_tiles() : 0;
   return vh::launch_decode_attn(p, static_cast<cudaStream_t>(stream),

@@ -106,6 +106,7 @@ struct AttnParams {
   int min_tiles;               // lower bound on tiles per CTA when the work list is short
   int prefetch_kv;             // fused: request the first stages of cached K/V before the dependency wait
   int early_q;                 // thread 0 requests the first segment's q rows right after the wait
+  int host_io;                 // fused: q is host memory read in place (plain loads; the RoPE row is still copied)
   int l2_tiles;                // tiles after the first `stages` prefetched into L2 right after the wait
   int stage_bytes;             // K then V of one tile: [D/64][Hc][16 tokens][128 B swizzled] each
   int q_bytes;                 // bytes reserved for the q staging buffer

@@ -74,6 +74,7 @@ def attn(**over):
     (dict(flags=v.VH_FLAG_ROPE_INTERLEAVED), v.VH_EINVAL),    # nor this one (no RoPE here)
     (dict(flags=8), v.VH_EINVAL),
     (dict(flags=v.VH_FLAG_PLAN_THREE_CALL), v.VH_EINVAL),    # a flag of vh_decode_plan only
+    (dict(flags=v.VH_FLAG_HOST_IO), v.VH_EINVAL),            # a flag of vh_decode_fused only
     (dict(flags=v.VH_FLAG_PLANNED, ws=None), v.VH_EWORKSPACE),  # the plan lives in the workspace
     (dict(flags=v.VH_FLAG_FP16, q_rot=ODD), v.VH_EALIGN),     # fp16 passes the flag check
 ])
@@ -132,8 +133,9 @@ def test_fused_argument_checks():
                  None)
 
     assert call(q=None) == v.VH_EINVAL
-    assert call(flags=64) == v.VH_EINVAL           # unknown flag
+    assert call(flags=128) == v.VH_EINVAL          # unknown flag
     assert call(flags=v.VH_FLAG_PLAN_THREE_CALL) == v.VH_EINVAL   # a flag of vh_decode_plan only
+    assert call(flags=v.VH_FLAG_HOST_IO, q=ODD) == v.VH_EALIGN    # host I/O passes the flag check
     assert call(flags=v.VH_FLAG_PDL_KV, out=ODD) == v.VH_EALIGN
     assert call(flags=v.VH_FLAG_PDL | v.VH_FLAG_FP16 | v.VH_FLAG_ROPE_INTERLEAVED, out=ODD) == v.VH_EALIGN
     assert call(Hq=24) == v.VH_EINVAL
