@@ -275,8 +275,9 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
  *     row arrays, first page ids) from the plan vh_decode_plan wrote into
  *     this workspace, instead of deriving it from the lengths;
  *   - the workspace also holds that per-step plan: vh_decode_plan writes a
- *     region of it that this call only reads (and only with VH_FLAG_PLANNED).
- *   - VH_FLAG_HOST_IO: q, k_new, v_new, positions, seq_lens, active,
+ *     region of it that this call only reads (and only with VH_FLAG_PLANNED);
+ *   - VH_FLAG_HOST_IO (the pages have no counterpart: their runtime stages
+ *     the step's inputs in device buffers): q, k_new, v_new, positions, seq_lens, active,
  *     page_table and out may be pinned host memory that the device reaches
  *     directly (on GB300, over the NVLink-C2C link to the Grace CPU): the
  *     kernel reads the step's inputs and writes its output in place, so a
