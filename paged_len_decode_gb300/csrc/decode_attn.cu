@@ -98,14 +98,21 @@ __device__ __forceinline__ int tile_page_id(const int32_t* page_table, int mps, 
   return page_table ? page_table[lp] : static_cast<int>(lp);
 }
 
-// One warp copies `bytes` (a multiple of 16) from global memory to shared
-// memory with plain 16-byte loads: the path for q rows that live in host
-// memory the device reads in place (VH_FLAG_HOST_IO), which the bulk copy
-// engine is not used on.
-__device__ __forceinline__ void warp_copy_g2s(unsigned char* dst, const void* src, int bytes, int lane) {
-  const uint4* s4 = static_cast<const uint4*>(src);
+// One warp stages a segment's q rows (`bytes`, a multiple of 16) that live in
+// host memory the device reads in place (VH_FLAG_HOST_IO) with plain 16-byte
+// loads, then lane 0 requests the RoPE row (device memory) with a bulk copy
+// whose bytes complete the phase of `bar`.  Kept out of line: the common
+// path (q in device memory, bulk copies) keeps its code as it was.
+__device__ __noinline__ void stage_q_host(unsigned char* dst, const uint16_t* src, int bytes, uint32_t rope_dst,
+                                          const float* rope_src, int rope_bytes, uint32_t bar, int lane) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   for (int i = lane; i < bytes / 16; i += 32) d4[i] = s4[i];
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rope_bytes));
+    bulk_g2s(rope_dst, rope_src, static_cast<uint32_t>(rope_bytes), bar);
+  }
 }
 
 // In-place inclusive prefix sum of cum[1..n] (cum[0] = 0 already).
@@ -623,13 +630,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
     // q in host memory: consumer warp 0 loads the first segment's rows itself
     if (early_q && warp == 0) {
       const long long qrow = static_cast<long long>(b0_pre) * p.Hq + static_cast<long long>(h0) * G;
-      warp_copy_g2s(smem + p.q_off, p.q + qrow * D, HG * D * 2, lane);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));  // the RoPE row's bytes
-        bulk_g2s(smem_addr(smem + p.q_off) + HG * p.q_row_bytes,
-                 p.cos_sin + static_cast<long long>(posv[b0_pre]) * D, D * 4, qfull);
-      }
+      stage_q_host(smem + p.q_off, p.q + qrow * D, HG * D * 2, smem_addr(smem + p.q_off) + HG * p.q_row_bytes,
+                   p.cos_sin + static_cast<long long>(posv[b0_pre]) * D, p.q_tx_bytes, qfull, lane);
     }
   } else if (early_q && tid == 0) {
     mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));
@@ -770,13 +772,8 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
         if (FUSED && p.host_io && !(nseg == 0 && early_q)) {
           // q in host memory: the producer loads the rows itself (plain loads)
           const long long qrow = static_cast<long long>(b) * p.Hq + static_cast<long long>(h0) * G;
-          warp_copy_g2s(smem + p.q_off, p.q + qrow * D, HG * D * 2, lane);
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));  // the RoPE row's bytes
-            bulk_g2s(smem_addr(smem + p.q_off) + HG * p.q_row_bytes,
-                     p.cos_sin + static_cast<long long>(posv[b]) * D, D * 4, qfull);
-          }
+          stage_q_host(smem + p.q_off, p.q + qrow * D, HG * D * 2, smem_addr(smem + p.q_off) + HG * p.q_row_bytes,
+                       p.cos_sin + static_cast<long long>(posv[b]) * D, p.q_tx_bytes, qfull, lane);
         } else if (lane == 0 && !(nseg == 0 && early_q)) {
           // the q rows of the segment's row (one contiguous copy) and, fused, the RoPE row
           mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));
