@@ -26,6 +26,22 @@ def test_step_bytes_by_hand():
     per_row = 4 * 64 * 2 + 2 * 2 * 64 * 2 + 2 * 2 * 64 * 2 + 4 * 64 * 2
     assert by["step"] == kv + 2 * per_row + pt + 8 * 3
     assert by["attn"] == kv + 2 * (4 * 64 * 4 + 4 * 64 * 2) + pt + 8 * 3
+    assert by["flops"] == 4 * 4 * 64 * (17 + 40)     # q.K and p.V: 2 flops per element each, active rows only
+
+
+def test_oracle_accuracy_check_flags_a_wrong_output():
+    import oracle
+    inp = workloads.make_case(B=3, Hq=4, Hkv=2, D=64, P=16, seq_lens=[17, 1, 40], active=[1, 0, 1], seed=3)
+    ref = oracle.reference_step(inp)["out"]
+    ok = bench.oracle_accuracy(inp, ref.clone(), {})
+    assert ok["within_tolerance"] and ok["max_abs_err"] == 0.0 and ok["worst_margin"] < 0
+    bad = ref.clone()
+    bad[2, 3, 5] += 0.05                              # an active row, far outside 2e-3 + 1e-2 |ref|
+    got = bench.oracle_accuracy(inp, bad, {})
+    assert not got["within_tolerance"] and abs(got["max_abs_err"] - 0.05) < 1e-2
+    junk = ref.clone()
+    junk[1] = float("nan")                            # the padding row is not compared
+    assert bench.oracle_accuracy(inp, junk, {})["within_tolerance"]
 
 
 def _free_port():
@@ -106,3 +122,6 @@ def test_rates_fractions_of_measured_peak_and_specification():
     assert r["frac_of_spec"] == round(6000.0 / bench.SPEC_HBM_GBS, 4)
     assert r["tokens_per_s"] == 64 * 2 / 1e-6                        # whole job: both ranks
     assert r["ms_per_launch"] == 0.00025
+    assert "tflops" not in r
+    r = bench.rates({**by, "flops": 2_000_000}, ms_step=0.001, world=1, peak=6000.0, L=1)
+    assert r["tflops"] == 2.0                                         # 2 MFLOP in 1 us
