@@ -684,12 +684,84 @@ def measure_workload(name, args, rank, world, dev, stream, *, headline: bool):
                       {"value": None, "unit": "tokens/s", "note": "measured for single-layer steps only"})
         if s.L == 1:
             res["l2_hot"] = l2_hot_measure(s, by, K, args, world, stream, pdl)
+            res["stack"] = stack_measure(s, by, K, args, world, stream, peak)
         res["_setup"] = s
         res["_by"] = by
     else:
         del s
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
+    return res
+
+
+def stack_measure(s, by, K, args, world, stream, peak):
+    """The fused step inside a layer stack: each step first runs a stand-in
+    QKV projection (three cuBLAS GEMMs from a hidden state of Hq*D to q, k_new
+    and v_new, weight replicas cycled beyond 4x L2 as a stack's per-layer
+    weights would be), then the fused step reads the projections' outputs.
+    The attention's cost in the stack is the step time minus that of the
+    same GEMMs alone, with programmatic dependent launch on the GEMMs (the
+    cached K/V requested before the wait), without it, and with PDL and the
+    per-step plan (one vh_decode_plan per PLAN_LAYERS layer calls)."""
+    dev, et = s.out.device, s.out.dtype
+    hidden = s.Hq * s.D
+    wbytes = hidden * (s.Hq + 2 * s.Hkv) * s.D * 2
+    n_w = max(2, math.ceil(4 * s.l2 / wbytes))
+    g = torch.Generator(device="cpu").manual_seed(20260777)
+    x = (torch.randn(s.B, hidden, generator=g) * 0.5).to(dev, et)
+    ws = [[(torch.randn(hidden, n * s.D, generator=g) * hidden ** -0.5).to(dev, et)
+           for n in (s.Hq, s.Hkv, s.Hkv)] for _ in range(n_w)]
+    q = torch.empty(s.B, s.Hq, s.D, dtype=et, device=dev)
+    k_new = torch.empty(s.B, s.Hkv, s.D, dtype=et, device=dev)
+    v_new = torch.empty_like(k_new)
+    src = workloads.DecodeInputs(**{**{k: getattr(s.inp, k) for k in (
+        "B", "Hq", "Hkv", "D", "P", "max_pages_per_seq", "num_pages", "theta", "pool", "layout", "page_table",
+        "seq_lens", "active")}, "q": q, "k_new": k_new, "v_new": v_new})
+
+    def proj(i):
+        wq, wk, wv = ws[i % n_w]
+        torch.matmul(x, wq, out=q.view(s.B, -1))
+        torch.matmul(x, wk, out=k_new.view(s.B, -1))
+        torch.matmul(x, wv, out=v_new.view(s.B, -1))
+
+    def graph(with_attn, pdl, planned=False):
+        proj(0)
+        if planned:
+            s.plan(0)
+        if with_attn:
+            s.fused(0, pdl=False, src=src, planned=planned)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(K):
+                    if planned and i % PLAN_LAYERS == 0:
+                        s.plan(i % s.R)  # the step's work list, once per PLAN_LAYERS layer calls
+                    proj(i)
+                    if with_attn:
+                        s.fused(i % s.R, pdl=pdl, src=src, planned=planned)
+        torch.cuda.current_stream().wait_stream(stream)
+        return [gr]
+
+    out = {}
+    pdl_kv, s.pdl_kv = s.pdl_kv, s.R > 1
+    for key, fn in (("gemm_only", lambda: graph(False, False)), ("with_attn_pdl", lambda: graph(True, True)),
+                    ("with_attn_no_pdl", lambda: graph(True, False)),
+                    ("with_attn_planned_pdl", lambda: graph(True, True, planned=True))):
+        gr = fn()
+        out[key], _, _ = time_replays(gr, K, stream, world, args.replays, min(args.seconds, 0.5))
+        del gr
+    s.pdl_kv = pdl_kv
+    res = {"gemm_ms_per_step": round(out["gemm_only"], 6), "weight_replicas": n_w,
+           "note": "stand-in QKV projection (cuBLAS bf16 GEMMs, [B, Hq*D] x [Hq*D, (Hq+2*Hkv)*D], weights cycled "
+                   "beyond 4x L2) before every fused step; attention cost = step minus the GEMMs alone"}
+    for key, pl in (("pdl", "with_attn_pdl"), ("no_pdl", "with_attn_no_pdl"),
+                    ("planned_pdl", "with_attn_planned_pdl")):
+        attn = out[pl] - out["gemm_only"]
+        r = rates(by, attn, world, peak, s.L)
+        res[key] = {"step_ms": round(out[pl], 6), "attn_ms_per_step": r["ms_per_step"],
+                    "hbm_gbs": r["hbm_gbs"], "frac_of_peak": r["frac_of_peak"], "frac_of_spec": r["frac_of_spec"]}
     return res
 
 
@@ -806,6 +878,7 @@ def run_ours(args, rank, world):
         "planned_no_pdl": h.get("planned_no_pdl"),
         "three_call": h["three_call"],
         "l2_hot": h.get("l2_hot"),
+        "stack": h.get("stack"),
         "workloads": extra,
         "clocks": ck,
         "e2e": e2e,

@@ -210,8 +210,9 @@ size_t vh_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, i
  * flags: VH_FLAG_FP16 (cache and out are fp16) and VH_FLAG_PDL: launch as a
  *     programmatic dependent of the previous kernel on the stream (for
  *     instance vh_rope_kv_append): lengths, flags and page ids are read before
- *     that kernel has completed and must not be written by it; q_rot and the
- *     cache are read after.  VH_FLAG_PLANNED: take the work list from the
+ *     that kernel has completed and must not be written by it (nor by an
+ *     earlier kernel still running because that one let it start early);
+ *     q_rot and the cache are read after.  VH_FLAG_PLANNED: take the work list from the
  *     plan vh_decode_plan (with VH_FLAG_PLAN_THREE_CALL) wrote into this
  *     workspace for the same lengths, flags, page table, shape and num_ctas
  *     (see vh_decode_plan).
@@ -261,11 +262,15 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
  *     vh_rope_kv_append, and VH_FLAG_PDL to launch as a programmatic
  *     dependent of the previous kernel on the stream, so that this launch's start-up (reading
  *     seq_lens, active, positions and page_table, planning the split)
- *     overlaps the end of that kernel.  Only valid when the kernel launched
- *     immediately before on the same stream does not write seq_lens, active,
- *     positions or page_table (host copies in between are fine); everything
- *     else is read and written only after that kernel has completed.  The
- *     kernel itself always lets a following dependent launch start early.
+ *     overlaps the end of that kernel.  Only valid when no kernel that may
+ *     still run when this launch starts writes seq_lens, active, positions
+ *     or page_table: the kernel launched immediately before on the same
+ *     stream and, if that one is itself a programmatic dependent that lets
+ *     its dependents start early (as this library's attention kernels do),
+ *     the kernels before it, back to the last ordinary launch or copy (host
+ *     copies in between are fine); everything else is read and written only
+ *     after that kernel has completed.  The kernel itself always lets a
+ *     following dependent launch start early.
  *     VH_FLAG_PDL_KV implies VH_FLAG_PDL and also requests the first tiles
  *     of the cached keys and values before that kernel has completed: valid
  *     only when it writes none of the cache pages this call reads (for
@@ -315,9 +320,11 @@ int vh_decode_fused(const vh_e16* q, const vh_e16* k_new, const vh_e16* v_new,
  * padding, as vh_decode_fused does).  max_pos is ignored with
  * VH_FLAG_PLAN_THREE_CALL.
  * Ordering: this kernel is an ordinary launch (it waits for all earlier work
- * on the stream) that lets no later kernel start before it completes, so
- * every later launch on the stream, programmatic dependents included, may
- * read the plan before its own dependency wait.  Call it again whenever
+ * on the stream) that lets no later kernel start before all of its CTAs
+ * have exited, and each of its threads makes its plan writes visible at GPU
+ * scope (a fence) before exiting, so every later launch on the stream,
+ * programmatic dependents included, may read the plan before its own
+ * dependency wait.  Call it again whenever
  * seq_lens, active, positions or page_table change (normally once per decode
  * step, after they are written and before the step's first attention
  * launch); a planned launch whose shape, num_ctas or path does not match the

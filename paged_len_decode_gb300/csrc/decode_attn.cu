@@ -1283,9 +1283,11 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
 // arithmetic (tile counts, prefix sum, equal ranges) and writes its record:
 // tile range, first and last row, and the page ids of the range's first
 // kPlanWindow tiles; CTA 0 also writes the header and the per-row arrays.
-// The kernel never releases its dependents early, so every kernel after it
-// on the stream starts after it has completed and may read the plan before
-// its own dependency wait.
+// The kernel never releases its dependents early, and every thread ends with
+// a GPU-scope fence after its last plan write, so by the time the last CTA
+// has exited (when a programmatic dependent may start) the whole plan is
+// visible: every kernel after it on the stream may read the plan before its
+// own dependency wait.
 __global__ void __launch_bounds__(256) decode_plan_kernel(const PlanParams p) {
   extern __shared__ int plan_smem[];  // warp totals [32], then cum [B + 1] (all shared memory is dynamic)
   int* warp_tot = plan_smem;
@@ -1354,6 +1356,9 @@ __global__ void __launch_bounds__(256) decode_plan_kernel(const PlanParams p) {
       reinterpret_cast<int4*>(p.hdr)[1] = make_int4(n_eff, p.fused, p.max_pages_per_seq, p.P);
     }
   }
+  // the plan's writes are performed at GPU scope before this thread exits
+  // (a dependent's reads before its own wait are ordered only by this)
+  __threadfence();
 }
 
 // Three-call path: one CTA per (row, kv-head group), one warp per kv head of

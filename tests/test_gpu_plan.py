@@ -7,7 +7,9 @@ high-concurrency step (programmatic dependent launches between them, as a
 model runs them), plans that do not match the launch (another CTA count,
 the other path, none written) being ignored, and the data-error flags the
 plan raises, and the benchmark's chain (one plan, then layer launches
-linked by programmatic dependent launch) captured in a CUDA graph.  Pages of
+linked by programmatic dependent launch) captured in a CUDA graph, and
+plans that change from step to step read by the programmatic dependent
+launched right after each plan.  Pages of
 8 tokens (every 16-token tile spans two pages) are checked on both paths,
 both page layouts, with and without a plan.
 """
@@ -216,6 +218,65 @@ def test_plan_and_layer_chain_captured_in_a_graph():
             cpu = li.to("cpu")
             H.check_out(cpu, refs[l]["out"], outs[l].cpu())
             H.check_append(cpu, refs[l], li.pool.cpu())  # (uses the lengths, flags and page table only)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_alternating_plans_read_by_programmatic_dependents(graph):
+    # every step writes a new plan (other lengths, flags and page table, same
+    # shape) and the fused launch right after it is its programmatic
+    # dependent, which reads the plan before its own wait (with its first K/V
+    # tiles requested there too): a plan not yet visible would put the other
+    # step's tile ranges and page ids on this step's cache
+    v = H.vh()
+    steps = [case([700, 1, 300, 1200, 64, 900, 17, 450], active=[1, 1, 1, 1, 0, 1, 1, 1], Hq=16, Hkv=8,
+                  seed=71, mps=80),
+             case([33, 1100, 1, 512, 980, 5, 640, 256], active=[1, 1, 0, 1, 1, 1, 1, 1], Hq=16, Hkv=8,
+                  seed=72, mps=80)]
+    refs = [oracle.reference_step(st.to("cpu")) for st in steps]
+    B, Hq, Hkv, D, P = 8, 16, 8, 128, 16
+    cos_sin = torch.empty((80 * P, D), dtype=torch.float32, device="cuda")
+    v.vh_rope_table(cos_sin, steps[0].theta)
+    ws = v.alloc_workspace(B, Hq, Hkv, D, P, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in steps]
+    pools0 = [st.pool.clone() for st in steps]
+
+    def run(order):
+        for i in order:
+            st = steps[i]
+            v.vh_decode_plan(st.seq_lens, st.active, st.page_table, ws, Hq=Hq, Hkv=Hkv, D=D, page_size=P,
+                             num_pages=st.num_pages, max_pos=cos_sin.shape[0], err_flag=err)
+            v.vh_decode_fused(st.q, st.k_new, st.v_new, cos_sin, st.pool[:, 0], st.pool[:, 1], st.page_table,
+                              st.seq_lens, st.active, outs[i], ws, err_flag=err, pdl=True, pdl_kv=True,
+                              planned=True)
+
+    def check():
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for i, st in enumerate(steps):
+            cpu = st.to("cpu")
+            H.check_out(cpu, refs[i]["out"], outs[i].cpu())
+            H.check_append(cpu, refs[i], st.pool.cpu())
+
+    if not graph:
+        run([0, 1, 0, 1, 1, 0])  # appends rewrite the same slots with the same values
+        check()
+        return
+    run([0, 1])  # first calls outside the capture
+    torch.cuda.synchronize()
+    cg = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(cg, stream=s):
+            run([0, 1, 1, 0, 1])
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for i, st in enumerate(steps):
+            st.pool.copy_(pools0[i])
+            outs[i].fill_(float("nan"))
+        cg.replay()
+        check()
 
 
 @pytest.mark.parametrize("path", H.PATHS)
