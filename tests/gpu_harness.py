@@ -33,13 +33,16 @@ PATHS = ("three", "fused")
 
 
 def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max_pos=None, graph=False,
-             repeat=1, pdl=False, norm=None, interleaved=False, pdl_kv=False, planned=False):
+             repeat=1, pdl=False, norm=None, interleaved=False, pdl_kv=False, planned=False, host_io=False):
     """Run one decode step on `inp` (CPU or CUDA DecodeInputs) through the C interface.
 
     path "three": vh_rope_kv_append + vh_paged_decode_attn + vh_decode_combine;
     path "fused": vh_decode_fused (one launch; q_rot is not produced).
     planned: vh_decode_plan once, then the attention launches take their
     work list from it (all `repeat` calls share the one plan).
+    host_io (fused path): q, k_new, v_new, the lengths, flags, positions,
+    page table and the output are pinned host memory the kernel reads and
+    writes in place (VH_FLAG_HOST_IO).
     Returns dict(q_rot, out, pool_after, err) on the CPU (pool_after token-major);
     `inp` is not modified.
     """
@@ -69,15 +72,22 @@ def run_step(inp, *, path="three", num_ctas=0, positions=None, sm_scale=0.0, max
                          max_pos=max_pos, num_ctas=num_ctas, err_flag=err, fp16=g.pool.dtype == torch.float16,
                          three_call=path != "fused")
 
+    fin = {"q": g.q, "k_new": g.k_new, "v_new": g.v_new, "pt": g.api_page_table, "lens": g.seq_lens,
+           "act": g.active, "pos": pos}
+    if host_io:
+        assert path == "fused"
+        fin = {k: None if t is None else t.cpu().contiguous().pin_memory() for k, t in fin.items()}
+        out = out.cpu().pin_memory()
+
     def step():
         if planned:
             plan()
         for _ in range(repeat):
             if path == "fused":
-                v.vh_decode_fused(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.api_page_table, g.seq_lens,
-                                  g.active, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
-                                  err_flag=err, pdl=pdl, q_norm_w=nq, k_norm_w=nk, norm_eps=eps,
-                                  interleaved=interleaved, pdl_kv=pdl_kv, planned=planned)
+                v.vh_decode_fused(fin["q"], fin["k_new"], fin["v_new"], cos_sin, k_cache, v_cache, fin["pt"],
+                                  fin["lens"], fin["act"], out, ws, positions=fin["pos"], sm_scale=sm_scale,
+                                  num_ctas=num_ctas, err_flag=err, pdl=pdl, q_norm_w=nq, k_norm_w=nk, norm_eps=eps,
+                                  interleaved=interleaved, pdl_kv=pdl_kv, planned=planned, host_io=host_io)
             else:
                 v.decode_step(g.q, g.k_new, g.v_new, cos_sin, k_cache, v_cache, g.api_page_table, g.seq_lens,
                               g.active, q_rot, out, ws, positions=pos, sm_scale=sm_scale, num_ctas=num_ctas,
@@ -220,7 +230,8 @@ def check_q_rot(inp, ref_q_rot, gpu_q_rot):
 
 
 def full_check(inp, *, path="three", num_ctas=0, rows=None, positions=None, sm_scale=0.0, graph=False,
-               max_pos=None, repeat=1, pdl=False, norm=None, interleaved=False, pdl_kv=False, planned=False):
+               max_pos=None, repeat=1, pdl=False, norm=None, interleaved=False, pdl_kv=False, planned=False,
+               host_io=False):
     """Run the GPU path and the oracle on `inp`; check q_rot (three-call path),
     the append bits and the output.  norm: dict(q, k, eps) of RMSNorm weights.
     The element type (bf16 / fp16) and page layout are those of inp; the oracle
@@ -231,7 +242,7 @@ def full_check(inp, *, path="three", num_ctas=0, rows=None, positions=None, sm_s
                                 **nk)
     got = run_step(inp, path=path, num_ctas=num_ctas, positions=positions, sm_scale=sm_scale, graph=graph,
                    max_pos=max_pos, repeat=repeat, pdl=pdl, norm=norm, interleaved=interleaved, pdl_kv=pdl_kv,
-                   planned=planned)
+                   planned=planned, host_io=host_io)
     assert got["err"] == 0, f"device error flag {got['err']}"
     exempt, n_diff = check_append(cpu, ref, got["pool_after"], MIDPOINT_REL if norm is None else MIDPOINT_REL_NORM,
                                   interleaved=interleaved)
