@@ -29,12 +29,15 @@
  *     [num_layers, num_pages, 2, page_size, num_kv_heads, head_dim].
  *
  * Conventions for every call:
- *   - All pointers are DEVICE pointers owned by the caller; the library
- *     allocates nothing, frees nothing and keeps no state between calls
- *     other than per-device launch settings it caches on first use.
+ *   - All pointers are DEVICE pointers owned by the caller (except the
+ *     step inputs and output that VH_FLAG_HOST_IO lets vh_decode_fused take
+ *     in pinned host memory); the library allocates nothing, frees nothing
+ *     and keeps no state between calls other than per-device launch settings
+ *     it caches on first use (and the fixed scratch array of
+ *     vh_paged_decode_attn_noalloc).
  *   - 16-bit values are passed as uint16_t bit patterns: vh_bf16 is always
  *     bf16; vh_e16 is bf16, or IEEE fp16 when the call's flags hold
- *     VH_FLAG_FP16 (the Fish kernel of the first source below takes either
+ *     VH_FLAG_FP16 (the Fish kernel of the first source above takes either
  *     type).  One call uses one type for all of its 16-bit arrays.
  *   - Strides are in ELEMENTS.  One layer's cache is reached through
  *     k_cache / v_cache plus page_stride (elements between pages),
@@ -47,8 +50,8 @@
  *     v_cache = k_cache + Hkv*P*D, page_stride = 2*Hkv*P*D, token_stride = D,
  *     head_stride = P*D.  All three strides must be multiples of 8 elements
  *     (16 bytes); the caller guarantees that distinct (page, slot, head)
- *     rows do not overlap.  Token-major pages move one copy per token row of
- *     a CTA's heads, head-major pages one copy per (token, head).
+ *     rows do not overlap.  Both layouts take the same path: the cache is
+ *     described to the copy engine as a 4-D tensor with these strides.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
  *   - Every call checks its scalar arguments and pointer alignment on the
  *     host, launches asynchronously and never synchronises or reads device
