@@ -87,7 +87,7 @@ def test_gqa_groups_and_head_dims(G, D, path):
 
 
 @pytest.mark.parametrize("path", H.PATHS)
-@pytest.mark.parametrize("P", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("P", [8, 16, 32, 64, 128, 256, 512, 1024])
 def test_page_sizes(P, path):
     H.full_check(case([1, P - 1, P, P + 1, 3 * P + 5], P=P, Hq=8, Hkv=4, seed=P), path=path)
 
@@ -267,6 +267,20 @@ def test_large_batch_of_short_rows(path):
     active = (torch.rand(2048, generator=g) > 0.1).to(torch.int64).tolist()
     lens = [L if a else 1 for L, a in zip(lens, active)]
     inp = workloads.make_case(B=2048, Hq=8, Hkv=4, D=128, P=16, seq_lens=lens, active=active, seed=18,
+                              device="cuda", max_pages_per_seq=3)
+    H.full_check(inp, path=path)
+
+
+@pytest.mark.parametrize("path", H.PATHS)
+def test_batch_near_the_shared_memory_limit(path):
+    # 12,000 rows: every CTA keeps 12 bytes per row (tile count, length,
+    # position) in shared memory, 144 KB here, next to its pipeline stages
+    g = torch.Generator().manual_seed(19)
+    B = 12000
+    lens = torch.randint(1, 41, (B,), generator=g).tolist()
+    active = (torch.rand(B, generator=g) > 0.1).to(torch.int64).tolist()
+    lens = [L if a else 1 for L, a in zip(lens, active)]
+    inp = workloads.make_case(B=B, Hq=4, Hkv=2, D=64, P=16, seq_lens=lens, active=active, seed=20,
                               device="cuda", max_pages_per_seq=3)
     H.full_check(inp, path=path)
 
