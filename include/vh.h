@@ -291,8 +291,11 @@ int vh_decode_combine(const void* workspace, size_t workspace_bytes, vh_e16* out
  *     kernel reads the step's inputs and writes its output in place, so a
  *     serving loop needs no separate host<->device copies and no copy-to-kernel
  *     dependencies in its graphs.  q rows are then loaded with plain loads
- *     (the other inputs always are); cos_sin, the caches, the norm weights,
- *     err_flag and the workspace stay in device memory.  The caller keeps
+ *     (the other inputs always are), and with VH_FLAG_PDL the first q rows
+ *     of each CTA are read before the wait on the previous kernel, like the
+ *     lengths, flags and page ids: that kernel must not write q (inputs the
+ *     host writes before the launch never are); cos_sin, the caches, the
+ *     norm weights, err_flag and the workspace stay in device memory.  The caller keeps
  *     the host buffers unchanged until the launch has completed (double
  *     buffering across steps), as for any asynchronous read.
  * Errors: VH_EINVAL (also for unknown flags), VH_EALIGN, VH_EWORKSPACE,

@@ -619,21 +619,24 @@ __global__ void __launch_bounds__(kThreadsMax, 1) decode_attn_kernel(const __gri
       ++npre;
     }
   }
+  // The first segment's q rows (and, fused, its RoPE row) are requested at
+  // once: the consumers cannot start before they arrive, and the producer may
+  // still be busy with the requests it makes before the wait (page ids, first
+  // stages).  Later segments' q rows come from the producer.  q in host
+  // memory (VH_FLAG_HOST_IO) is written by the host before the launch, never
+  // by the previous kernel, so consumer warp 0 loads those rows before the
+  // wait (end-to-end c64 step 29.43 -> 28.41 us in one A/B call); q in device
+  // memory may come from the previous kernel and is requested by thread 0 as
+  // soon as the wait returns.
+  const bool early_q = p.early_q && c < n_eff;
+  if (FUSED && p.host_io && early_q && warp == 0) {
+    const long long qrow = static_cast<long long>(b0_pre) * p.Hq + static_cast<long long>(h0) * G;
+    stage_q_host(smem + p.q_off, p.q + qrow * D, HG * D * 2, smem_addr(smem + p.q_off) + HG * p.q_row_bytes,
+                 p.cos_sin + static_cast<long long>(posv[b0_pre]) * D, p.q_tx_bytes, qfull, lane);
+  }
   pdl_wait();
 
-  // The first segment's q rows (and, fused, its RoPE row) are requested at
-  // once by thread 0: the consumers cannot start before they arrive, and the
-  // producer may still be busy with the requests it makes before the wait
-  // (page ids, first stages).  Later segments' q rows come from the producer.
-  const bool early_q = p.early_q && c < n_eff;
-  if (FUSED && p.host_io) {
-    // q in host memory: consumer warp 0 loads the first segment's rows itself
-    if (early_q && warp == 0) {
-      const long long qrow = static_cast<long long>(b0_pre) * p.Hq + static_cast<long long>(h0) * G;
-      stage_q_host(smem + p.q_off, p.q + qrow * D, HG * D * 2, smem_addr(smem + p.q_off) + HG * p.q_row_bytes,
-                   p.cos_sin + static_cast<long long>(posv[b0_pre]) * D, p.q_tx_bytes, qfull, lane);
-    }
-  } else if (early_q && tid == 0) {
+  if (!(FUSED && p.host_io) && early_q && tid == 0) {
     mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.q_tx_bytes));
     const long long qrow = static_cast<long long>(b0_pre) * p.Hq + static_cast<long long>(h0) * G;
     const uint32_t qdst = smem_addr(smem + p.q_off);
