@@ -165,6 +165,21 @@ def test_append_places_token_in_its_slot(L, page_idx, off):
         assert after_bits[page, 0, off, h].tolist() == [brute.bf16_round_bits(v) for v in kr]
 
 
+@pytest.mark.parametrize("L,page_idx,off", [(8, 0, 7), (9, 1, 0), (24, 2, 7), (25, 3, 0)])
+def test_append_places_token_in_its_slot_with_8_token_pages(L, page_idx, off):
+    inp = _small_case([L, 3], P=8)
+    _, after, bad = oracle.rope_kv_append(inp.q, inp.k_new, inp.v_new, inp.pool, inp.page_table,
+                                          inp.seq_lens, inp.active, P=inp.P, theta=inp.theta)
+    assert bad == 0
+    page = int(inp.page_table[0, page_idx])
+    changed = _bits(inp.pool) != _bits(after)
+    mask = torch.zeros_like(changed)
+    mask[page, :, off] = True
+    mask[int(inp.page_table[1, 0]), :, 2] = True
+    assert not (changed & ~mask).any()
+    assert torch.equal(_bits(after)[page, 1, off], _bits(inp.v_new[0]))
+
+
 def test_append_skips_padding_rows_and_bad_rows():
     inp = _small_case([9, 1, 7], active=[1, 0, 1])
     # row 2 claims a length beyond its page-table row
@@ -393,6 +408,7 @@ def _nested(t):
     dict(lens=[1, 16, 40], Hq=2, Hkv=1, D=16, P=16),
     dict(lens=[9, 30], Hq=6, Hkv=3, D=4, P=16),
     dict(lens=[70, 12], Hq=4, Hkv=2, D=8, P=64),
+    dict(lens=[17, 8, 9, 25], Hq=4, Hkv=2, D=8, P=8),   # 8-token pages: keys cross a page every 8 slots
 ])
 def test_oracle_matches_brute_force(shape):
     inp = _small_case(shape["lens"], Hq=shape["Hq"], Hkv=shape["Hkv"], D=shape["D"], P=shape["P"], seed=21)
